@@ -1,0 +1,30 @@
+"""Test configuration: the ``gpu`` marker and the shared fixtures.
+
+Tests marked ``gpu`` need a CUDA device and the compiled CUDA library; all
+others run on the CPU (the oracle's pins, host-side argument checks, the
+library's exported symbols, the multi-rank host logic over gloo).
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU and the compiled CUDA library")
+
+
+@pytest.fixture(scope="session")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+@pytest.fixture(scope="session")
+def golden_dir():
+    return os.path.join(ROOT, "tests", "golden")
