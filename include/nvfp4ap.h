@@ -1,0 +1,154 @@
+/*
+ * nvfp4ap.h -- C ABI of libnvfp4ap.so: GB300 (sm_103a) adaptive-LayerNorm
+ * activation producers (LayerNorm -> adaptive modulation -> FP8 e4m3fn or
+ * NVFP4) and the six-way fp32 -> bf16 modulation producer.
+ *
+ * Source of the operations: the "adaptive-layernorm-producers" README,
+ * sections "Available Functions" (the function list), "Tensor Contract"
+ * (shapes, dtypes, contiguity, dim rules) and "Minimal Usage" (static
+ * buffers for CUDA Graph capture, the table form, the NVFP4 pair).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major memory
+ *    owned by the caller.  The library never allocates, never frees, never
+ *    synchronises and never reads device memory on the host, so every call
+ *    can be captured in a CUDA graph with static buffers.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns (2 bytes), e4m3 tensors are
+ *    OCP float8_e4m3fn bytes, fp32 tensors are IEEE binary32.
+ *  - `stream` is the CUDA stream the kernel is launched on (NULL = legacy
+ *    default stream).  The call returns after the launch is queued.
+ *  - The return value is an NVFP4AP_* status.  Every argument is checked on
+ *    the host before anything is launched; on a non-zero status nothing has
+ *    been launched and no memory has been touched, except NVFP4AP_ERR_LAUNCH,
+ *    which reports the CUDA error of the launch itself.
+ *  - rows == 0 (or batch*seq == 0) is a valid no-op; pointers may then be NULL.
+ *  - Alignment: x, scale, shift, temb, table and the outputs take a 16-byte
+ *    vector path when every pointer is 16-byte aligned and dim is a multiple
+ *    of 8; the FP8 ops otherwise fall back to a 4-byte (bf16 pair) path that
+ *    needs 4-byte aligned bf16 inputs and 2-byte aligned outputs.  The NVFP4
+ *    ops need 16-byte aligned x/scale/shift and an 8-byte aligned `packed`.
+ *    A pointer that violates its op's rule gives NVFP4AP_ERR_ALIGN.
+ *  - dim must be at most NVFP4AP_MAX_DIM for the LayerNorm ops (a whole row
+ *    is held in registers); the six-way op has no such limit.
+ */
+#ifndef NVFP4AP_H
+#define NVFP4AP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4ap_stream_t; /* same type as cudaStream_t */
+
+enum nvfp4ap_status {
+  NVFP4AP_OK = 0,
+  NVFP4AP_ERR_NULL = 1,    /* a required pointer is NULL (with rows > 0)      */
+  NVFP4AP_ERR_SHAPE = 2,   /* negative rows/batch/seq, or dim <= 0           */
+  NVFP4AP_ERR_DIM = 3,     /* dim odd (FP8), not a multiple of 16 (NVFP4), or
+                              above NVFP4AP_MAX_DIM                          */
+  NVFP4AP_ERR_INDEX = 4,   /* chunks < 1 or shift_idx/scale_idx out of range */
+  NVFP4AP_ERR_ALIGN = 5,   /* a pointer misses its alignment rule            */
+  NVFP4AP_ERR_LAUNCH = 6,  /* the CUDA launch failed (cudaGetLastError)      */
+  NVFP4AP_ERR_VALUE = 7    /* eps negative or not finite                      */
+};
+
+#define NVFP4AP_MAX_DIM 32768
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4ap_status_string(int status);
+
+/* Version of this ABI (major*10000 + minor*100 + patch). */
+int nvfp4ap_version(void);
+
+/* ------------------------------------------------------------------------
+ * FP8 producers.  For each row r of x (rows, dim) bf16:
+ *   mean, var = biased mean and variance of the row; rstd = 1/sqrt(var+eps)
+ *   y[d] = (x[r,d] - mean) * rstd * (1 + scale[.]) + shift[.]
+ *   out[r,d] = e4m3fn(y[d] / act_scale)   round-to-nearest-even, saturating
+ *                                          to +-448 (e4m3fn has no inf)
+ * act_scale: device pointer to ONE fp32 (the dequantisation scale, so the
+ * output value is about out * act_scale).  eps: host float, >= 0.
+ * out: (rows, dim) e4m3fn bytes.  dim must be even.
+ * ---------------------------------------------------------------------- */
+
+/* README "Available Functions": ada_layer_norm_quant_fp8_bf16.
+ * scale, shift: (dim,) bf16, broadcast over rows. */
+int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
+                                  const float* act_scale, float eps, void* out,
+                                  int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions": ada_layer_norm_quant_fp8_ptok_bf16.
+ * scale, shift: (rows, dim) bf16, one row of modulation per token. */
+int ada_layer_norm_quant_fp8_ptok_bf16(const void* x, const void* scale, const void* shift,
+                                       const float* act_scale, float eps, void* out,
+                                       int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions" / "Minimal Usage" (fused host modulation table
+ * add and chunk selection): ada_layer_norm_quant_fp8_ptok_table_bf16.
+ * temb: (rows, chunks, dim) bf16; table: (chunks, dim) fp32;
+ *   scale[r,d] = temb[r, scale_idx, d] + table[scale_idx, d]
+ *   shift[r,d] = temb[r, shift_idx, d] + table[shift_idx, d]
+ * (the sums are taken in fp32 and are not rounded to bf16).
+ * 0 <= shift_idx, scale_idx < chunks, else NVFP4AP_ERR_INDEX. */
+int ada_layer_norm_quant_fp8_ptok_table_bf16(const void* x, const void* temb, const float* table,
+                                             int64_t chunks, int64_t shift_idx, int64_t scale_idx,
+                                             const float* act_scale, float eps, void* out,
+                                             int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions": layer_norm_no_affine_quant_fp8_static_bf16.
+ * No modulation: y = (x - mean) * rstd. */
+int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
+                                               void* out, int64_t rows, int64_t dim,
+                                               nvfp4ap_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * NVFP4 producers ("Tensor Contract": packed (rows, dim/2) uint8 and the
+ * 128x4 swizzled uint8 scale layout; "Validation": the staged BF16-norm plus
+ * FP4 quantizer contract).  For each row, y as above (no act_scale), then
+ *   v = bf16(y)                                  (round-to-nearest-even)
+ *   per 16-element block b: amax = max |v|, s = e4m3fn(amax / 6) (RNE,
+ *     saturating); code_k = e2m1 nearest of v_k / decode(s), ties to the
+ *     even code, saturating at 6, sign kept (a zero scale gives +-0 codes)
+ *   packed[r, 8b + j] = code_{16b+2j} | code_{16b+2j+1} << 4
+ *   sf_swizzled[off(r, b)] = s, with C4 = ceil(dim/16 / 4) and
+ *     off(r,b) = ((r/128)*C4 + b/4)*512 + (r%32)*16 + ((r%128)/32)*4 + b%4
+ *   and every padding byte of the swizzled buffer (rows up to a multiple of
+ *   128, block columns up to a multiple of 4) is written as 0.
+ * dim % 16 == 0.  packed: rows*dim/2 bytes; sf_swizzled:
+ * swizzled_sf_size(rows, dim) bytes.
+ * ---------------------------------------------------------------------- */
+
+/* README "Available Functions": ada_layer_norm_quant_nvfp4_swizzled_bf16.
+ * scale, shift: (dim,) bf16 broadcast. */
+int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const void* scale, const void* shift,
+                                             float eps, void* packed, void* sf_swizzled,
+                                             int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions": layer_norm_no_affine_quant_nvfp4_swizzled_bf16. */
+int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,
+                                                   void* sf_swizzled, int64_t rows, int64_t dim,
+                                                   nvfp4ap_stream_t stream);
+
+/* README "Available Functions" / "Tensor Contract": swizzled_sf_size.
+ * Bytes of the swizzled scale buffer: ceil(rows/128)*128 * ceil(dim/16/4)*4.
+ * Returns -1 when rows < 0, dim <= 0 or dim % 16 != 0.  Host only. */
+int64_t swizzled_sf_size(int64_t rows, int64_t dim);
+
+/* ------------------------------------------------------------------------
+ * README "Available Functions" / "Tensor Contract": adaln_modulation6_bf16.
+ * params: (batch, seq, 6, dim) fp32; modulation: (6, dim) fp32;
+ * out[i]: six device pointers, each (batch, seq, dim) bf16:
+ *   out[i][b,s,d] = bf16( params[b,s,i,d] + modulation[i,d] )
+ * with one binary32 addition and round-to-nearest-even to bf16.
+ * `out` itself is a HOST array of six device pointers (read during the call).
+ * ---------------------------------------------------------------------- */
+int adaln_modulation6_bf16(const float* params, const float* modulation, void* const out[6],
+                           int64_t batch, int64_t seq, int64_t dim, nvfp4ap_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4AP_H */

@@ -1,0 +1,286 @@
+"""GB300 (sm_103a) adaptive-LayerNorm activation producers: Python binding.
+
+Thin ctypes binding of ``libnvfp4ap.so`` (C ABI in ``include/nvfp4ap.h``).
+The functions follow the adaptive-layernorm-producers README ("Available
+Functions", "Tensor Contract"): torch CUDA tensors in, outputs allocated when
+``out``/``packed``/``sf_swizzled`` are None, every launch on the current CUDA
+stream of the input's device.  This module only checks dtypes/shapes and
+passes pointers; all arithmetic runs in the library's CUDA kernels.  If the
+library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "ada_layer_norm_quant_fp8_bf16",
+    "ada_layer_norm_quant_fp8_ptok_bf16",
+    "ada_layer_norm_quant_fp8_ptok_table_bf16",
+    "layer_norm_no_affine_quant_fp8_static_bf16",
+    "ada_layer_norm_quant_nvfp4_swizzled_bf16",
+    "layer_norm_no_affine_quant_nvfp4_swizzled_bf16",
+    "adaln_modulation6_bf16",
+    "swizzled_sf_size",
+    "library_path",
+    "NvFp4ApError",
+]
+
+LIB_PATH = _build.LIB
+
+OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE = range(8)
+MAX_DIM = 32768
+
+
+class NvFp4ApError(RuntimeError):
+    """A non-zero status from the C ABI."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libnvfp4ap.so is not built ({LIB_PATH}); run "
+                           "nvfp4_activation_producer_gb300.build.build() or __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    L.nvfp4ap_status_string.restype = ctypes.c_char_p
+    L.nvfp4ap_status_string.argtypes = [i32]
+    L.nvfp4ap_version.restype = i32
+    L.nvfp4ap_version.argtypes = []
+    for name in ("ada_layer_norm_quant_fp8_bf16", "ada_layer_norm_quant_fp8_ptok_bf16"):
+        fn = getattr(L, name)
+        fn.restype = i32
+        fn.argtypes = [p, p, p, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_fp8_ptok_table_bf16.restype = i32
+    L.ada_layer_norm_quant_fp8_ptok_table_bf16.argtypes = [p, p, p, i64, i64, i64, p, f32, p, i64, i64, p]
+    L.layer_norm_no_affine_quant_fp8_static_bf16.restype = i32
+    L.layer_norm_no_affine_quant_fp8_static_bf16.argtypes = [p, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_nvfp4_swizzled_bf16.restype = i32
+    L.ada_layer_norm_quant_nvfp4_swizzled_bf16.argtypes = [p, p, p, f32, p, p, i64, i64, p]
+    L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16.restype = i32
+    L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16.argtypes = [p, f32, p, p, i64, i64, p]
+    L.swizzled_sf_size.restype = i64
+    L.swizzled_sf_size.argtypes = [i64, i64]
+    L.adaln_modulation6_bf16.restype = i32
+    L.adaln_modulation6_bf16.argtypes = [p, p, ctypes.POINTER(ctypes.c_void_p), i64, i64, i64, p]
+    _lib = L
+    return L
+
+
+def library_path() -> str:
+    _load()
+    return LIB_PATH
+
+
+def _raise(fn: str, rc: int):
+    if rc != OK:
+        msg = _load().nvfp4ap_status_string(rc).decode()
+        raise NvFp4ApError(fn, rc, msg)
+
+
+# ---------------------------------------------------------------------------
+# tensor-contract checks (README "Tensor Contract")
+# ---------------------------------------------------------------------------
+
+def _need(t: torch.Tensor, name: str, dtype, shape, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scalar(t: torch.Tensor, name: str, device):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or t.numel() != 1:
+        raise TypeError(f"{name} must be a CUDA float32 tensor with one element")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _x(x: torch.Tensor):
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a 2-D (rows, dim) tensor")
+    _need(x, "x", torch.bfloat16, x.shape)
+    return x.shape[0], x.shape[1], x.device
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _fp8_out(out, rows, dim, device):
+    if out is None:
+        return torch.empty((rows, dim), dtype=torch.float8_e4m3fn, device=device)
+    _need(out, "out", torch.float8_e4m3fn, (rows, dim), device)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 producers
+# ---------------------------------------------------------------------------
+
+def ada_layer_norm_quant_fp8_bf16(x, scale, shift, act_scale, eps: float = 1e-5, out=None):
+    """LayerNorm(x)*(1+scale)+shift -> e4m3fn(. / act_scale); scale/shift (dim,) bf16."""
+    rows, dim, dev = _x(x)
+    _need(scale, "scale", torch.bfloat16, (dim,), dev)
+    _need(shift, "shift", torch.bfloat16, (dim,), dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_fp8_bf16(_ptr(x), _ptr(scale), _ptr(shift), _ptr(act_scale), eps,
+                                               _ptr(out), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_fp8_bf16", rc)
+    return out
+
+
+def ada_layer_norm_quant_fp8_ptok_bf16(x, scale, shift, act_scale, eps: float = 1e-5, out=None):
+    """Per-token form: scale/shift (rows, dim) bf16."""
+    rows, dim, dev = _x(x)
+    _need(scale, "scale", torch.bfloat16, (rows, dim), dev)
+    _need(shift, "shift", torch.bfloat16, (rows, dim), dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_fp8_ptok_bf16(_ptr(x), _ptr(scale), _ptr(shift), _ptr(act_scale), eps,
+                                                    _ptr(out), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_fp8_ptok_bf16", rc)
+    return out
+
+
+def ada_layer_norm_quant_fp8_ptok_table_bf16(x, temb, table, act_scale, shift_idx: int, scale_idx: int,
+                                             eps: float = 1e-5, out=None):
+    """Table form: scale/shift = temb[:, idx, :] + table[idx, :]; temb (rows, chunks, dim) bf16,
+    table (chunks, dim) fp32."""
+    rows, dim, dev = _x(x)
+    if not isinstance(temb, torch.Tensor) or temb.dim() != 3:
+        raise ValueError("temb must be a 3-D (rows, chunks, dim) tensor")
+    chunks = temb.shape[1]
+    _need(temb, "temb", torch.bfloat16, (rows, chunks, dim), dev)
+    _need(table, "table", torch.float32, (chunks, dim), dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_fp8_ptok_table_bf16(_ptr(x), _ptr(temb), _ptr(table), chunks,
+                                                          int(shift_idx), int(scale_idx), _ptr(act_scale),
+                                                          eps, _ptr(out), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_fp8_ptok_table_bf16", rc)
+    return out
+
+
+def layer_norm_no_affine_quant_fp8_static_bf16(x, act_scale, eps: float = 1e-5, out=None):
+    """LayerNorm(x) (no affine) -> e4m3fn(. / act_scale)."""
+    rows, dim, dev = _x(x)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().layer_norm_no_affine_quant_fp8_static_bf16(_ptr(x), _ptr(act_scale), eps, _ptr(out), rows,
+                                                            dim, _stream(dev))
+    _raise("layer_norm_no_affine_quant_fp8_static_bf16", rc)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 producers
+# ---------------------------------------------------------------------------
+
+def swizzled_sf_size(rows: int, dim: int) -> int:
+    """Bytes of the 128x4-swizzled e4m3 scale buffer for a (rows, dim) activation."""
+    n = int(_load().swizzled_sf_size(int(rows), int(dim)))
+    if n < 0:
+        raise ValueError(f"swizzled_sf_size: invalid rows={rows}, dim={dim} (dim must be a positive multiple of 16)")
+    return n
+
+
+def _nvfp4_outs(packed, sf, rows, dim, dev):
+    if dim % 16 != 0:
+        raise ValueError("dim must be divisible by 16 for NVFP4 outputs")
+    if packed is None:
+        packed = torch.empty((rows, dim // 2), dtype=torch.uint8, device=dev)
+    else:
+        _need(packed, "packed", torch.uint8, (rows, dim // 2), dev)
+    n = swizzled_sf_size(rows, dim)
+    if sf is None:
+        sf = torch.empty((n,), dtype=torch.uint8, device=dev)
+    else:
+        if not isinstance(sf, torch.Tensor) or sf.dtype != torch.uint8 or not sf.is_cuda:
+            raise TypeError("sf_swizzled must be a CUDA uint8 tensor")
+        if sf.device != dev or not sf.is_contiguous() or sf.numel() != n:
+            raise ValueError(f"sf_swizzled must be a contiguous uint8 tensor of swizzled_sf_size = {n} elements")
+    return packed, sf
+
+
+def ada_layer_norm_quant_nvfp4_swizzled_bf16(x, scale, shift, eps: float = 1e-5, packed=None, sf_swizzled=None):
+    """LayerNorm(x)*(1+scale)+shift -> NVFP4 (packed e2m1, 128x4-swizzled e4m3 block scales)."""
+    rows, dim, dev = _x(x)
+    _need(scale, "scale", torch.bfloat16, (dim,), dev)
+    _need(shift, "shift", torch.bfloat16, (dim,), dev)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_nvfp4_swizzled_bf16(_ptr(x), _ptr(scale), _ptr(shift), eps, _ptr(packed),
+                                                          _ptr(sf_swizzled), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_nvfp4_swizzled_bf16", rc)
+    return packed, sf_swizzled
+
+
+def layer_norm_no_affine_quant_nvfp4_swizzled_bf16(x, eps: float = 1e-5, packed=None, sf_swizzled=None):
+    """LayerNorm(x) (no affine) -> NVFP4."""
+    rows, dim, dev = _x(x)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    rc = _load().layer_norm_no_affine_quant_nvfp4_swizzled_bf16(_ptr(x), eps, _ptr(packed), _ptr(sf_swizzled),
+                                                                rows, dim, _stream(dev))
+    _raise("layer_norm_no_affine_quant_nvfp4_swizzled_bf16", rc)
+    return packed, sf_swizzled
+
+
+# ---------------------------------------------------------------------------
+# six-way modulation
+# ---------------------------------------------------------------------------
+
+def adaln_modulation6_bf16(adaln_params, layer_modulation, out=None):
+    """Six bf16 (batch, seq, dim) tensors from fp32 (batch, seq, 6, dim) params + (6, dim) modulation.
+
+    ``out`` may be a (6, batch, seq, dim) bf16 tensor or a sequence of six
+    (batch, seq, dim) bf16 tensors; the result is a tuple of six tensors.
+    """
+    p = adaln_params
+    if not isinstance(p, torch.Tensor) or p.dim() != 4 or p.shape[2] != 6:
+        raise ValueError("adaln_params must be a (batch, seq, 6, dim) tensor")
+    b, s, _, dim = p.shape
+    dev = p.device
+    _need(p, "adaln_params", torch.float32, (b, s, 6, dim), dev)
+    _need(layer_modulation, "layer_modulation", torch.float32, (6, dim), dev)
+    if out is None:
+        buf = torch.empty((6, b, s, dim), dtype=torch.bfloat16, device=dev)
+        outs = tuple(buf[i] for i in range(6))
+    elif isinstance(out, torch.Tensor):
+        _need(out, "out", torch.bfloat16, (6, b, s, dim), dev)
+        outs = tuple(out[i] for i in range(6))
+    else:
+        outs = tuple(out)
+        if len(outs) != 6:
+            raise ValueError("out must hold six tensors")
+        for i, o in enumerate(outs):
+            _need(o, f"out[{i}]", torch.bfloat16, (b, s, dim), dev)
+    arr = (ctypes.c_void_p * 6)(*[o.data_ptr() for o in outs])
+    rc = _load().adaln_modulation6_bf16(_ptr(p), _ptr(layer_modulation), arr, b, s, dim, _stream(dev))
+    _raise("adaln_modulation6_bf16", rc)
+    return outs

@@ -1,0 +1,257 @@
+// abi.cu -- the C ABI of libnvfp4ap.so (declared in include/nvfp4ap.h).
+//
+// Each entry point checks its arguments on the host (shapes, dim rules,
+// indices, pointer alignment, eps), picks the kernel variant and launch shape
+// from dim, launches on the caller's stream and returns a status.  Nothing
+// here allocates, synchronises or touches device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "nvfp4ap.h"
+
+#define NVFP4AP_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace nvfp4ap {
+namespace {
+
+inline bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+// Launch shape for a row of `nvec` units (vectors or blocks): the candidate
+// per-thread counts are tried in order of preference and the one that wastes
+// the fewest thread slots (tpr * per_thread - nvec, tpr a multiple of 32 not
+// above the instance's limit) wins; ties keep the earlier candidate.
+// `forced` (> 0) restricts the choice to that per-thread count when it fits.
+template <typename MaxTpr>
+bool pick_shape(int64_t nvec, const int* cands, int ncand, MaxTpr max_tpr, int forced, RowShape* out) {
+  int64_t best_waste = -1;
+  for (int i = 0; i < ncand; ++i) {
+    const int nv = cands[i];
+    if (forced > 0 && nv != forced) continue;
+    const int lim = max_tpr(nv);
+    if (lim <= 0) continue;
+    int64_t tpr = (nvec + nv - 1) / nv;
+    tpr = (tpr + 31) / 32 * 32;
+    if (tpr > lim) continue;
+    const int64_t waste = tpr * nv - nvec;
+    if (best_waste < 0 || waste < best_waste) {
+      best_waste = waste;
+      out->tpr = (int)tpr;
+      out->per_thread = nv;
+    }
+  }
+  if (best_waste < 0) return false;
+  out->rpc = out->tpr >= 128 ? 1 : 128 / out->tpr;
+  return true;
+}
+
+bool grid_ok(int64_t rows, int rpc) { return (rows + rpc - 1) / rpc <= 0x7FFFFFFF; }
+
+int finish(cudaError_t e) {
+  if (e == cudaSuccess) return NVFP4AP_OK;
+  (void)cudaGetLastError();
+  return NVFP4AP_ERR_LAUNCH;
+}
+
+int check_common(int64_t rows, int64_t dim, float eps) {
+  if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
+  if (dim > NVFP4AP_MAX_DIM) return NVFP4AP_ERR_DIM;
+  if (!std::isfinite(eps) || eps < 0.f) return NVFP4AP_ERR_VALUE;
+  return NVFP4AP_OK;
+}
+
+// FP8 family: validation shared by K1-K4, then variant + shape + launch.
+int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
+  int rc = check_common(a.rows, a.dim, a.eps);
+  if (rc) return rc;
+  if (a.dim % 2 != 0) return NVFP4AP_ERR_DIM;
+  if (mod == MOD_TABLE && (a.chunks < 1 || a.shift_idx < 0 || a.shift_idx >= a.chunks ||
+                           a.scale_idx < 0 || a.scale_idx >= a.chunks))
+    return NVFP4AP_ERR_INDEX;
+  if (a.rows == 0) return NVFP4AP_OK;
+  if (!a.x || !a.out || !a.act_scale) return NVFP4AP_ERR_NULL;
+  if ((mod == MOD_BCAST || mod == MOD_PTOK) && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_TABLE && (!a.temb || !a.table)) return NVFP4AP_ERR_NULL;
+  if (!aligned(a.act_scale, 4)) return NVFP4AP_ERR_ALIGN;
+
+  // 16-byte vector path or bf16-pair path
+  const void* bf_in[3] = {a.x, nullptr, nullptr};
+  if (mod == MOD_BCAST || mod == MOD_PTOK) { bf_in[1] = a.scale; bf_in[2] = a.shift; }
+  if (mod == MOD_TABLE) bf_in[1] = a.temb;
+  bool vec8 = (a.dim % 8 == 0) && aligned(a.out, 8) && (mod != MOD_TABLE || aligned(a.table, 16));
+  bool pair_ok = aligned(a.out, 2) && (mod != MOD_TABLE || aligned(a.table, 8));
+  for (const void* p : bf_in) {
+    if (!p) continue;
+    vec8 = vec8 && aligned(p, 16);
+    pair_ok = pair_ok && aligned(p, 4);
+  }
+  if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
+  const int vec = vec8 ? 8 : 2;
+
+  static const int kVec8[] = {3, 4, 2, 6, 8, 1};
+  static const int kVec2[] = {8, 4, 16, 2, 32};
+  RowShape s{};
+  const bool ok = vec8 ? pick_shape(a.dim / 8, kVec8, 6, [](int nv) { return ln_fp8_max_tpr(8, nv); },
+                                    env_int("NVFP4AP_FP8_PER_THREAD"), &s)
+                       : pick_shape(a.dim / 2, kVec2, 5, [](int nv) { return ln_fp8_max_tpr(2, nv); },
+                                    env_int("NVFP4AP_FP8_PER_THREAD"), &s);
+  if (!ok) {
+    // a forced per-thread count that does not fit: fall back to the default choice
+    if (!(vec8 ? pick_shape(a.dim / 8, kVec8, 6, [](int nv) { return ln_fp8_max_tpr(8, nv); }, 0, &s)
+               : pick_shape(a.dim / 2, kVec2, 5, [](int nv) { return ln_fp8_max_tpr(2, nv); }, 0, &s)))
+      return NVFP4AP_ERR_DIM;
+  }
+  if (!grid_ok(a.rows, s.rpc)) return NVFP4AP_ERR_SHAPE;
+  return finish(launch_ln_fp8(a, mod, vec, s, st));
+}
+
+int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
+  int rc = check_common(a.rows, a.dim, a.eps);
+  if (rc) return rc;
+  if (a.dim % 16 != 0) return NVFP4AP_ERR_DIM;
+  if (a.rows == 0) return NVFP4AP_OK;
+  if (!a.x || !a.out || !a.sf) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
+  if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
+
+  static const int kCands[] = {2, 3, 1, 4, 6};
+  RowShape s{};
+  if (!pick_shape(a.dim / 16, kCands, 5, [](int b) { return ln_nvfp4_max_tpr(b); },
+                  env_int("NVFP4AP_NVFP4_PER_THREAD"), &s) &&
+      !pick_shape(a.dim / 16, kCands, 5, [](int b) { return ln_nvfp4_max_tpr(b); }, 0, &s))
+    return NVFP4AP_ERR_DIM;
+  const int64_t rows_pad = (a.rows + 127) / 128 * 128;
+  if (!grid_ok(rows_pad, s.rpc)) return NVFP4AP_ERR_SHAPE;
+  return finish(launch_ln_nvfp4(a, mod, s, st));
+}
+
+LnArgs ln_args(const void* x, float eps, void* out, int64_t rows, int64_t dim) {
+  LnArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.eps = eps;
+  a.out = out;
+  a.rows = rows;
+  a.dim = dim;
+  return a;
+}
+
+}  // namespace
+}  // namespace nvfp4ap
+
+using namespace nvfp4ap;
+
+NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
+  switch (status) {
+    case NVFP4AP_OK: return "ok";
+    case NVFP4AP_ERR_NULL: return "a required pointer is NULL";
+    case NVFP4AP_ERR_SHAPE: return "invalid shape (negative rows/batch/seq, dim <= 0, or grid too large)";
+    case NVFP4AP_ERR_DIM: return "dim violates the op's rule (FP8: even; NVFP4: multiple of 16; <= NVFP4AP_MAX_DIM)";
+    case NVFP4AP_ERR_INDEX: return "chunks < 1 or shift_idx/scale_idx out of range";
+    case NVFP4AP_ERR_ALIGN: return "a pointer misses its alignment rule";
+    case NVFP4AP_ERR_LAUNCH: return "CUDA launch failed";
+    case NVFP4AP_ERR_VALUE: return "eps is negative or not finite";
+    default: return "unknown status";
+  }
+}
+
+NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
+                                                 const float* act_scale, float eps, void* out, int64_t rows,
+                                                 int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_BCAST, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_bf16(const void* x, const void* scale, const void* shift,
+                                                      const float* act_scale, float eps, void* out,
+                                                      int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_PTOK, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_table_bf16(const void* x, const void* temb, const float* table,
+                                                            int64_t chunks, int64_t shift_idx, int64_t scale_idx,
+                                                            const float* act_scale, float eps, void* out,
+                                                            int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.temb = static_cast<const uint16_t*>(temb);
+  a.table = table;
+  a.chunks = chunks;
+  a.shift_idx = shift_idx;
+  a.scale_idx = scale_idx;
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_TABLE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
+                                                              void* out, int64_t rows, int64_t dim,
+                                                              nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const void* scale, const void* shift,
+                                                            float eps, void* packed, void* sf_swizzled,
+                                                            int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.sf = sf_swizzled;
+  return run_nvfp4(a, MOD_BCAST, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,
+                                                                  void* sf_swizzled, int64_t rows, int64_t dim,
+                                                                  nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.sf = sf_swizzled;
+  return run_nvfp4(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {
+  if (rows < 0 || dim <= 0 || dim % 16 != 0) return -1;
+  const int64_t rows_pad = (rows + 127) / 128 * 128;
+  const int64_t cols_pad = (dim / 16 + 3) / 4 * 4;
+  return rows_pad * cols_pad;
+}
+
+NVFP4AP_EXPORT int adaln_modulation6_bf16(const float* params, const float* modulation, void* const out[6],
+                                          int64_t batch, int64_t seq, int64_t dim, nvfp4ap_stream_t stream) {
+  if (batch < 0 || seq < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
+  if (seq != 0 && batch > INT64_MAX / seq) return NVFP4AP_ERR_SHAPE;
+  const int64_t tokens = batch * seq;
+  if (tokens == 0) return NVFP4AP_OK;
+  if (!params || !modulation || !out) return NVFP4AP_ERR_NULL;
+  Mod6Args a{};
+  a.params = params;
+  a.modulation = modulation;
+  a.tokens = tokens;
+  a.dim = dim;
+  bool vec8 = (dim % 8 == 0) && aligned(params, 16) && aligned(modulation, 16);
+  bool natural = aligned(params, 4) && aligned(modulation, 4);
+  for (int i = 0; i < 6; ++i) {
+    if (!out[i]) return NVFP4AP_ERR_NULL;
+    a.out[i] = static_cast<uint16_t*>(out[i]);
+    vec8 = vec8 && aligned(out[i], 16);
+    natural = natural && aligned(out[i], 2);
+  }
+  if (!natural) return NVFP4AP_ERR_ALIGN;
+  return finish(launch_modulation6(a, vec8, reinterpret_cast<cudaStream_t>(stream)));
+}

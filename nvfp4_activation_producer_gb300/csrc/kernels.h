@@ -1,0 +1,53 @@
+// kernels.h -- internal interface between the C ABI (abi.cu) and the kernel
+// translation units.  Not installed; the public interface is nvfp4ap.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4ap {
+
+// modulation source of a LayerNorm producer
+enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3 };
+
+// Arguments of one LayerNorm producer launch (device pointers, element counts).
+struct LnArgs {
+  const uint16_t* x;      // (rows, dim) bf16
+  const uint16_t* scale;  // BCAST: (dim,)  PTOK: (rows, dim)  bf16
+  const uint16_t* shift;
+  const uint16_t* temb;   // TABLE: (rows, chunks, dim) bf16
+  const float* table;     // TABLE: (chunks, dim) fp32
+  int64_t chunks, shift_idx, scale_idx;
+  const float* act_scale; // FP8: device scalar
+  float eps;
+  void* out;              // FP8: (rows, dim) e4m3; NVFP4: packed (rows, dim/2)
+  void* sf;               // NVFP4: swizzled scales
+  int64_t rows, dim;
+};
+
+// Launch shape of a row kernel: `tpr` threads per row, `per_thread` vectors
+// (FP8) or 16-element blocks (NVFP4) per thread, `rpc` rows per CTA.
+struct RowShape {
+  int tpr, per_thread, rpc;
+};
+
+// FP8 producers (K1-K4).  `vec` is 8 (16-byte vectors) or 2 (bf16 pairs).
+cudaError_t launch_ln_fp8(const LnArgs& a, int mod, int vec, RowShape s, cudaStream_t st);
+// Largest threads-per-row (and threads-per-CTA) the (vec, per_thread)
+// instance accepts; 0 if there is no such instance.
+int ln_fp8_max_tpr(int vec, int per_thread);
+
+// NVFP4 producers (K5-K6).
+cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
+int ln_nvfp4_max_tpr(int per_thread);
+
+// Six-way modulation (K7).
+struct Mod6Args {
+  const float* params;      // (tokens, 6, dim) fp32
+  const float* modulation;  // (6, dim) fp32
+  uint16_t* out[6];         // (tokens, dim) bf16 each
+  int64_t tokens, dim;
+};
+cudaError_t launch_modulation6(const Mod6Args& a, bool vec8, cudaStream_t st);
+
+}  // namespace nvfp4ap

@@ -28,3 +28,22 @@ def orc():
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def dev():
+    """cuda:0 with the CUDA library built; a gpu test fails (not skips) without them."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for a gpu-marked test")
+    from nvfp4_activation_producer_gb300 import build as b
+    b.build()
+    import nvfp4_activation_producer_gb300 as ap
+    ap.library_path()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="session")
+def ap(dev):
+    import nvfp4_activation_producer_gb300 as ap
+    return ap

@@ -1,0 +1,128 @@
+"""Host-side checks of the C-ABI library (CPU only, nothing is launched).
+
+- libnvfp4ap.so builds, loads and exports exactly the entry points that
+  include/nvfp4ap.h declares;
+- every argument error is reported with its status code before anything is
+  launched (the pointers below are never dereferenced);
+- swizzled_sf_size agrees with the oracle's size and the pages' byte counts.
+"""
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4ap.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_activation_producer_gb300 import build as b
+    path = b.build()
+    import nvfp4_activation_producer_gb300 as ap
+    return ap._load(), path
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\**\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_match_header(lib):
+    _, path = lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
+    declared = declared_functions()
+    assert declared == exported, (declared, exported)
+    assert len(declared) == 10
+
+
+def test_status_strings_and_version(lib):
+    L, _ = lib
+    for s in range(8):
+        assert L.nvfp4ap_status_string(s)
+    assert L.nvfp4ap_status_string(99) == b"unknown status"
+    assert L.nvfp4ap_version() >= 100
+
+
+def test_swizzled_sf_size_matches_oracle_and_pages(lib, orc, golden_dir):
+    L, _ = lib
+    for rows, dim in [(0, 16), (1, 16), (5070, 3072), (129, 80), (127, 48), (4096, 7168), (3, 32768)]:
+        assert L.swizzled_sf_size(rows, dim) == orc.swizzled_sf_size(rows, dim)
+    for bad in [(1, 8), (1, 0), (-1, 16), (4, 17)]:
+        assert L.swizzled_sf_size(*bad) == -1
+    g = json.load(open(os.path.join(golden_dir, "nvfp4_ring_sizes.json")))
+    for rec in g["records"]:
+        assert L.swizzled_sf_size(rec["row_capacity"], rec["K"]) == rec["sfa_bytes"]
+
+
+A = 0x100000  # a 16-byte aligned fake device address, never dereferenced
+NULL = None
+
+
+def test_fp8_argument_errors(lib):
+    L, _ = lib
+    f = L.ada_layer_norm_quant_fp8_bf16
+    assert f(A, A, A, A, 1e-5, A, -1, 64, NULL) == 2          # negative rows
+    assert f(A, A, A, A, 1e-5, A, 4, 0, NULL) == 2            # dim 0
+    assert f(A, A, A, A, 1e-5, A, 4, 63, NULL) == 3           # odd dim
+    assert f(A, A, A, A, 1e-5, A, 4, 32770, NULL) == 3        # above the maximum dim
+    assert f(A, A, A, A, -1.0, A, 4, 64, NULL) == 7           # negative eps
+    assert f(A, A, A, A, float("nan"), A, 4, 64, NULL) == 7   # NaN eps
+    assert f(NULL, A, A, A, 1e-5, A, 4, 64, NULL) == 1        # null x
+    assert f(A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1        # null scale
+    assert f(A, A, A, NULL, 1e-5, A, 4, 64, NULL) == 1        # null act_scale
+    assert f(A + 1, A, A, A, 1e-5, A, 4, 64, NULL) == 5       # x not even 4-byte aligned
+    assert f(A, A, A, A + 2, 1e-5, A, 4, 64, NULL) == 5       # act_scale misaligned
+    assert f(A, A, A, A, 1e-5, A + 1, 4, 64, NULL) == 5       # odd output address
+    assert f(NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0  # rows == 0: no-op
+    g = L.ada_layer_norm_quant_fp8_ptok_bf16
+    assert g(A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1
+    h = L.layer_norm_no_affine_quant_fp8_static_bf16
+    assert h(A, A, 1e-5, NULL, 4, 64, NULL) == 1
+    assert h(A, A, 1e-5, A, 4, 7, NULL) == 3
+
+
+def test_table_index_errors(lib):
+    L, _ = lib
+    t = L.ada_layer_norm_quant_fp8_ptok_table_bf16
+    assert t(A, A, A, 6, 6, 1, A, 1e-5, A, 4, 64, NULL) == 4   # shift_idx == chunks
+    assert t(A, A, A, 6, 0, -1, A, 1e-5, A, 4, 64, NULL) == 4  # negative scale_idx
+    assert t(A, A, A, 0, 0, 0, A, 1e-5, A, 4, 64, NULL) == 4   # no chunks
+    assert t(A, NULL, A, 6, 0, 1, A, 1e-5, A, 4, 64, NULL) == 1
+    assert t(A, A, A + 4, 6, 0, 1, A, 1e-5, A, 4, 64, NULL) == 5  # table not 8-byte aligned
+
+
+def test_nvfp4_argument_errors(lib):
+    L, _ = lib
+    f = L.ada_layer_norm_quant_nvfp4_swizzled_bf16
+    assert f(A, A, A, 1e-5, A, A, 4, 40, NULL) == 3            # dim % 16
+    assert f(A, A, A, 1e-5, A, A, 4, 32784, NULL) == 3         # above the maximum dim
+    assert f(A, A, A, 1e-5, NULL, A, 4, 64, NULL) == 1         # null packed
+    assert f(A, A, A, 1e-5, A, NULL, 4, 64, NULL) == 1         # null scales
+    assert f(A + 4, A, A, 1e-5, A, A, 4, 64, NULL) == 5        # x not 16-byte aligned
+    assert f(A, A, A + 8, 1e-5, A, A, 4, 64, NULL) == 5        # shift not 16-byte aligned
+    assert f(A, A, A, 1e-5, A + 4, A, 4, 64, NULL) == 5        # packed not 8-byte aligned
+    assert f(A, A, A, 1e-5, A, A, 0, 64, NULL) == 0
+    g = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16
+    assert g(A, 1e-5, A, A, -3, 64, NULL) == 2
+    assert g(A, float("inf"), A, A, 3, 64, NULL) == 7
+
+
+def test_modulation6_argument_errors(lib):
+    L, _ = lib
+    f = L.adaln_modulation6_bf16
+    six = lambda *p: (ctypes.c_void_p * 6)(*p)
+    outs = six(A, A, A, A, A, A)
+    assert f(A, A, outs, -1, 4, 64, NULL) == 2
+    assert f(A, A, outs, 1, 4, 0, NULL) == 2
+    assert f(NULL, A, outs, 1, 4, 64, NULL) == 1
+    assert f(A, A, six(A, A, A, NULL, A, A), 1, 4, 64, NULL) == 1
+    assert f(A + 2, A, outs, 1, 4, 64, NULL) == 5              # params not 4-byte aligned
+    assert f(A, A, six(A, A, A, A, A + 1, A), 1, 4, 64, NULL) == 5
+    assert f(NULL, NULL, outs, 0, 4, 64, NULL) == 0            # no tokens: no-op
