@@ -1,0 +1,562 @@
+"""Benchmark of the adaptive-LayerNorm activation producers on GB300.
+
+One step = one call of every producer on its workload (the shapes of the
+producers' benchmark tables), all inputs resident in HBM, in this order:
+
+  fp8 broadcast 4096x3072 | fp8 layer norm 4096x3072 | fp8 per-token 2520x3072 |
+  fp8 table 4096x3072 (6 chunks) | nvfp4 broadcast 5070x3072 | nvfp4 layer norm
+  5070x3072 | modulation6 1x5070x6x3072
+
+Every producer reads its own buffers and one step streams ~0.9 GB, so no
+input is still in the 129 MB L2 when its producer runs again.
+
+metric: µs/call and achieved HBM GB/s per producer; the headline `value` is
+the step's algorithmic bytes (what the producers must read and write) divided
+by the step's device time, in GB/s, summed over ranks.  `e2e` is the same
+metric through the Python API with host buffers: every step copies its inputs
+from pinned host memory and its outputs back.  `roofline` is for the kernel
+with the largest share of the step; `per_op` lists every producer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--sweep] [--out FILE]
+
+`--impl reference` times the CPU oracle (the only reference implementation of
+this path) on a bounded sample of the same workload on the host cores.
+Under torchrun each rank runs the whole step on its own GPU (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (fraction of GB300 peak) per producer op/shape"
+WORKLOAD = ("adaLN producer step: fp8 broadcast 4096x3072, fp8 layer-norm 4096x3072, fp8 per-token 2520x3072 "
+            "(1% rows x8), fp8 table 4096x3072 (temb 6 chunks, fp32 table), nvfp4 broadcast 5070x3072, "
+            "nvfp4 layer-norm 5070x3072, modulation6 1x5070x6x3072")
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def step_workloads():
+    return [
+        ("fp8_broadcast", synth.fp8_broadcast(4096, 3072, 2001)),
+        ("fp8_layer_norm", synth.fp8_ln(4096, 3072, 2002)),
+        ("fp8_per_token", synth.fp8_ptok(2520, 3072, 1002)),
+        ("fp8_table", synth.fp8_table(4096, 3072, 1003)),
+        ("nvfp4_broadcast", synth.nvfp4_broadcast(5070, 3072, 1004)),
+        ("nvfp4_layer_norm", synth.nvfp4_ln(5070, 3072, 2004)),
+        ("modulation6", synth.modulation6(1, 5070, 3072, 1005)),
+    ]
+
+
+def alg_bytes(name: str, w) -> int:
+    """Bytes the producer must move: every input element it uses read once,
+    every output byte written once (per-op formulas of the design notes)."""
+    R, D = w.rows, w.dim
+    if name == "fp8_broadcast":
+        return 2 * R * D + 4 * D + R * D + 4
+    if name == "fp8_layer_norm":
+        return 2 * R * D + R * D + 4
+    if name == "fp8_per_token":
+        return 6 * R * D + R * D + 4
+    if name == "fp8_table":
+        return 2 * R * D + 4 * R * D + 8 * D + R * D + 4   # 2 of the temb chunks, 2 table rows
+    if name in ("nvfp4_broadcast", "nvfp4_layer_norm"):
+        mod = 4 * D if name == "nvfp4_broadcast" else 0
+        sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
+        return 2 * R * D + mod + R * D // 2 + sf
+    if name == "modulation6":
+        return 24 * R * D + 24 * D + 12 * R * D
+    raise KeyError(name)
+
+
+class DeviceOp:
+    """Inputs resident on the device, outputs preallocated, one call = one launch."""
+
+    def __init__(self, ap, name, w, dev):
+        self.ap, self.name, self.w = ap, name, w
+        self.d = {k: v.to(dev) for k, v in w.inputs.items()}
+        R, D = w.rows, w.dim
+        if name.startswith("fp8"):
+            self.out = (torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev),)
+        elif name.startswith("nvfp4"):
+            self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
+                        torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev))
+        else:
+            self.out = (torch.empty((6, 1, R, D), dtype=torch.bfloat16, device=dev),)
+        self.bytes = alg_bytes(name, w)
+
+    def api_call(self):
+        """The producer through the Python API (tensor checks, then the C ABI)."""
+        ap, d, o, p = self.ap, self.d, self.out, self.w.params
+        n = self.name
+        if n == "fp8_broadcast":
+            ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"], p["eps"], out=o[0])
+        elif n == "fp8_layer_norm":
+            ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"], p["eps"], out=o[0])
+        elif n == "fp8_per_token":
+            ap.ada_layer_norm_quant_fp8_ptok_bf16(d["x"], d["scale"], d["shift"], d["act_scale"], p["eps"], out=o[0])
+        elif n == "fp8_table":
+            ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"],
+                                                        p["shift_idx"], p["scale_idx"], p["eps"], out=o[0])
+        elif n == "nvfp4_broadcast":
+            ap.ada_layer_norm_quant_nvfp4_swizzled_bf16(d["x"], d["scale"], d["shift"], p["eps"],
+                                                        packed=o[0], sf_swizzled=o[1])
+        elif n == "nvfp4_layer_norm":
+            ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(d["x"], p["eps"], packed=o[0], sf_swizzled=o[1])
+        elif n == "modulation6":
+            ap.adaln_modulation6_bf16(d["params"], d["modulation"], out=o[0])
+
+    def bind_raw(self, stream: int):
+        """Pre-marshalled C-ABI call (pointers fixed), so the timed loop adds
+        only the ctypes call and the launch to each producer."""
+        import ctypes
+        L = self.ap._load()
+        d, o, p, R, D = self.d, self.out, self.w.params, self.w.rows, self.w.dim
+        P = lambda t: t.data_ptr()
+        n = self.name
+        if n == "fp8_broadcast":
+            fn, a = L.ada_layer_norm_quant_fp8_bf16, (P(d["x"]), P(d["scale"]), P(d["shift"]), P(d["act_scale"]),
+                                                      p["eps"], P(o[0]), R, D, stream)
+        elif n == "fp8_layer_norm":
+            fn, a = L.layer_norm_no_affine_quant_fp8_static_bf16, (P(d["x"]), P(d["act_scale"]), p["eps"], P(o[0]),
+                                                                   R, D, stream)
+        elif n == "fp8_per_token":
+            fn, a = L.ada_layer_norm_quant_fp8_ptok_bf16, (P(d["x"]), P(d["scale"]), P(d["shift"]),
+                                                           P(d["act_scale"]), p["eps"], P(o[0]), R, D, stream)
+        elif n == "fp8_table":
+            fn, a = L.ada_layer_norm_quant_fp8_ptok_table_bf16, (P(d["x"]), P(d["temb"]), P(d["table"]),
+                                                                 d["temb"].shape[1], p["shift_idx"], p["scale_idx"],
+                                                                 P(d["act_scale"]), p["eps"], P(o[0]), R, D, stream)
+        elif n == "nvfp4_broadcast":
+            fn, a = L.ada_layer_norm_quant_nvfp4_swizzled_bf16, (P(d["x"]), P(d["scale"]), P(d["shift"]), p["eps"],
+                                                                 P(o[0]), P(o[1]), R, D, stream)
+        elif n == "nvfp4_layer_norm":
+            fn, a = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16, (P(d["x"]), p["eps"], P(o[0]), P(o[1]), R, D,
+                                                                       stream)
+        else:
+            self._outs6 = (ctypes.c_void_p * 6)(*[o[0][i].data_ptr() for i in range(6)])
+            fn, a = L.adaln_modulation6_bf16, (P(d["params"]), P(d["modulation"]), self._outs6, 1, R, D, stream)
+        name = self.name
+
+        def call():
+            rc = fn(*a)
+            if rc:
+                raise RuntimeError(f"{name}: status {rc}")
+        self.raw = call
+        return call
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_sources_digest() -> str:
+    csrc = os.path.join(ROOT, "nvfp4_activation_producer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(op: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_sources_digest") != kernel_sources_digest():
+        return None
+    rec = t.get("per_launch", {}).get(op)
+    return rec.get("dram_bytes") if rec else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 50 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [s for t, s in self.samples if self.t0 and self.t1 and self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not rows:
+            rows = [s for _, s in self.samples]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import nvfp4_activation_producer_gb300 as ap
+    from nvfp4_activation_producer_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    works = step_workloads()
+    ops = [DeviceOp(ap, n, w, dev) for n, w in works]
+    stream = torch.cuda.current_stream(dev)
+    step_bytes = sum(o.bytes for o in ops)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    calls = [o.bind_raw(stream.cuda_stream) for o in ops]
+    for _ in range(args.warmup):
+        for o in ops:
+            o.api_call()       # the public API once per op and warm-up step
+        for c in calls:
+            c()
+    barrier()
+
+    # per-op events inside the timed region, on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[local_rank] if vis else str(local_rank)
+    clocks = ClockSampler(smi_index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    clocks.mark("t0")
+    t_start.record(stream)
+    for k in range(args.steps):
+        for i, c in enumerate(calls):
+            ev[k][i][0].record(stream)
+            c()
+            ev[k][i][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clocks.mark("t1")
+    clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs") if peaks else None
+    peak_src = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    per_op = []
+    for i, o in enumerate(ops):
+        us = statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)) * 1e3
+        gbs = o.bytes / (us * 1e-6) / 1e9
+        per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
+                       "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4)})
+    dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])
+    d = per_op[dom]
+    roofline = {"bound": "hbm", "kernel": d["op"], "achieved": d["gbs"], "peak": hbm, "peak_source": peak_src,
+                "unit": "GB/s", "frac": round(d["gbs"] / hbm, 4), "alg_bytes_per_launch": d["alg_bytes"],
+                "traffic": committed_traffic(d["op"])}
+
+    # end to end through the Python API with host buffers (pinned), fewer steps
+    e2e = None if args.no_e2e else run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step_alg_bytes": step_bytes,
+                   "l2": "no flush: each step streams ~0.9 GB of distinct buffers (> 129 MB L2) between repeats "
+                         "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
+        "roofline": roofline, "per_op": per_op, "e2e": e2e,
+        "gpu_launches": len(ops) * args.steps, "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
+    return result
+
+
+def run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier):
+    host_ops = []
+    h2d = d2h = 0
+    for name, w in works:
+        pinned = {k: v.pin_memory() for k, v in w.inputs.items()}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in w.inputs.items()}
+        op = DeviceOp.__new__(DeviceOp)
+        op.ap, op.name, op.w, op.d = ap, name, w, dev_in
+        R, D = w.rows, w.dim
+        if name.startswith("fp8"):
+            op.out = (torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev),)
+        elif name.startswith("nvfp4"):
+            op.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
+                      torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev))
+        else:
+            op.out = (torch.empty((6, 1, R, D), dtype=torch.bfloat16, device=dev),)
+        host_out = tuple(torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in op.out)
+        h2d += sum(v.numel() * v.element_size() for v in pinned.values())
+        d2h += sum(o.numel() * o.element_size() for o in op.out)
+        host_ops.append((op, pinned, host_out))
+
+    def one_step():
+        for op, pinned, host_out in host_ops:
+            for k, v in pinned.items():
+                op.d[k].copy_(v, non_blocking=True)
+            op.api_call()
+            for h, o in zip(host_out, op.out):
+                h.copy_(o, non_blocking=True)
+
+    steps = max(3, min(args.e2e_steps, args.steps))
+    for _ in range(2):
+        one_step()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one_step()
+    t1.record(stream)
+    barrier()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / steps
+    return {"value": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms_step, 4), "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(works, frac_rows: int, nthreads: int):
+    """Run the oracle on the first rows/frac_rows rows of every producer; returns the
+    algorithmic bytes of the sample."""
+    import oracle
+    total = 0
+    for name, w in works:
+        n = max(1, w.rows // frac_rows)
+        x = synth.u16(w.inputs["x"][:n]) if "x" in w.inputs else None
+        eps = w.params.get("eps", 1e-5)
+        if name == "fp8_broadcast":
+            oracle.ln_quant_fp8(x, 0.025, oracle.MOD_BCAST, eps, nthreads, scale=synth.u16(w.inputs["scale"]),
+                                shift=synth.u16(w.inputs["shift"]))
+        elif name == "fp8_layer_norm":
+            oracle.ln_quant_fp8(x, 0.025, oracle.MOD_NONE, eps, nthreads)
+        elif name == "fp8_per_token":
+            oracle.ln_quant_fp8(x, 0.025, oracle.MOD_PTOK, eps, nthreads, scale=synth.u16(w.inputs["scale"][:n]),
+                                shift=synth.u16(w.inputs["shift"][:n]))
+        elif name == "fp8_table":
+            oracle.ln_quant_fp8(x, 0.025, oracle.MOD_TABLE, eps, nthreads, temb=synth.u16(w.inputs["temb"][:n]),
+                                table=w.inputs["table"].numpy(), shift_idx=w.params["shift_idx"],
+                                scale_idx=w.params["scale_idx"])
+        elif name == "nvfp4_broadcast":
+            oracle.ln_quant_nvfp4(x, oracle.MOD_BCAST, eps, nthreads, scale=synth.u16(w.inputs["scale"]),
+                                  shift=synth.u16(w.inputs["shift"]))
+        elif name == "nvfp4_layer_norm":
+            oracle.ln_quant_nvfp4(x, oracle.MOD_NONE, eps, nthreads)
+        elif name == "modulation6":
+            oracle.adaln_modulation6(w.inputs["params"][:, :n].numpy(), w.inputs["modulation"].numpy(), nthreads)
+        sub = synth.Workload(w.op, n, w.dim)
+        total += alg_bytes(name, sub)
+    return total
+
+
+def cpu_baseline(works, budget_s: float = 15.0, frac_rows: int = 8):
+    import oracle
+    oracle.build()
+    nthreads = oracle.default_threads()
+    oracle_sample_step(works, 64, nthreads)  # warm the page cache / code
+    t0 = time.perf_counter()
+    reps, total = 0, 0
+    while True:
+        total += oracle_sample_step(works, frac_rows, nthreads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / 1e9, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"first 1/{frac_rows} of the rows of every producer of the step, repeated {reps}x "
+                      f"({dt:.1f} s, {total / 1e9:.2f} GB algorithmic)"}
+
+
+def run_reference(args):
+    works = step_workloads()
+    step_bytes = sum(alg_bytes(n, w) for n, w in works)
+    import oracle
+    oracle.build()
+    nthreads = oracle.default_threads()
+    frac = 16
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample_step(works, frac, nthreads)
+    times, sample_bytes = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        sample_bytes = oracle_sample_step(works, frac, nthreads)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times)
+    value = sample_bytes * len(times) / dt / 1e9
+    ms_full = step_bytes / (value * 1e9) * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_full, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "step_alg_bytes": step_bytes,
+                       "sample": f"each step runs the CPU oracle on the first 1/{frac} of the rows of every "
+                                 f"producer; ms_per_step is scaled to the full step"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"first 1/{frac} of the rows of every producer, {args.steps} steps"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+# row sweep of the FP8 broadcast producer (optional)
+# ---------------------------------------------------------------------------
+
+def run_sweep(args, dev):
+    import nvfp4_activation_producer_gb300 as ap
+    l2 = 129 * 2 ** 20
+    res = []
+    for D in synth.SWEEP_DIMS:
+        for R in synth.SWEEP_ROWS:
+            w = synth.fp8_broadcast(R, D, synth.SWEEP_SEED)
+            one = alg_bytes("fp8_broadcast", w)
+            nsets = max(2, int(np.ceil(3 * l2 / one)))
+            nsets = min(nsets, 512)
+            x = w.inputs["x"].to(dev)
+            xs = [x.clone() for _ in range(nsets)]
+            outs = [torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev) for _ in range(nsets)]
+            sc, sh, act = (w.inputs[k].to(dev) for k in ("scale", "shift", "act_scale"))
+            for i in range(nsets):
+                ap.ada_layer_norm_quant_fp8_bf16(xs[i], sc, sh, act, out=outs[i])
+            reps = max(nsets, 200)
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for i in range(reps):
+                ap.ada_layer_norm_quant_fp8_bf16(xs[i % nsets], sc, sh, act, out=outs[i % nsets])
+            t1.record()
+            torch.cuda.synchronize()
+            us = t0.elapsed_time(t1) * 1e3 / reps
+            res.append({"rows": R, "dim": D, "us_per_call": round(us, 3), "gbs": round(one / us / 1e3, 1),
+                        "rows_per_s": round(R / us * 1e6), "buffer_sets": nsets})
+            del xs, outs
+    return res
+
+
+def main():
+    ap_ = argparse.ArgumentParser()
+    ap_.add_argument("--gpus", type=int, default=1)
+    ap_.add_argument("--steps", type=int, default=2000)
+    ap_.add_argument("--warmup", type=int, default=20)
+    ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap_.add_argument("--e2e-steps", type=int, default=20)
+    ap_.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap_.add_argument("--no-cpu-baseline", action="store_true")
+    ap_.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap_.add_argument("--sweep", action="store_true", help="also time the FP8 broadcast row sweep")
+    ap_.add_argument("--out", default=None, help="also write the JSON line (and the sweep) to this file")
+    args = ap_.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            line = run_reference(args)
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result = run_ours(args, rank, world, local_rank)
+    if args.sweep and rank == 0:
+        result["sweep_fp8_broadcast"] = run_sweep(args, torch.device("cuda", local_rank))
+    if rank == 0:
+        line = json.dumps(result)
+        print(line, flush=True)
+        if args.out:
+            with open(args.out, "w") as f:
+                f.write(line + "\n")
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -73,7 +73,7 @@ def _crafted_rows():
         blocks.append(b)
     blocks.append(np.zeros(16))                                          # all-zero block: scale 0
     blocks.append(np.array([-2.0 ** -100, 2.0 ** -100] + [0.0] * 14))    # underflowing block: signed zeros
-    blocks.append(np.array([4000.0, -4000.0, 3000.0, 1.0] + [0.0] * 12))  # scale saturates at 448
+    blocks.append(np.array([4000.0, -4000.0, 2560.0, 1.0] + [0.0] * 12))  # scale saturates at 448
     blocks.append(np.array([6.0, -0.125, 0.125, -2.875, 2.875, 2.0 ** -10] + [0.5] * 10))  # small values round to +-0
     # amax/6 = 1.0625 lies halfway between e4m3 1.0 and 1.125: the scale is 1.0
     blocks.append(np.array([6.375, 1, -1, 2, -3, 0.5, -0.5, 4, -4, 1.5, -1.5, 3, 0.25, 0.75, -5, 5.0]))
