@@ -271,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     works = step_workloads()
     ops = [DeviceOp(ap, n, w, dev) for n, w in works]
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
     step_bytes = sum(o.bytes for o in ops)
 
     def barrier():
@@ -280,16 +280,43 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
 
     calls = [o.bind_raw(stream.cuda_stream) for o in ops]
-    for _ in range(args.warmup):
-        for o in ops:
-            o.api_call()       # the public API once per op and warm-up step
-        for c in calls:
-            c()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for o in ops:
+                o.api_call()       # the public API once per op and warm-up step
+            for c in calls:
+                c()
     barrier()
 
-    # per-op events inside the timed region, on the launching stream
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-          for _ in range(args.steps)]
+    # The timed region replays a CUDA graph of M steps (7 launches each, every
+    # launch bracketed by timing events on the launching stream), so the host
+    # never starves the GPU between launches.  `--eager` launches directly.
+    M = max(1, min(args.graph_steps, args.steps))
+    R = max(1, -(-args.steps // M))
+    graph = None
+    if not args.eager:
+        try:
+            ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in ops] for _ in range(M)]
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for m in range(M):
+                    for i, c in enumerate(calls):
+                        ev[m][i][0].record(stream)
+                        c()
+                        ev[m][i][1].record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            barrier()
+        except Exception as e:  # no graph-capturable timing events in this torch
+            print(f"bench: graph timing unavailable ({e}); launching eagerly", file=sys.stderr)
+            graph = None
+    if graph is None:
+        M, R = args.steps, 1
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+              for _ in range(M)]
+    steps = M * R
+
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = vis.split(",")[local_rank] if vis else str(local_rank)
@@ -298,13 +325,18 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     barrier()
     clocks.mark("t0")
-    t_start.record(stream)
-    for k in range(args.steps):
-        for i, c in enumerate(calls):
-            ev[k][i][0].record(stream)
-            c()
-            ev[k][i][1].record(stream)
-    t_end.record(stream)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        if graph is not None:
+            for _ in range(R):
+                graph.replay()
+        else:
+            for k in range(M):
+                for i, c in enumerate(calls):
+                    ev[k][i][0].record(stream)
+                    c()
+                    ev[k][i][1].record(stream)
+        t_end.record(stream)
     barrier()
     clocks.mark("t1")
     clocks.stop()
@@ -313,8 +345,9 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([elapsed_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    ms_per_step = elapsed_ms / args.steps
+    ms_per_step = elapsed_ms / steps
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    args.steps = steps
 
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs") if peaks else None
@@ -322,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
     hbm = hbm or 6800.0
     per_op = []
     for i, o in enumerate(ops):
-        us = statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)) * 1e3
+        us = statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(M)) * 1e3
         gbs = o.bytes / (us * 1e-6) / 1e9
         per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
                        "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4)})
@@ -343,7 +376,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "no flush: each step streams ~0.9 GB of distinct buffers (> 129 MB L2) between repeats "
                          "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": roofline, "per_op": per_op, "e2e": e2e,
-        "gpu_launches": len(ops) * args.steps, "clocks": clocks.summary(),
+        "gpu_launches": len(ops) * steps, "clocks": clocks.summary(),
+        "timing": ("CUDA graph of %d steps replayed %d times; per-op times from the events of the last replay" % (M, R))
+        if graph is not None else "eager launches, per-op events around every launch",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
@@ -380,14 +415,16 @@ def run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier):
                 h.copy_(o, non_blocking=True)
 
     steps = max(3, min(args.e2e_steps, args.steps))
-    for _ in range(2):
-        one_step()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one_step()
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        one_step()
-    t1.record(stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            one_step()
+        t1.record(stream)
     barrier()
     ms = t0.elapsed_time(t1)
     if world > 1:
@@ -524,6 +561,8 @@ def main():
     ap_.add_argument("--warmup", type=int, default=20)
     ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap_.add_argument("--e2e-steps", type=int, default=20)
+    ap_.add_argument("--graph-steps", type=int, default=25, help="steps captured per CUDA graph")
+    ap_.add_argument("--eager", action="store_true", help="launch directly instead of replaying a CUDA graph")
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
     ap_.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")

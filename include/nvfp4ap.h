@@ -52,7 +52,9 @@ enum nvfp4ap_status {
   NVFP4AP_ERR_INDEX = 4,   /* chunks < 1 or shift_idx/scale_idx out of range */
   NVFP4AP_ERR_ALIGN = 5,   /* a pointer misses its alignment rule            */
   NVFP4AP_ERR_LAUNCH = 6,  /* the CUDA launch failed (cudaGetLastError)      */
-  NVFP4AP_ERR_VALUE = 7    /* eps negative or not finite                      */
+  NVFP4AP_ERR_VALUE = 7,   /* eps negative or not finite                      */
+  NVFP4AP_ERR_FAULT = 8    /* a kernel's bounded wait ran out (see
+                              nvfp4ap_take_device_fault)                      */
 };
 
 #define NVFP4AP_MAX_DIM 32768
@@ -62,6 +64,16 @@ const char* nvfp4ap_status_string(int status);
 
 /* Version of this ABI (major*10000 + minor*100 + patch). */
 int nvfp4ap_version(void);
+
+/* The LayerNorm producers stage rows through shared memory with
+ * asynchronous bulk copies and wait on them with a bounded wait (about one
+ * second).  If a wait ever runs out, the kernel stops early, leaves its
+ * output incomplete and sets a fault word on the current device instead of
+ * hanging.  This call reads and clears that word: NVFP4AP_ERR_FAULT if any
+ * kernel on the current device has set it since the last call, NVFP4AP_OK if
+ * not, NVFP4AP_ERR_LAUNCH if the device could not be read.  Unlike every
+ * other entry point it synchronises with the device (a blocking copy). */
+int nvfp4ap_take_device_fault(void);
 
 /* ------------------------------------------------------------------------
  * FP8 producers.  For each row r of x (rows, dim) bf16:

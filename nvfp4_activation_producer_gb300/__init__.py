@@ -27,12 +27,13 @@ __all__ = [
     "adaln_modulation6_bf16",
     "swizzled_sf_size",
     "library_path",
+    "take_device_fault",
     "NvFp4ApError",
 ]
 
 LIB_PATH = _build.LIB
 
-OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE = range(8)
+OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT = range(9)
 MAX_DIM = 32768
 
 
@@ -60,6 +61,8 @@ def _load() -> ctypes.CDLL:
     L.nvfp4ap_status_string.argtypes = [i32]
     L.nvfp4ap_version.restype = i32
     L.nvfp4ap_version.argtypes = []
+    L.nvfp4ap_take_device_fault.restype = i32
+    L.nvfp4ap_take_device_fault.argtypes = []
     for name in ("ada_layer_norm_quant_fp8_bf16", "ada_layer_norm_quant_fp8_ptok_bf16"):
         fn = getattr(L, name)
         fn.restype = i32
@@ -78,6 +81,12 @@ def _load() -> ctypes.CDLL:
     L.adaln_modulation6_bf16.argtypes = [p, p, ctypes.POINTER(ctypes.c_void_p), i64, i64, i64, p]
     _lib = L
     return L
+
+
+def take_device_fault() -> None:
+    """Raise NvFp4ApError if a producer kernel on the current device ran out of
+    its bounded wait since the last check (synchronises with the device)."""
+    _raise("nvfp4ap_take_device_fault", _load().nvfp4ap_take_device_fault())
 
 
 def library_path() -> str:

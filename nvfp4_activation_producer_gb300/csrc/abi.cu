@@ -55,6 +55,40 @@ bool pick_shape(int64_t nvec, const int* cands, int ncand, MaxTpr max_tpr, int f
 
 bool grid_ok(int64_t rows, int rpc) { return (rows + rpc - 1) / rpc <= 0x7FFFFFFF; }
 
+// Multiprocessor count of the current device (cached per device ordinal).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Shape of the TMA ring kernel for a row of `dim`: 8 warps per CTA and as
+// many stages (up to 4) as fit a budget of ~110 KB of shared memory per CTA,
+// so that two CTAs share an SM; fewer warps with one stage when a stage is
+// large.  Returns false when not even one warp with one stage fits (227 KB).
+bool pick_ring(int mod, int64_t dim, RingShape* rs) {
+  const int64_t budget = (env_int("NVFP4AP_RING_SMEM_KB") > 0 ? env_int("NVFP4AP_RING_SMEM_KB") : 110) * 1024;
+  int warps = env_int("NVFP4AP_RING_WARPS") > 0 ? env_int("NVFP4AP_RING_WARPS") : 8;
+  if (warps > 16) warps = 16;
+  int stages = env_int("NVFP4AP_RING_STAGES");
+  rs->ctas_per_sm = env_int("NVFP4AP_RING_CTAS");
+  if (stages <= 0) {
+    stages = 4;
+    while (stages > 1 && ring_smem_bytes(mod, dim, warps, stages) > budget) --stages;
+    while (warps > 1 && ring_smem_bytes(mod, dim, warps, stages) > budget) --warps;
+  }
+  if (stages > 8) stages = 8;
+  if (ring_smem_bytes(mod, dim, warps, stages) > 227 * 1024) return false;
+  rs->warps = warps;
+  rs->stages = stages;
+  return true;
+}
+
 int finish(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4AP_OK;
   (void)cudaGetLastError();
@@ -96,6 +130,12 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
   const int vec = vec8 ? 8 : 2;
 
+  RingShape rs{};
+  if (vec8 && env_int("NVFP4AP_RING") >= 0 && pick_ring(mod, a.dim, &rs)) {
+    const int sms = sm_count();
+    if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, st));
+  }
+
   static const int kVec8[] = {3, 4, 2, 6, 8, 1};
   static const int kVec2[] = {8, 4, 16, 2, 32};
   RowShape s{};
@@ -122,6 +162,12 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
   if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
+
+  RingShape rs{};
+  if (env_int("NVFP4AP_RING") >= 0 && pick_ring(mod, a.dim, &rs)) {
+    const int sms = sm_count();
+    if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, st));
+  }
 
   static const int kCands[] = {2, 3, 1, 4, 6};
   RowShape s{};
@@ -159,11 +205,21 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
     case NVFP4AP_ERR_ALIGN: return "a pointer misses its alignment rule";
     case NVFP4AP_ERR_LAUNCH: return "CUDA launch failed";
     case NVFP4AP_ERR_VALUE: return "eps is negative or not finite";
+    case NVFP4AP_ERR_FAULT: return "a producer kernel's bounded wait ran out (its output is incomplete)";
     default: return "unknown status";
   }
 }
 
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
+
+NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
+  unsigned int f = 0u;
+  if (take_ring_fault(&f) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NVFP4AP_ERR_LAUNCH;
+  }
+  return f ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+}
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
                                                  const float* act_scale, float eps, void* out, int64_t rows,

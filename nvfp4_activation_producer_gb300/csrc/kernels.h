@@ -41,6 +41,19 @@ int ln_fp8_max_tpr(int vec, int per_thread);
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 int ln_nvfp4_max_tpr(int per_thread);
 
+// TMA-staged persistent ring kernels (FP8 and NVFP4): `warps` warps per
+// CTA, each with `stages` shared-memory stages of one row; at most
+// `ctas_per_sm` CTAs per SM (0 = as many as fit).  Needs dim % 8 == 0 (FP8)
+// or % 16 == 0 (NVFP4) and 16-byte aligned inputs.
+struct RingShape {
+  int warps, stages, ctas_per_sm;
+};
+int64_t ring_smem_bytes(int mod, int64_t dim, int warps, int stages);
+cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, cudaStream_t st);
+// Reads and clears the fault word the ring kernels set when a bounded wait
+// runs out (synchronising copy).
+cudaError_t take_ring_fault(unsigned int* fault);
+
 // Six-way modulation (K7).
 struct Mod6Args {
   const float* params;      // (tokens, 6, dim) fp32

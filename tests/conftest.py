@@ -47,3 +47,14 @@ def dev():
 def ap(dev):
     import nvfp4_activation_producer_gb300 as ap
     return ap
+
+
+@pytest.fixture(params=["ring", "regs"])
+def path(request, monkeypatch):
+    """Run a LayerNorm-producer test on the TMA ring kernels and on the
+    register kernels (NVFP4AP_RING=-1 selects the latter)."""
+    if request.param == "regs":
+        monkeypatch.setenv("NVFP4AP_RING", "-1")
+    else:
+        monkeypatch.delenv("NVFP4AP_RING", raising=False)
+    return request.param

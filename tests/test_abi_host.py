@@ -39,12 +39,12 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 10
+    assert len(declared) == 11
 
 
 def test_status_strings_and_version(lib):
     L, _ = lib
-    for s in range(8):
+    for s in range(9):
         assert L.nvfp4ap_status_string(s)
     assert L.nvfp4ap_status_string(99) == b"unknown status"
     assert L.nvfp4ap_version() >= 100

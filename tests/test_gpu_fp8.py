@@ -35,7 +35,7 @@ def _act(w):
 
 
 @pytest.mark.parametrize("rows,dim", SHAPES)
-def test_layer_norm_fp8(ap, dev, rows, dim):
+def test_layer_norm_fp8(ap, dev, path, rows, dim):
     w = synth.fp8_ln(rows, dim, seed=rows * 31 + dim)
     d = _d(w, dev)
     out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"], eps=1e-5)
@@ -44,7 +44,7 @@ def test_layer_norm_fp8(ap, dev, rows, dim):
 
 
 @pytest.mark.parametrize("rows,dim", SHAPES)
-def test_broadcast_fp8(ap, dev, rows, dim):
+def test_broadcast_fp8(ap, dev, path, rows, dim):
     w = synth.fp8_broadcast(rows, dim, seed=rows * 17 + dim, outliers=0.05)
     d = _d(w, dev)
     out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
@@ -54,7 +54,7 @@ def test_broadcast_fp8(ap, dev, rows, dim):
 
 
 @pytest.mark.parametrize("rows,dim", SHAPES)
-def test_per_token_fp8(ap, dev, rows, dim):
+def test_per_token_fp8(ap, dev, path, rows, dim):
     w = synth.fp8_ptok(rows, dim, seed=rows * 13 + dim)
     d = _d(w, dev)
     out = ap.ada_layer_norm_quant_fp8_ptok_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
@@ -65,7 +65,7 @@ def test_per_token_fp8(ap, dev, rows, dim):
 
 @pytest.mark.parametrize("rows,dim,chunks,si,ci", [(1, 32, 6, 0, 1), (129, 3072, 6, 0, 1), (77, 1536, 6, 4, 2),
                                                    (64, 2050, 3, 2, 2), (300, 2048, 2, 1, 0), (5, 32768, 6, 5, 3)])
-def test_table_fp8(ap, dev, rows, dim, chunks, si, ci):
+def test_table_fp8(ap, dev, path, rows, dim, chunks, si, ci):
     w = synth.fp8_table(rows, dim, seed=rows * 7 + dim, chunks=chunks, shift_idx=si, scale_idx=ci)
     d = _d(w, dev)
     out = ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"], si, ci)
@@ -107,7 +107,7 @@ def _constant_rows_with_shift(shift_vals: np.ndarray, rows: int):
     return x, sc, sh
 
 
-def test_fp8_exact_ties_on_constant_rows(ap, dev):
+def test_fp8_exact_ties_on_constant_rows(ap, dev, path):
     # constant rows normalise to exactly 0, so y = shift; act_scale = 0.5 is a
     # power of two, so y / act_scale is exact and every midpoint between two
     # e4m3 values is a tie that must round to the even code
@@ -145,7 +145,7 @@ def test_guard_bands_untouched(ap, dev):
     assert np.all(b[:pad] == 0xA5) and np.all(b[-pad:] == 0xA5)
 
 
-def test_batch_invariance(ap, dev):
+def test_batch_invariance(ap, dev, path):
     w = synth.fp8_broadcast(1024, 3072, seed=77)
     d = _d(w, dev)
     full = _codes(ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"]))
@@ -156,7 +156,7 @@ def test_batch_invariance(ap, dev):
             assert np.array_equal(part, full[start:start + n])
 
 
-def test_side_stream_and_graph_capture(ap, dev):
+def test_side_stream_and_graph_capture(ap, dev, path):
     w = synth.fp8_table(256, 3072, seed=8)
     d = _d(w, dev)
     ref = _codes(ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"], 0, 1))
@@ -173,3 +173,40 @@ def test_side_stream_and_graph_capture(ap, dev):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(_codes(out2), ref)
+
+
+@pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
+def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
+    # one warp with one or two stages per CTA and one CTA per SM: every warp
+    # walks many rows, so each stage's mbarrier goes through many phases
+    rows, dim = 6000, 256
+    for warps, stages in ((1, 1), (2, 2), (3, 4)):
+        monkeypatch.setenv("NVFP4AP_RING_WARPS", str(warps))
+        monkeypatch.setenv("NVFP4AP_RING_STAGES", str(stages))
+        monkeypatch.setenv("NVFP4AP_RING_CTAS", "1")
+        if op == "table":
+            w = synth.fp8_table(rows, dim, seed=warps)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"], 0, 1)
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_TABLE,
+                                      temb=synth.u16(w.inputs["temb"]), table=w.inputs["table"].numpy(),
+                                      shift_idx=0, scale_idx=1)
+        elif op == "ptok":
+            w = synth.fp8_ptok(rows, dim, seed=warps)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_ptok_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_PTOK, scale=u["scale"], shift=u["shift"])
+        elif op == "bcast":
+            w = synth.fp8_broadcast(rows, dim, seed=warps)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+        else:
+            w = synth.fp8_ln(rows, dim, seed=warps)
+            d = _d(w, dev)
+            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
+        check_fp8(_codes(out), ref, _act(w))
+    ap.take_device_fault()  # no bounded wait ran out

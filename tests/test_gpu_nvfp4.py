@@ -56,7 +56,7 @@ def _oracle(w, kind):
 
 @pytest.mark.parametrize("rows,dim", SHAPES)
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
-def test_nvfp4_parity(ap, dev, kind, rows, dim):
+def test_nvfp4_parity(ap, dev, path, kind, rows, dim):
     w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=rows * 3 + dim)
     gp, gs = _run(ap, kind, w, dev)
     op, os_, v = _oracle(w, kind)
@@ -82,7 +82,7 @@ def _crafted_rows():
     return np.concatenate([v, np.zeros(dim - v.size)]).astype(np.float32)
 
 
-def test_nvfp4_exact_ties_and_edges(ap, dev):
+def test_nvfp4_exact_ties_and_edges(ap, dev, path):
     shift = _crafted_rows()
     dim = shift.size
     rows = 130  # ragged: two rows in the second 128-row tile
@@ -98,7 +98,7 @@ def test_nvfp4_exact_ties_and_edges(ap, dev):
     assert not gs[padding_mask(rows, dim)].any()
 
 
-def test_zero_modulation_equals_plain(ap, dev):
+def test_zero_modulation_equals_plain(ap, dev, path):
     w = synth.nvfp4_broadcast(200, 3072, seed=4)
     x = w.inputs["x"].to(dev)
     z = torch.zeros(3072, dtype=torch.bfloat16, device=dev)
@@ -107,7 +107,7 @@ def test_zero_modulation_equals_plain(ap, dev):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_batch_invariance(ap, dev):
+def test_batch_invariance(ap, dev, path):
     w = synth.nvfp4_broadcast(640, 3072, seed=12)
     x, sc, sh = (w.inputs[k].to(dev) for k in ("x", "scale", "shift"))
     pk, sf = ap.ada_layer_norm_quant_nvfp4_swizzled_bf16(x, sc, sh)
@@ -127,3 +127,17 @@ def test_misaligned_input_rejected(ap, dev):
     with pytest.raises(ap.NvFp4ApError) as e:
         ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(y)
     assert e.value.status == ap.ERR_ALIGN
+
+
+@pytest.mark.parametrize("kind", ["ln", "bcast"])
+def test_ring_wraps_many_rows_per_warp(ap, dev, kind, monkeypatch):
+    rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
+    for warps, stages in ((1, 1), (2, 3)):
+        monkeypatch.setenv("NVFP4AP_RING_WARPS", str(warps))
+        monkeypatch.setenv("NVFP4AP_RING_STAGES", str(stages))
+        monkeypatch.setenv("NVFP4AP_RING_CTAS", "1")
+        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=warps)
+        gp, gs = _run(ap, kind, w, dev)
+        op, os_, v = _oracle(w, kind)
+        check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
+    ap.take_device_fault()
