@@ -270,6 +270,9 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     works = step_workloads()
+    if args.only:
+        keep = set(args.only.split(","))
+        works = [(n, w) for n, w in works if n in keep]
     ops = [DeviceOp(ap, n, w, dev) for n, w in works]
     stream = torch.cuda.Stream(dev)
     step_bytes = sum(o.bytes for o in ops)
@@ -563,6 +566,7 @@ def main():
     ap_.add_argument("--e2e-steps", type=int, default=20)
     ap_.add_argument("--graph-steps", type=int, default=25, help="steps captured per CUDA graph")
     ap_.add_argument("--eager", action="store_true", help="launch directly instead of replaying a CUDA graph")
+    ap_.add_argument("--only", default=None, help="comma list of producers to run (for profiling one kernel)")
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
     ap_.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
