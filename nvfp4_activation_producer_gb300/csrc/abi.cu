@@ -89,6 +89,25 @@ bool pick_ring(int mod, int64_t dim, RingShape* rs) {
   return true;
 }
 
+// Shape of the register row kernel: the most 8-element chunks per thread
+// (the fewest threads per row) that waste no thread slot, up to 96 elements
+// per thread for the streams with one input row and 24 for the per-token
+// forms, which hold three input rows in registers.  Rows per CTA fill 128
+// threads (NVFP4AP_ROWS_PER_CTA overrides).
+bool pick_rows(int mod, int64_t dim, RowShape* s) {
+  static const int kWide[] = {12, 8, 6, 4, 3, 2, 1};
+  static const int kToken[] = {3, 4, 2, 6, 1};
+  const bool per_token = (mod == MOD_PTOK || mod == MOD_TABLE);
+  const int* c = per_token ? kToken : kWide;
+  const int n = per_token ? 5 : 7;
+  auto lim = [mod](int nv) { return ln_rows_max_tpr(mod, nv); };
+  if (!pick_shape(dim / 8, c, n, lim, env_int("NVFP4AP_PER_THREAD"), s) && !pick_shape(dim / 8, c, n, lim, 0, s))
+    return false;
+  const int want = env_int("NVFP4AP_ROWS_PER_CTA");
+  if (want > 0 && want <= 16 && want * s->tpr <= 1024) s->rpc = want;
+  return true;
+}
+
 int finish(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4AP_OK;
   (void)cudaGetLastError();
@@ -130,10 +149,16 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
   const int vec = vec8 ? 8 : 2;
 
+  const int kernel = env_int("NVFP4AP_KERNEL");  // 0 rows (default), 1 ring, 2 earlier register kernel
   RingShape rs{};
-  if (vec8 && env_int("NVFP4AP_RING") >= 0 && pick_ring(mod, a.dim, &rs)) {
+  if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, st));
+  }
+  RowShape rows_shape{};
+  if (vec8 && kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
+    if (!grid_ok(a.rows, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
+    return finish(launch_ln_rows(a, false, mod, rows_shape, st));
   }
 
   static const int kVec8[] = {3, 4, 2, 6, 8, 1};
@@ -163,10 +188,17 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
 
+  const int kernel = env_int("NVFP4AP_KERNEL");  // 0 rows (default), 1 ring, 2 earlier register kernel
   RingShape rs{};
-  if (env_int("NVFP4AP_RING") >= 0 && pick_ring(mod, a.dim, &rs)) {
+  if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, st));
+  }
+  RowShape rows_shape{};
+  if (kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
+    const int64_t rows_pad = (a.rows + 127) / 128 * 128;
+    if (!grid_ok(rows_pad, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
+    return finish(launch_ln_rows(a, true, mod, rows_shape, st));
   }
 
   static const int kCands[] = {2, 3, 1, 4, 6};

@@ -37,6 +37,11 @@ cudaError_t launch_ln_fp8(const LnArgs& a, int mod, int vec, RowShape s, cudaStr
 // instance accepts; 0 if there is no such instance.
 int ln_fp8_max_tpr(int vec, int per_thread);
 
+// Register-resident row kernels for FP8 (dim % 8 == 0, 16-byte aligned) and
+// NVFP4: `per_thread` 8-element chunks per thread.
+cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
+int ln_rows_max_tpr(int mod, int per_thread);
+
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 int ln_nvfp4_max_tpr(int per_thread);

@@ -1,0 +1,295 @@
+// ln_rows.cu -- adaptive-LayerNorm producers (FP8 e4m3fn and NVFP4) for
+// sm_103a, register-resident rows.
+//
+// Operations (adaptive-layernorm-producers README, "Available Functions",
+// "Tensor Contract", "Validation"; NVFP4 encoding facts from the
+// h3-blackwell-runtime compare page):
+//   y = (x - mean) * rstd * (1 + scale) + shift, rstd = 1/sqrt(var + eps)
+//   FP8:   out = e4m3fn(y / act_scale), nearest-even, saturating
+//   NVFP4: v = bf16(y); per 16 elements s = e4m3fn(amax/6); e2m1 codes of
+//          v/s, two per byte (low nibble first); s in the 128x4 tiled layout
+//          with zero padding.
+//
+// Design.  A row is owned by `tpr` threads (a warp or a few warps); thread t
+// owns the 8-element chunks t, t+tpr, ... of the row (a warp reads 512
+// contiguous bytes per step).  Every load of the row -- and of its per-token
+// modulation rows -- is issued before any arithmetic and the row stays in
+// registers as packed bf16, so x is read from HBM exactly once.  The shape is
+// chosen so that each thread holds many elements (up to 96): the per-row work
+// (two-value reduction, rsqrt) is then small next to the per-element work,
+// which is what bounds these kernels on GB300 (a 3-byte-per-element stream
+// leaves ~18 instructions per element at full HBM bandwidth).
+//
+// Statistics in one pass over the registers, shifted by the row's first
+// element K (exact and identical for every thread): s1 = sum(x - K),
+// s2 = sum((x - K)^2); mean = K + s1/D, var = s2/D - (s1/D)^2.  The shift keeps
+// the cancellation small for rows whose mean is large against their spread,
+// and a constant row gives s1 = s2 = 0, so mean = K and x - mean = 0 exactly.
+#include "device.cuh"
+#include "kernels.h"
+
+namespace nvfp4ap {
+namespace {
+
+enum { KIND_FP8 = 0, KIND_NVFP4 = 1 };
+
+__device__ __forceinline__ int64_t sf_off(int64_t r, int c, int ct) {
+  return ((r >> 7) * ct + (c >> 2)) * 512 + (int)((r & 31) << 4) + (int)(((r >> 5) & 3) << 2) + (c & 3);
+}
+
+__device__ __forceinline__ void unpack4(uint4 v, uint32_t (&w)[4]) {
+  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+}
+
+// Largest threads-per-row of an instance: NV chunks of 8 elements per thread,
+// dim <= 32768 -> 4096 chunks per row.
+__host__ __device__ constexpr int rows_max_tpr(int nv) {
+  return ((4096 + nv - 1) / nv + 31) / 32 * 32 > 512 ? 512 : ((4096 + nv - 1) / nv + 31) / 32 * 32;
+}
+
+template <int KIND, int MOD, int NV>
+__global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const float inv_d) {
+  constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
+  __shared__ float2 red[16][16];  // [row group][warp of the row]
+
+  const int tpr = blockDim.x;
+  const int t = threadIdx.x, ry = threadIdx.y;
+  const int lane = t & 31, warp = t >> 5, nwarps = tpr >> 5;
+  const int64_t D = a.dim;
+  const int nch = (int)(D >> 3);
+  const int64_t row = (int64_t)blockIdx.x * blockDim.y + ry;
+  const bool active = row < a.rows;
+  const int64_t rbase = active ? row * D : 0;
+
+  // ---- all loads of the row first -------------------------------------------
+  uint32_t xw[NV][4];
+  uint32_t sw[kPerToken ? NV : 1][4], hw[kPerToken ? NV : 1][4];
+  const uint16_t* sc_src = nullptr;
+  const uint16_t* sh_src = nullptr;
+  if constexpr (MOD == MOD_PTOK) {
+    sc_src = a.scale + rbase;
+    sh_src = a.shift + rbase;
+  } else if constexpr (MOD == MOD_TABLE) {
+    const uint16_t* te = a.temb + (active ? row * a.chunks * D : 0);
+    sc_src = te + a.scale_idx * D;
+    sh_src = te + a.shift_idx * D;
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int j = t + k * tpr;
+    if (active && j < nch) {
+      unpack4(ld_once_v4(a.x + rbase + (int64_t)j * 8), xw[k]);
+      if constexpr (kPerToken) {
+        unpack4(ld_once_v4(sc_src + (int64_t)j * 8), sw[k]);
+        unpack4(ld_once_v4(sh_src + (int64_t)j * 8), hw[k]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xw[k][i] = 0u;
+    }
+  }
+  const float K = active ? __uint_as_float((uint32_t)__ldg(a.x + rbase) << 16) : 0.f;
+
+  // ---- statistics: one pass, shifted by K -------------------------------------
+  float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+  const float2 nk = splat2(-K);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (t + k * tpr < nch) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 d = add2(bf16x2_to_f2(xw[k][i]), nk);
+        s1 = add2(s1, d);
+        s2 = fma2(d, d, s2);
+      }
+    }
+  }
+  float2 s = make_float2(s1.x + s1.y, s2.x + s2.y);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s.x += __shfl_xor_sync(0xFFFFFFFFu, s.x, o);
+    s.y += __shfl_xor_sync(0xFFFFFFFFu, s.y, o);
+  }
+  if (nwarps > 1) {
+    if (lane == 0) red[ry][warp] = s;
+    __syncthreads();
+    s = red[ry][0];
+    for (int w = 1; w < nwarps; ++w) {
+      const float2 u = red[ry][w];
+      s.x += u.x;
+      s.y += u.y;
+    }
+  }
+  if (!active) {
+    if constexpr (KIND == KIND_NVFP4) {
+      // rows past the end inside the last 128-row tile: zero scale bytes
+      const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
+      const int64_t rows_pad = (a.rows + 127) & ~(int64_t)127;
+      if (row < rows_pad)
+        for (int c = t; c < padc; c += tpr) st_b8(reinterpret_cast<uint8_t*>(a.sf) + sf_off(row, c, ct), 0u);
+    }
+    return;
+  }
+  const float m1 = s.x * inv_d;
+  const float mean = K + m1;
+  const float var = fmaxf(fmaf(s.y, inv_d, -m1 * m1), 0.f);
+  const float rstd = rsqrtf(var + a.eps);
+  const float2 nmean = splat2(-mean);
+
+  if constexpr (KIND == KIND_FP8) {
+    // ---- FP8: q = (x - mean) * rstd * (1 + scale) + shift) / act_scale ------
+    const float inv_act = 1.0f / __ldg(a.act_scale);
+    const float2 rstd2 = splat2(rstd), inv2 = splat2(inv_act), rinv2 = splat2(rstd * inv_act);
+    uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) + row * D;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j = t + k * tpr;
+      if (j >= nch) continue;
+      uint32_t sc[4], sh[4];
+      if constexpr (MOD == MOD_BCAST) {
+        unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
+        unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
+      } else if constexpr (kPerToken) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { sc[i] = sw[k][i]; sh[i] = hw[k][i]; }
+      }
+      uint32_t q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 d = add2(bf16x2_to_f2(xw[k][i]), nmean);
+        float2 y;
+        if constexpr (MOD == MOD_NONE) {
+          y = mul2(d, rinv2);
+        } else {
+          float2 g = bf16x2_to_f2(sc[i]), h = bf16x2_to_f2(sh[i]);
+          if constexpr (MOD == MOD_TABLE) {
+            g = add2(g, ld_reuse_f2(a.table + a.scale_idx * D + (int64_t)j * 8 + 2 * i));
+            h = add2(h, ld_reuse_f2(a.table + a.shift_idx * D + (int64_t)j * 8 + 2 * i));
+          }
+          y = mul2(fma2(d, fma2(g, rstd2, rstd2), h), inv2);
+        }
+        q[i] = f2_to_e4m3x2(y);
+      }
+      st_stream_v2(orow + (int64_t)j * 8, q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+    }
+  } else {
+    // ---- NVFP4: chunk j is half of block j/2; lanes t and t^1 hold the halves
+    const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
+    const float2 rstd2 = splat2(rstd);
+    uint8_t* prow = reinterpret_cast<uint8_t*>(a.out) + row * (D >> 1);
+    uint8_t* sf = reinterpret_cast<uint8_t*>(a.sf);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j = t + k * tpr;
+      if (k * tpr >= nch) break;  // the same for every thread of the row
+      const bool valid = j < nch;
+      uint32_t vb[4] = {0u, 0u, 0u, 0u};
+      if (valid) {
+        uint32_t sc[4], sh[4];
+        if constexpr (MOD == MOD_BCAST) {
+          unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
+          unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 d = add2(bf16x2_to_f2(xw[k][i]), nmean);
+          float2 y;
+          if constexpr (MOD == MOD_BCAST)
+            y = fma2(d, fma2(bf16x2_to_f2(sc[i]), rstd2, rstd2), bf16x2_to_f2(sh[i]));
+          else
+            y = mul2(d, rstd2);
+          vb[i] = f2_to_bf16x2(y);
+        }
+      }
+      const uint32_t m = bf16x2_absmax(bf16x2_absmax(vb[0], vb[1]), bf16x2_absmax(vb[2], vb[3]));
+      float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      // e4m3(amax/6) via the fp32 constant 1/6 gives the byte of the exact
+      // quotient (see ln_nvfp4.cu); the e2m1 decision uses a quotient that is
+      // exact at every midpoint (q0 = v*rcp(s), one exact-remainder step).
+      const uint32_t sbyte = f2_to_e4m3x2(make_float2(amax * (1.0f / 6.0f), 0.f)) & 0xFFu;
+      const float scl = e4m3_to_f32(sbyte);
+      const float r = (scl == 0.f) ? 0.f : rcp_approx(scl);
+      const float2 r2 = splat2(r), ns2 = splat2(-scl);
+      float2 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 v = bf16x2_to_f2(vb[i]);
+        const float2 q0 = mul2(v, r2);
+        q[i] = fma2(fma2(q0, ns2, v), r2, q0);
+      }
+      const uint32_t codes = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
+      if (valid) {
+        st_stream_b32(prow + (int64_t)j * 4, codes);
+        if ((j & 1) == 0) st_b8(sf + sf_off(row, j >> 1, ct), sbyte);
+      }
+    }
+    for (int c = nblk + t; c < padc; c += tpr) st_b8(sf + sf_off(row, c, ct), 0u);
+  }
+}
+
+template <int KIND, int MOD>
+cudaError_t launch_nv(const LnArgs& a, RowShape s, cudaStream_t st) {
+  constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
+  const int64_t work_rows = KIND == KIND_NVFP4 ? (a.rows + 127) / 128 * 128 : a.rows;
+  const dim3 block(s.tpr, s.rpc);
+  const dim3 grid((unsigned)((work_rows + s.rpc - 1) / s.rpc));
+  const float inv_d = (float)(1.0 / (double)a.dim);
+#define NVFP4AP_CASE(N)                                                    \
+  case N:                                                                  \
+    ln_rows_kernel<KIND, MOD, N><<<grid, block, 0, st>>>(a, inv_d);        \
+    break;
+  if constexpr (kPerToken) {
+    switch (s.per_thread) {
+      NVFP4AP_CASE(1)
+      NVFP4AP_CASE(2)
+      NVFP4AP_CASE(3)
+      NVFP4AP_CASE(4)
+      NVFP4AP_CASE(6)
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (s.per_thread) {
+      NVFP4AP_CASE(1)
+      NVFP4AP_CASE(2)
+      NVFP4AP_CASE(3)
+      NVFP4AP_CASE(4)
+      NVFP4AP_CASE(6)
+      NVFP4AP_CASE(8)
+      NVFP4AP_CASE(12)
+      default: return cudaErrorInvalidValue;
+    }
+  }
+#undef NVFP4AP_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int ln_rows_max_tpr(int mod, int per_thread) {
+  const bool per_token = (mod == MOD_PTOK || mod == MOD_TABLE);
+  switch (per_thread) {
+    case 1: case 2: case 3: case 4: case 6: return rows_max_tpr(per_thread);
+    case 8: case 12: return per_token ? 0 : rows_max_tpr(per_thread);
+    default: return 0;
+  }
+}
+
+cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st) {
+  if (nvfp4) {
+    switch (mod) {
+      case MOD_NONE: return launch_nv<KIND_NVFP4, MOD_NONE>(a, s, st);
+      case MOD_BCAST: return launch_nv<KIND_NVFP4, MOD_BCAST>(a, s, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (mod) {
+    case MOD_NONE: return launch_nv<KIND_FP8, MOD_NONE>(a, s, st);
+    case MOD_BCAST: return launch_nv<KIND_FP8, MOD_BCAST>(a, s, st);
+    case MOD_PTOK: return launch_nv<KIND_FP8, MOD_PTOK>(a, s, st);
+    case MOD_TABLE: return launch_nv<KIND_FP8, MOD_TABLE>(a, s, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace nvfp4ap

@@ -49,12 +49,14 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["ring", "regs"])
+@pytest.fixture(params=["rows", "ring", "legacy"])
 def path(request, monkeypatch):
-    """Run a LayerNorm-producer test on the TMA ring kernels and on the
-    register kernels (NVFP4AP_RING=-1 selects the latter)."""
-    if request.param == "regs":
-        monkeypatch.setenv("NVFP4AP_RING", "-1")
+    """Run a LayerNorm-producer test on each kernel family: the register row
+    kernels (default), the TMA ring kernels (NVFP4AP_KERNEL=1) and the first
+    register kernels (NVFP4AP_KERNEL=2)."""
+    value = {"rows": None, "ring": "1", "legacy": "2"}[request.param]
+    if value is None:
+        monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
-        monkeypatch.delenv("NVFP4AP_RING", raising=False)
+        monkeypatch.setenv("NVFP4AP_KERNEL", value)
     return request.param

@@ -177,6 +177,7 @@ def test_side_stream_and_graph_capture(ap, dev, path):
 
 @pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
 def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
+    monkeypatch.setenv("NVFP4AP_KERNEL", "1")
     # one warp with one or two stages per CTA and one CTA per SM: every warp
     # walks many rows, so each stage's mbarrier goes through many phases
     rows, dim = 6000, 256

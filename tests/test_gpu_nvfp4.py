@@ -131,6 +131,7 @@ def test_misaligned_input_rejected(ap, dev):
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_ring_wraps_many_rows_per_warp(ap, dev, kind, monkeypatch):
+    monkeypatch.setenv("NVFP4AP_KERNEL", "1")
     rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
     for warps, stages in ((1, 1), (2, 3)):
         monkeypatch.setenv("NVFP4AP_RING_WARPS", str(warps))
