@@ -291,34 +291,44 @@ def run_ours(args, rank, world, local_rank):
                 c()
     barrier()
 
-    # The timed region replays a CUDA graph of M steps (7 launches each, every
-    # launch bracketed by timing events on the launching stream), so the host
-    # never starves the GPU between launches.  `--eager` launches directly.
+    # Timed region, two phases, both CUDA graphs replayed on `stream` and timed
+    # with CUDA events on it (the host never starves the GPU between launches):
+    #  1. the step: M steps (7 launches each) per graph, replayed R times;
+    #     `value` and `ms_per_step` come from here;
+    #  2. each producer alone: a graph of `per_op_launches` back-to-back calls
+    #     over rotating copies of its buffers (together > 3x L2, so every call
+    #     reads HBM), replayed 3 times; `per_op` and `roofline` come from here.
     M = max(1, min(args.graph_steps, args.steps))
     R = max(1, -(-args.steps // M))
-    graph = None
-    if not args.eager:
-        try:
-            ev = [[(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for _ in ops] for _ in range(M)]
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                for m in range(M):
-                    for i, c in enumerate(calls):
-                        ev[m][i][0].record(stream)
-                        c()
-                        ev[m][i][1].record(stream)
-            with torch.cuda.stream(stream):
-                graph.replay()
-            barrier()
-        except Exception as e:  # no graph-capturable timing events in this torch
-            print(f"bench: graph timing unavailable ({e}); launching eagerly", file=sys.stderr)
-            graph = None
-    if graph is None:
-        M, R = args.steps, 1
-        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-              for _ in range(M)]
     steps = M * R
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(M):
+            for c in calls:
+                c()
+    with torch.cuda.stream(stream):
+        graph.replay()
+    barrier()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(dev), "L2_cache_size") else 129 * 2 ** 20
+    per_op_graphs = []
+    for o in ops:
+        nsets = max(2, -(-3 * l2 // o.bytes))
+        copies = [o] + [DeviceOp(ap, o.name, o.w, dev) for _ in range(nsets - 1)]
+        ccalls = [c.bind_raw(stream.cuda_stream) for c in copies]
+        with torch.cuda.stream(stream):
+            for c in ccalls:
+                c()
+        g = torch.cuda.CUDAGraph()
+        n = args.per_op_launches
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                ccalls[i % nsets]()
+        with torch.cuda.stream(stream):
+            g.replay()
+        per_op_graphs.append((o, g, n, copies, nsets))
+    barrier()
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -328,18 +338,21 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     barrier()
     clocks.mark("t0")
+    op_events = []
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        if graph is not None:
-            for _ in range(R):
-                graph.replay()
-        else:
-            for k in range(M):
-                for i, c in enumerate(calls):
-                    ev[k][i][0].record(stream)
-                    c()
-                    ev[k][i][1].record(stream)
+        for _ in range(R):
+            graph.replay()
         t_end.record(stream)
+        for o, g, n, _, _ in per_op_graphs:
+            evs = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                evs.append((e0, e1))
+            op_events.append(evs)
     barrier()
     clocks.mark("t1")
     clocks.stop()
@@ -351,6 +364,8 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = elapsed_ms / steps
     value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
     args.steps = steps
+    launches = len(ops) * steps + sum(n * 3 for _, _, n, _, _ in per_op_graphs)
+    del per_op_graphs
 
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs") if peaks else None
@@ -358,11 +373,12 @@ def run_ours(args, rank, world, local_rank):
     hbm = hbm or 6800.0
     per_op = []
     for i, o in enumerate(ops):
-        us = statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(M)) * 1e3
+        n = args.per_op_launches
+        us = statistics.median(e0.elapsed_time(e1) for e0, e1 in op_events[i]) * 1e3 / n
         gbs = o.bytes / (us * 1e-6) / 1e9
         per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
                        "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4)})
-    dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])
+    dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])  # largest share of the step
     d = per_op[dom]
     roofline = {"bound": "hbm", "kernel": d["op"], "achieved": d["gbs"], "peak": hbm, "peak_source": peak_src,
                 "unit": "GB/s", "frac": round(d["gbs"] / hbm, 4), "alg_bytes_per_launch": d["alg_bytes"],
@@ -379,9 +395,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "no flush: each step streams ~0.9 GB of distinct buffers (> 129 MB L2) between repeats "
                          "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": roofline, "per_op": per_op, "e2e": e2e,
-        "gpu_launches": len(ops) * steps, "clocks": clocks.summary(),
-        "timing": ("CUDA graph of %d steps replayed %d times; per-op times from the events of the last replay" % (M, R))
-        if graph is not None else "eager launches, per-op events around every launch",
+        "gpu_launches": launches, "clocks": clocks.summary(),
+        "timing": ("step: CUDA graph of %d steps replayed %d times; per_op: graph of %d back-to-back calls per "
+                   "producer over rotating buffers > 3x L2, median of 3 replays" % (M, R, args.per_op_launches)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
@@ -565,7 +581,7 @@ def main():
     ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap_.add_argument("--e2e-steps", type=int, default=20)
     ap_.add_argument("--graph-steps", type=int, default=25, help="steps captured per CUDA graph")
-    ap_.add_argument("--eager", action="store_true", help="launch directly instead of replaying a CUDA graph")
+    ap_.add_argument("--per-op-launches", type=int, default=32, help="back-to-back calls per producer graph")
     ap_.add_argument("--only", default=None, help="comma list of producers to run (for profiling one kernel)")
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
