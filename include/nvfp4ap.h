@@ -53,8 +53,10 @@ enum nvfp4ap_status {
   NVFP4AP_ERR_ALIGN = 5,   /* a pointer misses its alignment rule            */
   NVFP4AP_ERR_LAUNCH = 6,  /* the CUDA launch failed (cudaGetLastError)      */
   NVFP4AP_ERR_VALUE = 7,   /* eps negative or not finite                      */
-  NVFP4AP_ERR_FAULT = 8    /* a kernel's bounded wait ran out (see
+  NVFP4AP_ERR_FAULT = 8,   /* a kernel's bounded wait ran out (see
                               nvfp4ap_take_device_fault)                      */
+  NVFP4AP_ERR_SCRATCH = 9  /* the call needs more than the static scratch of
+                              ada_layer_norm_quant_fp8_bf16_noalloc holds     */
 };
 
 #define NVFP4AP_MAX_DIM 32768
@@ -91,6 +93,36 @@ int nvfp4ap_take_device_fault(void);
 int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
                                   const float* act_scale, float eps, void* out,
                                   int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* No counterpart in the paper: an addition of this library.
+ *
+ * ada_layer_norm_quant_fp8_bf16_noalloc computes exactly what
+ * ada_layer_norm_quant_fp8_bf16 computes, with the same arguments, for callers
+ * that cannot allocate device memory at all -- for example code that runs
+ * under a device-memory budget fixed at start-up, or inside a framework region
+ * whose caching allocator must not grow.  It runs the TMA ring kernel, which
+ * keeps one progress word per CTA (rows finished; bit 31 set if one of the
+ * CTA's bounded waits ran out) in device scratch; here that scratch is a fixed
+ * array inside the library, 1024 words (4 KB), 256-byte aligned, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine):
+ * it clears the words it will use with cudaMemsetAsync on `stream`, then
+ * launches.
+ *  - dim % 8 == 0; x, scale, shift 16-byte aligned, out 8-byte aligned,
+ *    act_scale 4-byte aligned (else NVFP4AP_ERR_DIM / NVFP4AP_ERR_ALIGN).
+ *  - A call whose launch would need more than 1024 CTAs is rejected with
+ *    NVFP4AP_ERR_SCRATCH before anything is launched (the persistent grid is
+ *    at most a few CTAs per SM, so 1024 covers current GPUs).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and sets up the kernel's shared-memory attribute;
+ *    make that first call before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams, or different host
+ *    threads) race on it.  Serialise them on one stream.
+ *  - A bounded wait that runs out is reported by nvfp4ap_take_device_fault(). */
+int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const void* scale, const void* shift,
+                                          const float* act_scale, float eps, void* out,
+                                          int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
 /* README "Available Functions": ada_layer_norm_quant_fp8_ptok_bf16.
  * scale, shift: (rows, dim) bf16, one row of modulation per token. */

@@ -33,7 +33,7 @@ __all__ = [
 
 LIB_PATH = _build.LIB
 
-OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT = range(9)
+OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT, ERR_SCRATCH = range(10)
 MAX_DIM = 32768
 
 
@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.restype = i32
         fn.argtypes = [p, p, p, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_fp8_bf16_noalloc.restype = i32
+    L.ada_layer_norm_quant_fp8_bf16_noalloc.argtypes = [p, p, p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_fp8_ptok_table_bf16.restype = i32
     L.ada_layer_norm_quant_fp8_ptok_table_bf16.argtypes = [p, p, p, i64, i64, i64, p, f32, p, i64, i64, p]
     L.layer_norm_no_affine_quant_fp8_static_bf16.restype = i32

@@ -239,6 +239,7 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
     case NVFP4AP_ERR_LAUNCH: return "CUDA launch failed";
     case NVFP4AP_ERR_VALUE: return "eps is negative or not finite";
     case NVFP4AP_ERR_FAULT: return "a producer kernel's bounded wait ran out (its output is incomplete)";
+    case NVFP4AP_ERR_SCRATCH: return "the call needs more per-CTA words than the library's static scratch array holds";
     default: return "unknown status";
   }
 }
@@ -262,6 +263,27 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scal
   a.shift = static_cast<const uint16_t*>(shift);
   a.act_scale = act_scale;
   return run_fp8(a, MOD_BCAST, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const void* scale, const void* shift,
+                                                         const float* act_scale, float eps, void* out,
+                                                         int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  int rc = check_common(rows, dim, eps);
+  if (rc) return rc;
+  if (dim % 8 != 0) return NVFP4AP_ERR_DIM;
+  if (rows == 0) return NVFP4AP_OK;
+  if (!x || !scale || !shift || !act_scale || !out) return NVFP4AP_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(scale, 16) || !aligned(shift, 16) || !aligned(out, 8) || !aligned(act_scale, 4))
+    return NVFP4AP_ERR_ALIGN;
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4AP_ERR_LAUNCH;
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.act_scale = act_scale;
+  rc = noalloc_fp8_bcast(a, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (rc == NVFP4AP_ERR_LAUNCH) (void)cudaGetLastError();
+  return rc;
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_bf16(const void* x, const void* scale, const void* shift,

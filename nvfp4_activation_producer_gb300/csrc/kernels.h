@@ -55,6 +55,10 @@ struct RingShape {
 };
 int64_t ring_smem_bytes(int mod, int64_t dim, int warps, int stages);
 cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, cudaStream_t st);
+// FP8 broadcast producer on the ring kernel with its per-CTA words in the
+// library's static scratch array; returns an NVFP4AP_* status (arguments
+// already validated, dim % 8 == 0, 16-byte aligned inputs).
+int noalloc_fp8_bcast(const LnArgs& a, int sms, cudaStream_t st);
 // Reads and clears the fault word the ring kernels set when a bounded wait
 // runs out (synchronising copy).
 cudaError_t take_ring_fault(unsigned int* fault);

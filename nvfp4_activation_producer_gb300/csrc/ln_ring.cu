@@ -222,8 +222,10 @@ __device__ __forceinline__ void nvfp4_row(const LnArgs& a, int64_t row, const ui
   for (int cc = nblk + lane; cc < padc; cc += 32) st_b8(sf + sf_off(row, cc, ct), 0u);
 }
 
+// `cta_state` (may be null): one word per CTA; each warp adds the number of
+// rows it finished, and bit 31 marks a CTA one of whose waits ran out.
 template <int KIND, int MOD>
-__global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int S) {
+__global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int S, unsigned int* cta_state) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int W = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t D = a.dim;
@@ -282,12 +284,17 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
 
   int s = 0;
   uint32_t parity = 0u;
+  unsigned int done = 0u;
   for (int64_t row = gw; row < a.rows; row += G) {
     const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&wb[s], parity));
     if (!ok) {
-      if (lane == 0) atomicOr(&g_ring_fault, 1u);
+      if (lane == 0) {
+        atomicOr(&g_ring_fault, 1u);
+        if (cta_state) atomicOr(&cta_state[blockIdx.x], 0x80000000u);
+      }
       return;
     }
+    ++done;
     const uint8_t* stage = ring + (size_t)s * stage_bytes;
     if constexpr (KIND == KIND_FP8) fp8_row<MOD>(a, row, stage, cst, lane, inv_act);
     else nvfp4_row<MOD>(a, row, stage, cst, lane);
@@ -298,6 +305,7 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
     }
     if (++s == S) { s = 0; parity ^= 1u; }
   }
+  if (cta_state && lane == 0 && done) atomicAdd(&cta_state[blockIdx.x], done);
 
   if constexpr (KIND == KIND_NVFP4) {
     // rows past the end inside the last 128-row tile: zero scale bytes
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
   }
 }
 
-using RingKernel = void (*)(const LnArgs, const int);
+using RingKernel = void (*)(const LnArgs, const int, unsigned int*);
 
 RingKernel pick(int kind, int mod) {
   if (kind == KIND_FP8) {
@@ -370,8 +378,54 @@ cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, i
   const int64_t work_rows = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
   int64_t grid = (work_rows + rs.warps - 1) / rs.warps;
   if (grid > (int64_t)sms * occ) grid = (int64_t)sms * occ;
-  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages);
+  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, nullptr);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free FP8 broadcast producer (see nvfp4ap.h,
+// ada_layer_norm_quant_fp8_bf16_noalloc): the ring kernel's per-CTA words
+// live in this fixed array instead of any allocated buffer.
+// ---------------------------------------------------------------------------
+
+constexpr int kNoAllocMaxCtas = 1024;  // 4 KB, held by every device that loads the library
+static __device__ __align__(256) unsigned int g_noalloc_cta_state[kNoAllocMaxCtas];
+
+// Device address of g_noalloc_cta_state on the current device, looked up once
+// per device (the host-side name is only a stand-in for the device symbol).
+static unsigned int* noalloc_scratch(int dev) {
+  static std::mutex mu;
+  static unsigned int* addr[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_cta_state) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
+
+int noalloc_fp8_bcast(const LnArgs& a, int sms, cudaStream_t st) {
+  // ring shape as for the allocating path: 8 warps, up to 4 stages in ~110 KB
+  RingShape rs{8, 4, 0};
+  while (rs.stages > 1 && ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages) > 110 * 1024) --rs.stages;
+  while (rs.warps > 1 && ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages) > 110 * 1024) --rs.warps;
+  const int64_t smem = ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages);
+  if (smem > 227 * 1024) return 3;  // NVFP4AP_ERR_DIM
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 6;
+  unsigned int* state = noalloc_scratch(dev);
+  if (!state) return 6;  // NVFP4AP_ERR_LAUNCH
+  RingKernel k = ln_ring_kernel<KIND_FP8, MOD_BCAST>;
+  const int occ = ring_occupancy(k, rs.warps * 32, smem);
+  if (occ < 1) return 6;
+  int64_t grid = (a.rows + rs.warps - 1) / rs.warps;
+  if (grid > (int64_t)sms * occ) grid = (int64_t)sms * occ;
+  if (grid > kNoAllocMaxCtas) return 9;  // NVFP4AP_ERR_SCRATCH
+  if (cudaMemsetAsync(state, 0, (size_t)grid * sizeof(unsigned int), st) != cudaSuccess) return 6;
+  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, state);
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
 
 cudaError_t take_ring_fault(unsigned int* fault) {

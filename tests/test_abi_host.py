@@ -39,12 +39,12 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 11
+    assert len(declared) == 12
 
 
 def test_status_strings_and_version(lib):
     L, _ = lib
-    for s in range(9):
+    for s in range(10):
         assert L.nvfp4ap_status_string(s)
     assert L.nvfp4ap_status_string(99) == b"unknown status"
     assert L.nvfp4ap_version() >= 100
@@ -126,3 +126,16 @@ def test_modulation6_argument_errors(lib):
     assert f(A + 2, A, outs, 1, 4, 64, NULL) == 5              # params not 4-byte aligned
     assert f(A, A, six(A, A, A, A, A + 1, A), 1, 4, 64, NULL) == 5
     assert f(NULL, NULL, outs, 0, 4, 64, NULL) == 0            # no tokens: no-op
+
+
+def test_noalloc_argument_errors(lib):
+    L, _ = lib
+    f = L.ada_layer_norm_quant_fp8_bf16_noalloc
+    f.restype = ctypes.c_int
+    p, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [p, p, p, p, f32, p, i64, i64, p]
+    assert f(A, A, A, A, 1e-5, A, 4, 60, NULL) == 3            # dim not a multiple of 8
+    assert f(A, A, A, A, 1e-5, A, -4, 64, NULL) == 2
+    assert f(A + 4, A, A, A, 1e-5, A, 4, 64, NULL) == 5        # x not 16-byte aligned
+    assert f(A, A, A, A, 1e-5, NULL, 4, 64, NULL) == 1
+    assert f(NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0
