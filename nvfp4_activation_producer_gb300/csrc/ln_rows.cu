@@ -91,16 +91,19 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
   const float K = active ? __uint_as_float((uint32_t)__ldg(a.x + rbase) << 16) : 0.f;
 
   // ---- statistics: one pass, shifted by K -------------------------------------
+  // dk = x - K stays in registers (fp32) for the output step.
+  float2 dk[NV][4];
   float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
   const float2 nk = splat2(-K);
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    if (t + k * tpr < nch) {
+    const bool valid = t + k * tpr < nch;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 d = add2(bf16x2_to_f2(xw[k][i]), nk);
-        s1 = add2(s1, d);
-        s2 = fma2(d, d, s2);
+    for (int i = 0; i < 4; ++i) {
+      dk[k][i] = add2(bf16x2_to_f2(xw[k][i]), nk);
+      if (valid) {
+        s1 = add2(s1, dk[k][i]);
+        s2 = fma2(dk[k][i], dk[k][i], s2);
       }
     }
   }
@@ -130,11 +133,10 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
     }
     return;
   }
-  const float m1 = s.x * inv_d;
-  const float mean = K + m1;
+  const float m1 = s.x * inv_d;  // mean - K
   const float var = fmaxf(fmaf(s.y, inv_d, -m1 * m1), 0.f);
   const float rstd = rsqrtf(var + a.eps);
-  const float2 nmean = splat2(-mean);
+  const float2 nm1 = splat2(-m1);  // x - mean = dk - m1
 
   if constexpr (KIND == KIND_FP8) {
     // ---- FP8: q = (x - mean) * rstd * (1 + scale) + shift) / act_scale ------
@@ -153,18 +155,29 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
 #pragma unroll
         for (int i = 0; i < 4; ++i) { sc[i] = sw[k][i]; sh[i] = hw[k][i]; }
       }
+      float2 tg[4], th[4];
+      if constexpr (MOD == MOD_TABLE) {
+        // the two fp32 table rows of this chunk, 32 bytes each
+        const float* ts = a.table + a.scale_idx * D + (int64_t)j * 8;
+        const float* tsh = a.table + a.shift_idx * D + (int64_t)j * 8;
+        const float4 t0 = ld_reuse_f4(ts), t1 = ld_reuse_f4(ts + 4), u0 = ld_reuse_f4(tsh), u1 = ld_reuse_f4(tsh + 4);
+        tg[0] = make_float2(t0.x, t0.y); tg[1] = make_float2(t0.z, t0.w);
+        tg[2] = make_float2(t1.x, t1.y); tg[3] = make_float2(t1.z, t1.w);
+        th[0] = make_float2(u0.x, u0.y); th[1] = make_float2(u0.z, u0.w);
+        th[2] = make_float2(u1.x, u1.y); th[3] = make_float2(u1.z, u1.w);
+      }
       uint32_t q[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 d = add2(bf16x2_to_f2(xw[k][i]), nmean);
+        const float2 d = add2(dk[k][i], nm1);
         float2 y;
         if constexpr (MOD == MOD_NONE) {
           y = mul2(d, rinv2);
         } else {
           float2 g = bf16x2_to_f2(sc[i]), h = bf16x2_to_f2(sh[i]);
           if constexpr (MOD == MOD_TABLE) {
-            g = add2(g, ld_reuse_f2(a.table + a.scale_idx * D + (int64_t)j * 8 + 2 * i));
-            h = add2(h, ld_reuse_f2(a.table + a.shift_idx * D + (int64_t)j * 8 + 2 * i));
+            g = add2(g, tg[i]);
+            h = add2(h, th[i]);
           }
           y = mul2(fma2(d, fma2(g, rstd2, rstd2), h), inv2);
         }
@@ -177,7 +190,10 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
     const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
     const float2 rstd2 = splat2(rstd);
     uint8_t* prow = reinterpret_cast<uint8_t*>(a.out) + row * (D >> 1);
-    uint8_t* sf = reinterpret_cast<uint8_t*>(a.sf);
+    // this row's part of the 128x4 tiled scale offset; a block column c adds
+    // (c / 4) * 512 + c % 4
+    uint8_t* sfrow = reinterpret_cast<uint8_t*>(a.sf) + (row >> 7) * (int64_t)ct * 512 +
+                     (int)((row & 31) << 4) + (int)(((row >> 5) & 3) << 2);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 d = add2(bf16x2_to_f2(xw[k][i]), nmean);
+          const float2 d = add2(dk[k][i], nm1);
           float2 y;
           if constexpr (MOD == MOD_BCAST)
             y = fma2(d, fma2(bf16x2_to_f2(sc[i]), rstd2, rstd2), bf16x2_to_f2(sh[i]));
@@ -205,26 +221,33 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
       float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
       amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
       // e4m3(amax/6) via the fp32 constant 1/6 gives the byte of the exact
-      // quotient (see ln_nvfp4.cu); the e2m1 decision uses a quotient that is
-      // exact at every midpoint (q0 = v*rcp(s), one exact-remainder step).
+      // quotient (see ln_nvfp4.cu).
       const uint32_t sbyte = f2_to_e4m3x2(make_float2(amax * (1.0f / 6.0f), 0.f)) & 0xFFu;
       const float scl = e4m3_to_f32(sbyte);
-      const float r = (scl == 0.f) ? 0.f : rcp_approx(scl);
-      const float2 r2 = splat2(r), ns2 = splat2(-scl);
+      // v/s as v * (r_hi + r_lo): r_hi ~ 1/s, r_lo = r_hi * (1 - s * r_hi), so
+      // r_hi + r_lo = 1/s to ~2^-44 relative; q = fma(v, r_hi, v * r_lo) is then
+      // the exact quotient rounded once, which equals every representable
+      // midpoint of the e2m1 grid exactly and is otherwise far closer to v/s than
+      // v/s is to any midpoint.  s = 0 gives r = 0 and q = +-0 (sign of v).
+      const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
+      const float rl = rh * fmaf(-scl, rh, 1.0f);
+      const float2 rh2 = splat2(rh), rl2 = splat2(rl);
       float2 q[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 v = bf16x2_to_f2(vb[i]);
-        const float2 q0 = mul2(v, r2);
-        q[i] = fma2(fma2(q0, ns2, v), r2, q0);
+        q[i] = fma2(v, rh2, mul2(v, rl2));
       }
       const uint32_t codes = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
       if (valid) {
         st_stream_b32(prow + (int64_t)j * 4, codes);
-        if ((j & 1) == 0) st_b8(sf + sf_off(row, j >> 1, ct), sbyte);
+        if ((j & 1) == 0) {
+          const int c = j >> 1;
+          st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte);
+        }
       }
     }
-    for (int c = nblk + t; c < padc; c += tpr) st_b8(sf + sf_off(row, c, ct), 0u);
+    for (int c = nblk + t; c < padc; c += tpr) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
   }
 }
 

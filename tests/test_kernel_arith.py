@@ -1,0 +1,87 @@
+"""CPU checks of the arithmetic shortcuts the NVFP4 kernels rely on.
+
+The kernels take two decisions through cheaper fp32 sequences than the
+oracle's exact ones; these tests replay those sequences in numpy (float32
+steps, fused multiply-add emulated in float64, where the product is exact) over
+every case that can matter, and compare with exact rational arithmetic:
+
+1. block scale: e4m3(amax * fp32(1/6)) == e4m3(amax / 6) for every finite
+   non-negative bf16 amax (torch's e4m3 conversion, saturating at 448);
+2. e2m1 decision: q = fma(v, r_hi, v * r_lo) with r_hi ~ 1/s (the hardware
+   reciprocal, allowed to be off by up to 2 ulp) and r_lo = r_hi * (1 - s*r_hi)
+   rounds to the same e2m1 code as the exact v/s, for every e4m3 scale s, at
+   every midpoint (ties) and on bf16 values around them.
+"""
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+F32 = np.float32
+
+
+def _e4m3(vals: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.asarray(vals, dtype=np.float32)).clamp(max=448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_block_scale_by_multiplication_equals_division():
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)  # every finite non-negative bf16
+    amax = (bits << 16).view(np.float32)
+    by_mul = _e4m3(amax * F32(1.0 / 6.0))
+    exact = _e4m3((amax.astype(np.float64) / 6.0).astype(np.float32))
+    assert np.array_equal(by_mul, exact)
+
+
+def _fma32(a, b, c):
+    return (a.astype(np.float64) * b.astype(np.float64) + c.astype(np.float64)).astype(np.float32)
+
+
+MIDS = [Fraction(1, 4), Fraction(3, 4), Fraction(5, 4), Fraction(7, 4), Fraction(5, 2), Fraction(7, 2), Fraction(5)]
+GRID = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+
+
+def _code_exact(v: Fraction, s: Fraction) -> int:
+    q = abs(v) / s
+    d = [abs(q - g) for g in GRID]
+    best = min(d)
+    c = [k for k, x in enumerate(d) if x == best]
+    return c[0] if len(c) == 1 else [k for k in c if k % 2 == 0][0]
+
+
+def _code_rne32(q: np.ndarray) -> np.ndarray:
+    # nearest of the e2m1 grid, ties to even, on float32 quotients
+    a = np.abs(q.astype(np.float64))
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    d = np.abs(a[:, None] - grid[None, :])
+    best = d.min(axis=1, keepdims=True)
+    tie = (d == best)
+    even = tie & (np.arange(8)[None, :] % 2 == 0)
+    return np.where(tie.sum(axis=1) > 1, even.argmax(axis=1), tie.argmax(axis=1))
+
+
+def test_e2m1_quotient_is_exact_at_midpoints_for_every_scale():
+    scales = torch.arange(1, 0x7F, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for s in scales:
+        s32 = F32(s)
+        base = F32(1.0) / s32
+        for ulps in (-2, -1, 0, 1, 2):
+            rh = np.nextafter(base, F32(np.inf if ulps > 0 else -np.inf), dtype=np.float32) if ulps else base
+            for _ in range(abs(ulps) - 1):
+                rh = np.nextafter(rh, F32(np.inf if ulps > 0 else -np.inf), dtype=np.float32)
+            rl = F32(rh * _fma32(np.array([-s32]), np.array([rh]), np.array([F32(1)]))[0])
+            # ties and their bf16 neighbours, both signs
+            vals = []
+            for m in MIDS:
+                v = float(m) * float(s)
+                b = torch.tensor([v], dtype=torch.float64).float().to(torch.bfloat16)
+                if float(b) != v:
+                    continue  # not representable as a bf16 v: no tie possible
+                bits = int(b.view(torch.int16))
+                for k in (-1, 0, 1):
+                    vals.append(torch.tensor([bits + k], dtype=torch.int16).view(torch.bfloat16).item())
+            v = np.array(vals + [-x for x in vals], dtype=np.float32)
+            q = _fma32(v, np.full_like(v, rh), (v * rl).astype(np.float32))
+            got = _code_rne32(q)
+            exp = np.array([_code_exact(Fraction(float(x)), Fraction(float(s))) for x in v])
+            assert np.array_equal(got, exp), (s, ulps)
