@@ -224,6 +224,12 @@ LnArgs ln_args(const void* x, float eps, void* out, int64_t rows, int64_t dim) {
 }
 
 }  // namespace
+
+bool pdl_enabled() {
+  const char* v = std::getenv("NVFP4AP_PDL");
+  return !(v && v[0] == '0');
+}
+
 }  // namespace nvfp4ap
 
 using namespace nvfp4ap;

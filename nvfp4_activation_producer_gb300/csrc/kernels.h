@@ -7,6 +7,26 @@
 
 namespace nvfp4ap {
 
+// Launch `k` on `st` with programmatic stream serialisation (PDL) unless
+// NVFP4AP_PDL=0: the kernel may then be dispatched while the previous kernel
+// on the stream drains (the kernel itself waits for it, see pdl_enter()).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // modulation source of a LayerNorm producer
 enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3 };
 

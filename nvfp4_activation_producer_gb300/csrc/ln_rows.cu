@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
   const int64_t row = (int64_t)blockIdx.x * blockDim.y + ry;
   const bool active = row < a.rows;
   const int64_t rbase = active ? row * D : 0;
+  pdl_enter();
 
   // ---- all loads of the row first -------------------------------------------
   uint32_t xw[NV][4];
@@ -194,56 +195,74 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
     // (c / 4) * 512 + c % 4
     uint8_t* sfrow = reinterpret_cast<uint8_t*>(a.sf) + (row >> 7) * (int64_t)ct * 512 +
                      (int)((row & 31) << 4) + (int)(((row >> 5) & 3) << 2);
+    // Phase by phase over the thread's chunks, so that the chunks' dependency
+    // chains (stage -> block max -> partner shuffle -> scale -> quotient ->
+    // conversion) interleave instead of running one after another.
+    uint32_t vb[NV][4];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
-      if (k * tpr >= nch) break;  // the same for every thread of the row
       const bool valid = j < nch;
-      uint32_t vb[4] = {0u, 0u, 0u, 0u};
-      if (valid) {
-        uint32_t sc[4], sh[4];
-        if constexpr (MOD == MOD_BCAST) {
+      uint32_t sc[4], sh[4];
+      if constexpr (MOD == MOD_BCAST) {
+        if (valid) {
           unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
           unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
-        }
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 d = add2(dk[k][i], nm1);
-          float2 y;
-          if constexpr (MOD == MOD_BCAST)
-            y = fma2(d, fma2(bf16x2_to_f2(sc[i]), rstd2, rstd2), bf16x2_to_f2(sh[i]));
-          else
-            y = mul2(d, rstd2);
-          vb[i] = f2_to_bf16x2(y);
+          for (int i = 0; i < 4; ++i) sc[i] = sh[i] = 0u;
         }
       }
-      const uint32_t m = bf16x2_absmax(bf16x2_absmax(vb[0], vb[1]), bf16x2_absmax(vb[2], vb[3]));
-      float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 d = add2(dk[k][i], nm1);
+        float2 y;
+        if constexpr (MOD == MOD_BCAST)
+          y = fma2(d, fma2(bf16x2_to_f2(sc[i]), rstd2, rstd2), bf16x2_to_f2(sh[i]));
+        else
+          y = mul2(d, rstd2);
+        vb[k][i] = valid ? f2_to_bf16x2(y) : 0u;
+      }
+    }
+    float amax[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const uint32_t m = bf16x2_absmax(bf16x2_absmax(vb[k][0], vb[k][1]), bf16x2_absmax(vb[k][2], vb[k][3]));
+      amax[k] = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
+    }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xFFFFFFFFu, amax[k], 1));
+    uint32_t sbyte[NV], codes[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
       // e4m3(amax/6) via the fp32 constant 1/6 gives the byte of the exact
       // quotient (see ln_nvfp4.cu).
-      const uint32_t sbyte = f2_to_e4m3x2(make_float2(amax * (1.0f / 6.0f), 0.f)) & 0xFFu;
-      const float scl = e4m3_to_f32(sbyte);
+      sbyte[k] = f2_to_e4m3x2(make_float2(amax[k] * (1.0f / 6.0f), 0.f)) & 0xFFu;
+      const float scl = e4m3_to_f32(sbyte[k]);
       // v/s as v * (r_hi + r_lo): r_hi ~ 1/s, r_lo = r_hi * (1 - s * r_hi), so
       // r_hi + r_lo = 1/s to ~2^-44 relative; q = fma(v, r_hi, v * r_lo) is then
       // the exact quotient rounded once, which equals every representable
-      // midpoint of the e2m1 grid exactly and is otherwise far closer to v/s than
-      // v/s is to any midpoint.  s = 0 gives r = 0 and q = +-0 (sign of v).
+      // midpoint of the e2m1 grid exactly and is otherwise far closer to v/s
+      // than v/s is to any midpoint.  s = 0 gives r = 0 and q = +-0.
       const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
       const float rl = rh * fmaf(-scl, rh, 1.0f);
       const float2 rh2 = splat2(rh), rl2 = splat2(rl);
       float2 q[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 v = bf16x2_to_f2(vb[i]);
+        const float2 v = bf16x2_to_f2(vb[k][i]);
         q[i] = fma2(v, rh2, mul2(v, rl2));
       }
-      const uint32_t codes = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
-      if (valid) {
-        st_stream_b32(prow + (int64_t)j * 4, codes);
+      codes[k] = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
+    }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j = t + k * tpr;
+      if (j < nch) {
+        st_stream_b32(prow + (int64_t)j * 4, codes[k]);
         if ((j & 1) == 0) {
           const int c = j >> 1;
-          st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte);
+          st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte[k]);
         }
       }
     }
@@ -258,10 +277,9 @@ cudaError_t launch_nv(const LnArgs& a, RowShape s, cudaStream_t st) {
   const dim3 block(s.tpr, s.rpc);
   const dim3 grid((unsigned)((work_rows + s.rpc - 1) / s.rpc));
   const float inv_d = (float)(1.0 / (double)a.dim);
-#define NVFP4AP_CASE(N)                                                    \
-  case N:                                                                  \
-    ln_rows_kernel<KIND, MOD, N><<<grid, block, 0, st>>>(a, inv_d);        \
-    break;
+#define NVFP4AP_CASE(N)                                                            \
+  case N:                                                                          \
+    return launch_maybe_pdl(ln_rows_kernel<KIND, MOD, N>, grid, block, 0, st, a, inv_d);
   if constexpr (kPerToken) {
     switch (s.per_thread) {
       NVFP4AP_CASE(1)

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) mod6_vec8_kernel(const float* __rest
   const int i = blockIdx.y;
   const IDX base = (IDX)blockIdx.x * (kThreads * kUnroll) + threadIdx.x;
   const float* pbase = params + (int64_t)i * dim;
+  pdl_enter();
   uint4 p0[kUnroll], p1[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
@@ -96,11 +97,11 @@ cudaError_t launch_modulation6(const Mod6Args& a, bool vec8, cudaStream_t st) {
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)gx, 6);
     if (total + per_cta < ((int64_t)1 << 31))
-      mod6_vec8_kernel<uint32_t><<<grid, kThreads, 0, st>>>(a.params, a.modulation, o, (uint32_t)nch,
-                                                            (uint32_t)total, a.dim);
+      return launch_maybe_pdl(mod6_vec8_kernel<uint32_t>, grid, dim3(kThreads), 0, st, a.params, a.modulation, o,
+                              (uint32_t)nch, (uint32_t)total, a.dim);
     else
-      mod6_vec8_kernel<uint64_t><<<grid, kThreads, 0, st>>>(a.params, a.modulation, o, (uint64_t)nch,
-                                                            (uint64_t)total, a.dim);
+      return launch_maybe_pdl(mod6_vec8_kernel<uint64_t>, grid, dim3(kThreads), 0, st, a.params, a.modulation, o,
+                              (uint64_t)nch, (uint64_t)total, a.dim);
   } else {
     const int64_t total = a.tokens * a.dim;  // elements of one output
     int64_t gx = (total + kThreads - 1) / kThreads;
