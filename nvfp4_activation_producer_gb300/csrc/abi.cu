@@ -105,8 +105,17 @@ bool pick_rows(int mod, int64_t dim, RowShape* s) {
   if (!pick_shape(dim / 8, c, n, lim, env_int("NVFP4AP_PER_THREAD"), s) && !pick_shape(dim / 8, c, n, lim, 0, s))
     return false;
   const int want = env_int("NVFP4AP_ROWS_PER_CTA");
-  if (want > 0 && want <= 16 && want * s->tpr <= 1024) s->rpc = want;
+  if (want > 0 && want <= 16 && want * s->tpr <= 512) s->rpc = want;  // the kernels are bounded to 512 threads
   return true;
+}
+
+// The persistent broadcast kernel takes one row per CTA of at most 256
+// threads and up to 6 chunks per thread (NVFP4AP_PERSIST=0 turns it off).
+bool persist_ok(const RowShape& s) {
+  if (env_int("NVFP4AP_PERSIST") < 0) return false;
+  const bool nv_ok = s.per_thread == 1 || s.per_thread == 2 || s.per_thread == 3 || s.per_thread == 4 ||
+                     s.per_thread == 6;
+  return nv_ok && s.tpr <= 256 && s.rpc == 1;
 }
 
 int finish(cudaError_t e) {
@@ -159,6 +168,11 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   RowShape rows_shape{};
   if (vec8 && kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
     if (!grid_ok(a.rows, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
+    if (mod == MOD_BCAST && persist_ok(rows_shape)) {
+      const int sms = sm_count();
+      if (sms > 0)
+        return finish(launch_ln_bcast_persistent(a, false, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
+    }
     return finish(launch_ln_rows(a, false, mod, rows_shape, st));
   }
 
@@ -199,6 +213,11 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
     const int64_t rows_pad = (a.rows + 127) / 128 * 128;
     if (!grid_ok(rows_pad, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
+    if (mod == MOD_BCAST && persist_ok(rows_shape)) {
+      const int sms = sm_count();
+      if (sms > 0)
+        return finish(launch_ln_bcast_persistent(a, true, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
+    }
     return finish(launch_ln_rows(a, true, mod, rows_shape, st));
   }
 

@@ -61,6 +61,12 @@ int ln_fp8_max_tpr(int vec, int per_thread);
 // NVFP4: `per_thread` 8-element chunks per thread.
 cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
 int ln_rows_max_tpr(int mod, int per_thread);
+// Persistent broadcast-modulation variant (one row per CTA at a time, the
+// next row prefetched, fp32 modulation in registers): tpr <= 256, rpc == 1,
+// per_thread in {1, 2, 3, 4, 6}; at most `ctas_per_sm` CTAs per SM (0 = as
+// many as fit).
+cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, RowShape s, int sms, int ctas_per_sm,
+                                       cudaStream_t st);
 
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);

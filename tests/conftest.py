@@ -49,14 +49,20 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["rows", "ring", "legacy"])
+@pytest.fixture(params=["rows", "rows_flat", "ring", "legacy"])
 def path(request, monkeypatch):
     """Run a LayerNorm-producer test on each kernel family: the register row
-    kernels (default), the TMA ring kernels (NVFP4AP_KERNEL=1) and the first
-    register kernels (NVFP4AP_KERNEL=2)."""
-    value = {"rows": None, "ring": "1", "legacy": "2"}[request.param]
+    kernels (default; the broadcast forms on the persistent variant), the
+    row kernels without the persistent variant (NVFP4AP_PERSIST=-1), the TMA
+    ring kernels (NVFP4AP_KERNEL=1) and the first register kernels
+    (NVFP4AP_KERNEL=2)."""
+    value = {"rows": None, "rows_flat": None, "ring": "1", "legacy": "2"}[request.param]
     if value is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
         monkeypatch.setenv("NVFP4AP_KERNEL", value)
+    if request.param == "rows_flat":
+        monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
+    else:
+        monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
     return request.param
