@@ -159,20 +159,23 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
   const int vec = vec8 ? 8 : 2;
 
-  const int kernel = env_int("NVFP4AP_KERNEL");  // 0 rows (default), 1 ring, 2 earlier register kernel
+  // 0 TMA pipeline (default), 1 TMA warp-per-row ring, 2 first register
+  // kernel, 3 register row kernels
+  const int kernel = env_int("NVFP4AP_KERNEL");
   RingShape rs{};
   if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, st));
   }
   RowShape rows_shape{};
-  if (vec8 && kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
+  if (vec8 && (kernel == 0 || kernel == 3) && pick_rows(mod, a.dim, &rows_shape)) {
     if (!grid_ok(a.rows, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
-    if (mod == MOD_BCAST && persist_ok(rows_shape)) {
-      const int sms = sm_count();
-      if (sms > 0)
-        return finish(launch_ln_bcast_persistent(a, false, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
-    }
+    const int sms = sm_count();
+    if (kernel == 0 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
+      return finish(launch_ln_tma(a, false, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
+                                  env_int("NVFP4AP_TMA_CTAS"), st));
+    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0)
+      return finish(launch_ln_bcast_persistent(a, false, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     return finish(launch_ln_rows(a, false, mod, rows_shape, st));
   }
 
@@ -203,21 +206,22 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
 
-  const int kernel = env_int("NVFP4AP_KERNEL");  // 0 rows (default), 1 ring, 2 earlier register kernel
+  const int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8
   RingShape rs{};
   if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, st));
   }
   RowShape rows_shape{};
-  if (kernel == 0 && pick_rows(mod, a.dim, &rows_shape)) {
+  if ((kernel == 0 || kernel == 3) && pick_rows(mod, a.dim, &rows_shape)) {
     const int64_t rows_pad = (a.rows + 127) / 128 * 128;
     if (!grid_ok(rows_pad, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
-    if (mod == MOD_BCAST && persist_ok(rows_shape)) {
-      const int sms = sm_count();
-      if (sms > 0)
-        return finish(launch_ln_bcast_persistent(a, true, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
-    }
+    const int sms = sm_count();
+    if (kernel == 0 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
+      return finish(launch_ln_tma(a, true, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
+                                  env_int("NVFP4AP_TMA_CTAS"), st));
+    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0)
+      return finish(launch_ln_bcast_persistent(a, true, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     return finish(launch_ln_rows(a, true, mod, rows_shape, st));
   }
 
@@ -272,12 +276,12 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
-  unsigned int f = 0u;
-  if (take_ring_fault(&f) != cudaSuccess) {
+  unsigned int f = 0u, g = 0u;
+  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  return f ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  return (f | g) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,

@@ -89,6 +89,14 @@ int noalloc_fp8_bcast(const LnArgs& a, int sms, cudaStream_t st);
 // runs out (synchronising copy).
 cudaError_t take_ring_fault(unsigned int* fault);
 
+// Persistent TMA-pipelined row kernels (ln_tma.cu): one row per CTA at a
+// time (rpc == 1, tpr <= 256, per_thread 1..4), rows staged through a ring of
+// shared-memory stages by bulk copies.  forced_stages / ctas_per_sm: 0 = auto.
+bool ln_tma_supported(bool nvfp4, int mod, RowShape s);
+cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
+                          int ctas_per_sm, cudaStream_t st);
+cudaError_t take_tma_fault(unsigned int* fault);
+
 // Six-way modulation (K7).
 struct Mod6Args {
   const float* params;      // (tokens, 6, dim) fp32

@@ -49,18 +49,18 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["rows", "rows_flat", "ring", "legacy"])
+@pytest.fixture(params=["tma", "rows", "rows_flat", "ring", "legacy"])
 def path(request, monkeypatch):
-    """Run a LayerNorm-producer test on each kernel family: the register row
-    kernels (default; the broadcast forms on the persistent variant), the
-    row kernels without the persistent variant (NVFP4AP_PERSIST=-1), the TMA
-    ring kernels (NVFP4AP_KERNEL=1) and the first register kernels
-    (NVFP4AP_KERNEL=2)."""
-    value = {"rows": None, "rows_flat": None, "ring": "1", "legacy": "2"}[request.param]
-    if value is None:
+    """Run a LayerNorm-producer test on each kernel family: the persistent
+    TMA-pipelined kernels (default), the register row kernels with the
+    persistent broadcast variant (NVFP4AP_KERNEL=3) and without it
+    (NVFP4AP_PERSIST=-1), the warp-per-row TMA ring kernels
+    (NVFP4AP_KERNEL=1) and the first register kernels (NVFP4AP_KERNEL=2)."""
+    kernel = {"tma": None, "rows": "3", "rows_flat": "3", "ring": "1", "legacy": "2"}[request.param]
+    if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
-        monkeypatch.setenv("NVFP4AP_KERNEL", value)
+        monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
     if request.param == "rows_flat":
         monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
     else:

@@ -211,3 +211,41 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
             ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
         check_fp8(_codes(out), ref, _act(w))
     ap.take_device_fault()  # no bounded wait ran out
+
+
+@pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
+def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
+    # one CTA per SM and 1, 2 or 5 stages: each CTA walks ~40 rows, so every
+    # stage's mbarrier goes through many phases and refills
+    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    rows, dim = 6000, 1024
+    for stages in (1, 2, 5):
+        monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))
+        monkeypatch.setenv("NVFP4AP_TMA_CTAS", "1")
+        seed = 40 + stages
+        if op == "table":
+            w = synth.fp8_table(rows, dim, seed=seed, shift_idx=4, scale_idx=2)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"], 4, 2)
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_TABLE,
+                                      temb=synth.u16(w.inputs["temb"]), table=w.inputs["table"].numpy(),
+                                      shift_idx=4, scale_idx=2)
+        elif op == "ptok":
+            w = synth.fp8_ptok(rows, dim, seed=seed)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_ptok_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_PTOK, scale=u["scale"], shift=u["shift"])
+        elif op == "bcast":
+            w = synth.fp8_broadcast(rows, dim, seed=seed)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+        else:
+            w = synth.fp8_ln(rows, dim, seed=seed)
+            d = _d(w, dev)
+            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
+        check_fp8(_codes(out), ref, _act(w))
+    ap.take_device_fault()

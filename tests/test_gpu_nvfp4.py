@@ -142,3 +142,17 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, kind, monkeypatch):
         op, os_, v = _oracle(w, kind)
         check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
     ap.take_device_fault()
+
+
+@pytest.mark.parametrize("kind", ["ln", "bcast"])
+def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
+    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
+    for stages in (1, 3):
+        monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))
+        monkeypatch.setenv("NVFP4AP_TMA_CTAS", "1")
+        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=stages)
+        gp, gs = _run(ap, kind, w, dev)
+        op, os_, v = _oracle(w, kind)
+        check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
+    ap.take_device_fault()
