@@ -6,6 +6,7 @@
 // here allocates, synchronises or touches device memory.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 
 #include <cuda_runtime.h>
@@ -120,6 +121,7 @@ bool persist_ok(const RowShape& s) {
 
 int finish(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4AP_OK;
+  if (env_int("NVFP4AP_DEBUG") > 0) std::fprintf(stderr, "nvfp4ap: launch failed: %s\n", cudaGetErrorString(e));
   (void)cudaGetLastError();
   return NVFP4AP_ERR_LAUNCH;
 }

@@ -23,6 +23,8 @@
 //  * every mbarrier wait is bounded (about one second); a CTA whose wait runs
 //    out (decided CTA-wide at the reduction barrier) waits, again bounded, for
 //    its copies still in flight, sets the fault word and returns.
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "device.cuh"
@@ -347,7 +349,12 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
     if (cache[i].k == k && cache[i].dim == dim && cache[i].tpr == tpr && cache[i].forced == forced_stages &&
         cache[i].dev == dev)
       return cache[i].p;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return {0, 0};
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return {0, 0};
+  const int64_t max_dyn = (int64_t)optin - (int64_t)fa.sharedSizeBytes;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn) != cudaSuccess)
     return {0, 0};
   TmaPlan best{0, 0};
   int64_t best_bytes = -1;
@@ -355,7 +362,7 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
   for (int S = 1; S <= 6; ++S) {
     if (forced_stages > 0 && S != forced_stages) continue;
     const int64_t smem = tma_smem(mod, dim, S);
-    if (smem > 227 * 1024) break;
+    if (smem > max_dyn) break;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, tpr, (size_t)smem) != cudaSuccess) continue;
     const int64_t bytes = (int64_t)occ * S * stage;
@@ -365,6 +372,10 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
     }
   }
   if (n < 128) cache[n++] = Entry{k, dim, tpr, forced_stages, dev, best};
+  if (const char* dbg = std::getenv("NVFP4AP_DEBUG"))
+    if (dbg[0] == '1')
+      std::fprintf(stderr, "nvfp4ap: tma plan dim=%lld tpr=%d: stages=%d ctas/SM=%d\n", (long long)dim, tpr,
+                   best.stages, best.occ);
   return best;
 }
 
