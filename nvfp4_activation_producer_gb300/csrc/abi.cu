@@ -161,19 +161,22 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
   const int vec = vec8 ? 8 : 2;
 
-  // 0 TMA pipeline (default), 1 TMA warp-per-row ring, 2 first register
-  // kernel, 3 register row kernels
-  const int kernel = env_int("NVFP4AP_KERNEL");
+  // NVFP4AP_KERNEL: 0 auto (default: the TMA pipeline for the table form,
+  // the register row kernels otherwise -- the faster family for each form on
+  // GB300 at 2,520-32,768 rows), 1 warp-per-row TMA ring, 2 first register
+  // kernel, 3 register row kernels for every form, 4 TMA pipeline for every form
+  int kernel = env_int("NVFP4AP_KERNEL");
+  if (kernel == 0) kernel = (mod == MOD_TABLE) ? 4 : 3;
   RingShape rs{};
   if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, st));
   }
   RowShape rows_shape{};
-  if (vec8 && (kernel == 0 || kernel == 3) && pick_rows(mod, a.dim, &rows_shape)) {
+  if (vec8 && (kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
     if (!grid_ok(a.rows, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
     const int sms = sm_count();
-    if (kernel == 0 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
+    if (kernel == 4 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
       return finish(launch_ln_tma(a, false, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
                                   env_int("NVFP4AP_TMA_CTAS"), st));
     if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0)
@@ -208,18 +211,19 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
 
-  const int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8
+  int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8; auto = row kernels
+  if (kernel == 0) kernel = 3;
   RingShape rs{};
   if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
     if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, st));
   }
   RowShape rows_shape{};
-  if ((kernel == 0 || kernel == 3) && pick_rows(mod, a.dim, &rows_shape)) {
+  if ((kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
     const int64_t rows_pad = (a.rows + 127) / 128 * 128;
     if (!grid_ok(rows_pad, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
     const int sms = sm_count();
-    if (kernel == 0 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
+    if (kernel == 4 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
       return finish(launch_ln_tma(a, true, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
                                   env_int("NVFP4AP_TMA_CTAS"), st));
     if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0)

@@ -330,10 +330,9 @@ int64_t tma_smem(int mod, int64_t dim, int stages) {
   return ((int64_t)stages * 8 + 127) / 128 * 128 + (int64_t)stages * stage;
 }
 
-// Stages and resident CTAs per SM for (kernel, tpr, dim): the stage count
-// (1..6) that maximises the bytes in flight per SM, occ(S) * S * stage
-// bytes; cached per key and device, queried outside any stream capture on
-// the first call.
+// Stages and resident CTAs per SM for (kernel, tpr, dim), cached per key and
+// device (queried on the first call, which should come before any stream
+// capture).
 struct TmaPlan {
   int stages, occ;
 };
@@ -356,6 +355,8 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
   const int64_t max_dyn = (int64_t)optin - (int64_t)fa.sharedSizeBytes;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn) != cudaSuccess)
     return {0, 0};
+  // fewest stages that keep >= 96 KB per SM in flight (measured best on
+  // GB300: more stages cost resident CTAs), else the most bytes in flight
   TmaPlan best{0, 0};
   int64_t best_bytes = -1;
   const int64_t stage = tma_smem(mod, dim, 1) - 128;
@@ -364,12 +365,14 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
     const int64_t smem = tma_smem(mod, dim, S);
     if (smem > max_dyn) break;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, tpr, (size_t)smem) != cudaSuccess) continue;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, tpr, (size_t)smem) != cudaSuccess || occ < 1)
+      continue;
     const int64_t bytes = (int64_t)occ * S * stage;
-    if (occ >= 1 && bytes > best_bytes) {
+    if (bytes > best_bytes) {
       best_bytes = bytes;
       best = {S, occ};
     }
+    if (bytes >= 96 * 1024) break;
   }
   if (n < 128) cache[n++] = Entry{k, dim, tpr, forced_stages, dev, best};
   if (const char* dbg = std::getenv("NVFP4AP_DEBUG"))

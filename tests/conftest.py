@@ -49,14 +49,15 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["tma", "rows", "rows_flat", "ring", "legacy"])
+@pytest.fixture(params=["auto", "rows", "rows_flat", "tma", "ring", "legacy"])
 def path(request, monkeypatch):
-    """Run a LayerNorm-producer test on each kernel family: the persistent
-    TMA-pipelined kernels (default), the register row kernels with the
-    persistent broadcast variant (NVFP4AP_KERNEL=3) and without it
-    (NVFP4AP_PERSIST=-1), the warp-per-row TMA ring kernels
-    (NVFP4AP_KERNEL=1) and the first register kernels (NVFP4AP_KERNEL=2)."""
-    kernel = {"tma": None, "rows": "3", "rows_flat": "3", "ring": "1", "legacy": "2"}[request.param]
+    """Run a LayerNorm-producer test on each kernel family: the default choice
+    (TMA pipeline for the table form, register row kernels otherwise), the
+    register row kernels for every form (NVFP4AP_KERNEL=3) with and without
+    the persistent broadcast variant (NVFP4AP_PERSIST=-1), the TMA pipeline
+    for every form (4), the warp-per-row TMA ring (1) and the first register
+    kernels (2)."""
+    kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tma": "4", "ring": "1", "legacy": "2"}[request.param]
     if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:

@@ -217,7 +217,7 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
 def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
     # one CTA per SM and 1, 2 or 5 stages: each CTA walks ~40 rows, so every
     # stage's mbarrier goes through many phases and refills
-    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    monkeypatch.setenv("NVFP4AP_KERNEL", "4")
     rows, dim = 6000, 1024
     for stages in (1, 2, 5):
         monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))

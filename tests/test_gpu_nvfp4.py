@@ -146,7 +146,7 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, kind, monkeypatch):
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
-    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    monkeypatch.setenv("NVFP4AP_KERNEL", "4")
     rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
     for stages in (1, 3):
         monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))
