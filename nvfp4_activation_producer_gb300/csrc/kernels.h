@@ -61,6 +61,10 @@ int ln_fp8_max_tpr(int vec, int per_thread);
 // NVFP4: `per_thread` 8-element chunks per thread.
 cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
 int ln_rows_max_tpr(int mod, int per_thread);
+// NVFP4 row kernel with four rows of one 128-row tile per CTA (rows r, r+32,
+// r+64, r+96): scale bytes leave as whole 16-byte chunks.  tpr <= 128,
+// per_thread 1..4, 16-byte aligned scale buffer.
+cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 // Persistent broadcast-modulation variant (one row per CTA at a time, the
 // next row prefetched, fp32 modulation in registers): tpr <= 256, rpc == 1,
 // per_thread in {1, 2, 3, 4, 6}; at most `ctas_per_sm` CTAs per SM (0 = as

@@ -49,17 +49,24 @@ __host__ __device__ constexpr int rows_max_tpr(int nv) {
   return ((4096 + nv - 1) / nv + 31) / 32 * 32 > 512 ? 512 : ((4096 + nv - 1) / nv + 31) / 32 * 32;
 }
 
-template <int KIND, int MOD, int NV>
+// TILE4 (NVFP4 only, blockDim.y == 4): the CTA owns rows t0 + r32 + 32*ry of
+// one 128-row tile (t0 = 128 * (blockIdx.x / 32), r32 = blockIdx.x % 32), so
+// the four rows' scale bytes of every 4-column group form one contiguous
+// 16-byte chunk of the 128x4 layout; they are gathered in shared memory and
+// written with one 16-byte store per chunk (padding rows and columns as 0).
+template <int KIND, int MOD, int NV, bool TILE4 = false>
 __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const float inv_d) {
   constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
   __shared__ float2 red[16][16];  // [row group][warp of the row]
+  __shared__ uint32_t sft[TILE4 ? 4 : 1][TILE4 ? 1024 : 1];  // [row group][4-column group]: 4 scale bytes
 
   const int tpr = blockDim.x;
   const int t = threadIdx.x, ry = threadIdx.y;
   const int lane = t & 31, warp = t >> 5, nwarps = tpr >> 5;
   const int64_t D = a.dim;
   const int nch = (int)(D >> 3);
-  const int64_t row = (int64_t)blockIdx.x * blockDim.y + ry;
+  const int64_t row = TILE4 ? (int64_t)(blockIdx.x >> 5) * 128 + (blockIdx.x & 31) + 32 * ry
+                            : (int64_t)blockIdx.x * blockDim.y + ry;
   const bool active = row < a.rows;
   const int64_t rbase = active ? row * D : 0;
   pdl_enter();
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
       s.y += u.y;
     }
   }
-  if (!active) {
+  if (!active && !TILE4) {
     if constexpr (KIND == KIND_NVFP4) {
       // rows past the end inside the last 128-row tile: zero scale bytes
       const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
@@ -257,18 +264,53 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
       }
       codes[k] = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
     }
+    if constexpr (TILE4) {
+      // gather this row's scale bytes: lane j (even) holds column j/2; the four
+      // columns of group g sit in lanes 8g, 8g+2, 8g+4, 8g+6 of the warp
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int j = t + k * tpr;
-      if (j < nch) {
-        st_stream_b32(prow + (int64_t)j * 4, codes[k]);
-        if ((j & 1) == 0) {
-          const int c = j >> 1;
-          st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte[k]);
+      for (int k = 0; k < NV; ++k) {
+        const int j = t + k * tpr;
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 2);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 4);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 6);
+        if (j < nch) {
+          if (active) st_stream_b32(prow + (int64_t)j * 4, codes[k]);
+          if ((j & 7) == 0) {
+            // columns 4g..4g+3 (g = j/8); those at or past nblk are padding (0)
+            const int c0 = j >> 1;
+            uint32_t w = 0u;
+            if (active) {
+              w = sbyte[k];
+              if (c0 + 1 < nblk) w |= b1 << 8;
+              if (c0 + 2 < nblk) w |= b2 << 16;
+              if (c0 + 3 < nblk) w |= b3 << 24;
+            }
+            sft[ry][j >> 3] = w;
+          }
         }
       }
+    } else {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int j = t + k * tpr;
+        if (j < nch) {
+          st_stream_b32(prow + (int64_t)j * 4, codes[k]);
+          if ((j & 1) == 0) {
+            const int c = j >> 1;
+            st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte[k]);
+          }
+        }
+      }
+      for (int c = nblk + t; c < padc; c += tpr) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
     }
-    for (int c = nblk + t; c < padc; c += tpr) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
+    if constexpr (TILE4) {
+      // the CTA's four rows are done: one 16-byte chunk per 4-column group
+      __syncthreads();
+      uint8_t* base = reinterpret_cast<uint8_t*>(a.sf) + (int64_t)(blockIdx.x >> 5) * ct * 512 +
+                      (int)((blockIdx.x & 31) << 4);
+      for (int g = ry * tpr + t; g < ct; g += 4 * tpr)
+        st_stream_v4(base + (int64_t)g * 512, make_uint4(sft[0][g], sft[1][g], sft[2][g], sft[3][g]));
+    }
   }
 }
 
@@ -540,6 +582,35 @@ cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, RowShape s, 
   if (s.tpr > 256 || s.rpc != 1) return cudaErrorInvalidValue;
   return nvfp4 ? launch_persist<KIND_NVFP4>(a, s, sms, ctas_per_sm, st)
                : launch_persist<KIND_FP8>(a, s, sms, ctas_per_sm, st);
+}
+
+cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStream_t st) {
+  if (s.tpr > 128) return cudaErrorInvalidValue;
+  const int64_t rows_pad = (a.rows + 127) / 128 * 128;
+  const dim3 block(s.tpr, 4), grid((unsigned)(rows_pad / 4));
+  const float inv_d = (float)(1.0 / (double)a.dim);
+#define NVFP4AP_CASE(M, N)                                                                          \
+  case N:                                                                                           \
+    return launch_maybe_pdl(ln_rows_kernel<KIND_NVFP4, M, N, true>, grid, block, 0, st, a, inv_d);
+  if (mod == MOD_NONE) {
+    switch (s.per_thread) {
+      NVFP4AP_CASE(MOD_NONE, 1)
+      NVFP4AP_CASE(MOD_NONE, 2)
+      NVFP4AP_CASE(MOD_NONE, 3)
+      NVFP4AP_CASE(MOD_NONE, 4)
+      default: return cudaErrorInvalidValue;
+    }
+  } else if (mod == MOD_BCAST) {
+    switch (s.per_thread) {
+      NVFP4AP_CASE(MOD_BCAST, 1)
+      NVFP4AP_CASE(MOD_BCAST, 2)
+      NVFP4AP_CASE(MOD_BCAST, 3)
+      NVFP4AP_CASE(MOD_BCAST, 4)
+      default: return cudaErrorInvalidValue;
+    }
+  }
+#undef NVFP4AP_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st) {

@@ -54,7 +54,8 @@ def path(request, monkeypatch):
     """Run a LayerNorm-producer test on each kernel family: the default choice
     (TMA pipeline for the table form, register row kernels otherwise), the
     register row kernels for every form (NVFP4AP_KERNEL=3) with and without
-    the persistent broadcast variant (NVFP4AP_PERSIST=-1), the TMA pipeline
+    the persistent broadcast and the NVFP4 four-row-tile variants
+    (NVFP4AP_PERSIST=-1, NVFP4AP_TILE4=-1), the TMA pipeline
     for every form (4), the warp-per-row TMA ring (1) and the first register
     kernels (2)."""
     kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tma": "4", "ring": "1", "legacy": "2"}[request.param]
@@ -64,6 +65,8 @@ def path(request, monkeypatch):
         monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
     if request.param == "rows_flat":
         monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
+        monkeypatch.setenv("NVFP4AP_TILE4", "-1")
     else:
         monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
+        monkeypatch.delenv("NVFP4AP_TILE4", raising=False)
     return request.param

@@ -22,10 +22,10 @@ SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (128,
           (5, 32768), (257, 1536), (51, 1152)]
 
 
-def _run(ap, fn_kind, w, dev, guard=4096):
+def _run(ap, fn_kind, w, dev, guard=4096, sf_shift=0):
     rows, dim = w.rows, w.dim
     n = ap.swizzled_sf_size(rows, dim)
-    sfbuf = torch.full((n + 2 * guard,), 0xFF, dtype=torch.uint8, device=dev)
+    sfbuf = torch.full((n + 2 * guard + sf_shift,), 0xFF, dtype=torch.uint8, device=dev)[sf_shift:]
     pkbuf = torch.full((rows * dim // 2 + 2 * guard,), 0xEE, dtype=torch.uint8, device=dev)
     sf = sfbuf[guard:guard + n]
     packed = pkbuf[guard:guard + rows * dim // 2].view(rows, dim // 2)
@@ -156,3 +156,12 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
         op, os_, v = _oracle(w, kind)
         check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
     ap.take_device_fault()
+
+
+@pytest.mark.parametrize("kind", ["ln", "bcast"])
+def test_unaligned_scale_buffer(ap, dev, kind):
+    # a scale buffer off 16-byte alignment takes the byte-store path
+    w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(300, 3072, seed=17)
+    gp, gs = _run(ap, kind, w, dev, sf_shift=4)
+    op, os_, v = _oracle(w, kind)
+    check_nvfp4(gp, gs, op, os_, 300, 3072, v_orc=v)
