@@ -226,10 +226,11 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
     if (kernel == 4 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
       return finish(launch_ln_tma(a, true, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
                                   env_int("NVFP4AP_TMA_CTAS"), st));
-    // four rows of a scale tile per CTA when the shape allows (NVFP4AP_TILE4=-1 off)
-    const bool tile4 = env_int("NVFP4AP_TILE4") >= 0 && rows_shape.tpr <= 128 && rows_shape.per_thread <= 4 &&
+    // four rows of a scale tile per CTA (whole 16-byte scale chunks): opt-in
+    // with NVFP4AP_TILE4=1 -- measured slower on GB300 than one row per CTA
+    const bool tile4 = env_int("NVFP4AP_TILE4") > 0 && rows_shape.tpr <= 128 && rows_shape.per_thread <= 4 &&
                        aligned(a.sf, 16);
-    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0 && env_int("NVFP4AP_TILE4") <= 0 && !tile4)
+    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0 && !tile4)
       return finish(launch_ln_bcast_persistent(a, true, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     if (tile4) return finish(launch_ln_rows_tile4(a, mod, rows_shape, st));
     return finish(launch_ln_rows(a, true, mod, rows_shape, st));

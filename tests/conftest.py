@@ -49,24 +49,27 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["auto", "rows", "rows_flat", "tma", "ring", "legacy"])
+@pytest.fixture(params=["auto", "rows", "rows_flat", "tile4", "tma", "ring", "legacy"])
 def path(request, monkeypatch):
     """Run a LayerNorm-producer test on each kernel family: the default choice
     (TMA pipeline for the table form, register row kernels otherwise), the
     register row kernels for every form (NVFP4AP_KERNEL=3) with and without
-    the persistent broadcast and the NVFP4 four-row-tile variants
-    (NVFP4AP_PERSIST=-1, NVFP4AP_TILE4=-1), the TMA pipeline
+    the persistent broadcast variant (NVFP4AP_PERSIST=-1), the NVFP4
+    four-row-tile variant (NVFP4AP_TILE4=1), the TMA pipeline
     for every form (4), the warp-per-row TMA ring (1) and the first register
     kernels (2)."""
-    kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tma": "4", "ring": "1", "legacy": "2"}[request.param]
+    kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tile4": "3", "tma": "4", "ring": "1",
+              "legacy": "2"}[request.param]
     if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
         monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
     if request.param == "rows_flat":
         monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
-        monkeypatch.setenv("NVFP4AP_TILE4", "-1")
     else:
         monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
+    if request.param == "tile4":
+        monkeypatch.setenv("NVFP4AP_TILE4", "1")
+    else:
         monkeypatch.delenv("NVFP4AP_TILE4", raising=False)
     return request.param
