@@ -10,7 +10,7 @@ passed as ``uint16`` bit patterns, e4m3 and packed e2m1 as ``uint8``.
 
 Sources: the adaptive-layernorm-producers README ("Available Functions",
 "Tensor Contract", "Minimal Usage", "Validation") and the NVFP4 facts of the
-h3-blackwell-runtime compare page (see ``orc.c`` for the readings R1-R8).
+h3-blackwell-runtime compare page (see ``orc.c`` for the readings R1-R8, R15, R16).
 """
 from __future__ import annotations
 
@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "orc.c")
 _HDR = os.path.join(_HERE, "orc.h")
 _SO = os.path.join(_HERE, "liborc.so")
 
-MOD_NONE, MOD_BCAST, MOD_PTOK, MOD_TABLE = 0, 1, 2, 3
+MOD_NONE, MOD_BCAST, MOD_PTOK, MOD_TABLE, MOD_MODFP8, MOD_AWQ = 0, 1, 2, 3, 4, 5
 
 
 def build(force: bool = False) -> str:
@@ -46,7 +46,10 @@ class _Mod(ctypes.Structure):
                 ("scale", ctypes.c_void_p), ("shift", ctypes.c_void_p),
                 ("temb", ctypes.c_void_p), ("table", ctypes.c_void_p),
                 ("chunks", ctypes.c_int64), ("shift_idx", ctypes.c_int64),
-                ("scale_idx", ctypes.c_int64)]
+                ("scale_idx", ctypes.c_int64),
+                ("scale_fp8", ctypes.c_void_p), ("shift_fp8", ctypes.c_void_p),
+                ("scale_deq", ctypes.c_float), ("shift_deq", ctypes.c_float),
+                ("inv_s", ctypes.c_void_p)]
 
 
 _lib = None
@@ -173,7 +176,8 @@ class _Keep:
 
 
 def _mod(keep: _Keep, kind: int, scale=None, shift=None, temb=None, table=None,
-         shift_idx: int = 0, scale_idx: int = 0) -> _Mod:
+         shift_idx: int = 0, scale_idx: int = 0, scale_fp8=None, shift_fp8=None,
+         scale_deq: float = 1.0, shift_deq: float = 1.0, inv_s=None) -> _Mod:
     m = _Mod()
     m.kind = kind
     m.scale = keep.ptr(scale, np.uint16)
@@ -183,6 +187,11 @@ def _mod(keep: _Keep, kind: int, scale=None, shift=None, temb=None, table=None,
     m.chunks = int(temb.shape[1]) if temb is not None else 0
     m.shift_idx = int(shift_idx)
     m.scale_idx = int(scale_idx)
+    m.scale_fp8 = keep.ptr(scale_fp8, np.uint8)
+    m.shift_fp8 = keep.ptr(shift_fp8, np.uint8)
+    m.scale_deq = float(scale_deq)
+    m.shift_deq = float(shift_deq)
+    m.inv_s = keep.ptr(inv_s, np.uint16)
     return m
 
 

@@ -41,6 +41,12 @@
  *      the precision in which the GPU takes the same decision.
  *   R8 six-way: out_i = bf16(params[..., i, :] + modulation[i, :]) with the
  *      addition in binary32.
+ *   R15 modfp8 producers: scale = decode(scale_fp8) * scale_deq and
+ *      shift = decode(shift_fp8) * shift_deq, unrounded (double); the rest as
+ *      for the broadcast producers.
+ *   R16 AWQ producer: the bf16 smoothing vector inv_s multiplies the modulated
+ *      activation, y * inv_s, before the FP8 quantiser (which then divides by
+ *      act_scale as in R3).
  */
 #include "orc.h"
 
@@ -217,6 +223,20 @@ static void mod_at(const orc_mod_t* m, int64_t r, int64_t d, int64_t dim,
       *shift = orc_bf16_to_f64(te[m->shift_idx * dim + d]) + (double)m->table[m->shift_idx * dim + d];
       return;
     }
+    case ORC_MOD_MODFP8:
+      /* e4m3 (dim,) vectors, each dequantised by its own fp32 scalar
+       * (README "Available Functions": the *_modfp8_* producers; "Tensor
+       * Contract": scale_fp8/shift_fp8 e4m3 (dim,), scale_deq/shift_deq fp32
+       * scalars).  Reading R15: value = decode(code) * deq, exact in double. */
+      *scale = orc_e4m3_decode(m->scale_fp8[d]) * (double)m->scale_deq;
+      *shift = orc_e4m3_decode(m->shift_fp8[d]) * (double)m->shift_deq;
+      return;
+    case ORC_MOD_AWQ:
+      /* bf16 broadcast scale/shift as in BCAST; inv_s is applied by
+       * modulated_row (README "Available Functions": awq_ada_layer_norm_...). */
+      *scale = orc_bf16_to_f64(m->scale[d]);
+      *shift = orc_bf16_to_f64(m->shift[d]);
+      return;
     default:
       *scale = 0.0;
       *shift = 0.0;
@@ -224,7 +244,10 @@ static void mod_at(const orc_mod_t* m, int64_t r, int64_t d, int64_t dim,
   }
 }
 
-/* y[d] = (x[d] - mean) * rstd * (1 + scale) + shift, double. */
+/* y[d] = (x[d] - mean) * rstd * (1 + scale) + shift, double.
+ * AWQ (reading R16): the smoothing multiplier is applied to the modulated
+ * activation, y[d] *= inv_s[d], before it is quantised -- the quantised
+ * tensor is the input of the smoothed GEMM, whose weights carry s. */
 static void modulated_row(const uint16_t* xr, const orc_mod_t* m, int64_t r, float eps,
                           double* y, int64_t dim) {
   double mu, rstd;
@@ -234,6 +257,7 @@ static void modulated_row(const uint16_t* xr, const orc_mod_t* m, int64_t r, flo
     mod_at(m, r, d, dim, &sc, &sh);
     double xhat = (orc_bf16_to_f64(xr[d]) - mu) * rstd;
     y[d] = xhat * (1.0 + sc) + sh;
+    if (m->kind == ORC_MOD_AWQ) y[d] *= orc_bf16_to_f64(m->inv_s[d]);
   }
 }
 

@@ -48,18 +48,24 @@ void orc_row_stats(const uint16_t* x, int64_t dim, float eps, double* mean, doub
 
 /* ---- producers ---------------------------------------------------------- */
 /* modulation sources */
-enum { ORC_MOD_NONE = 0, ORC_MOD_BCAST = 1, ORC_MOD_PTOK = 2, ORC_MOD_TABLE = 3 };
+enum { ORC_MOD_NONE = 0, ORC_MOD_BCAST = 1, ORC_MOD_PTOK = 2, ORC_MOD_TABLE = 3,
+       ORC_MOD_MODFP8 = 4, ORC_MOD_AWQ = 5 };
 
 typedef struct {
   int kind;
-  const uint16_t* scale;   /* BCAST: (dim,)   PTOK: (rows, dim)            */
+  const uint16_t* scale;   /* BCAST, AWQ: (dim,)   PTOK: (rows, dim)       */
   const uint16_t* shift;
   const uint16_t* temb;    /* TABLE: (rows, chunks, dim) bf16             */
   const float*    table;   /* TABLE: (chunks, dim) fp32                    */
   int64_t chunks, shift_idx, scale_idx;
+  const uint8_t*  scale_fp8;  /* MODFP8: (dim,) e4m3 codes                */
+  const uint8_t*  shift_fp8;
+  float scale_deq, shift_deq; /* MODFP8: fp32 multipliers of the decoded codes */
+  const uint16_t* inv_s;      /* AWQ: (dim,) bf16 smoothing multipliers    */
 } orc_mod_t;
 
-/* y = LN(x) * (1 + scale) + shift, as double, for all rows (rows, dim). */
+/* y = LN(x) * (1 + scale) + shift, as double, for all rows (rows, dim);
+ * AWQ: y = (LN(x) * (1 + scale) + shift) * inv_s. */
 int orc_modulated_rows(const uint16_t* x, const orc_mod_t* mod, float eps, double* y,
                        int64_t rows, int64_t dim, int nthreads);
 
