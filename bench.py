@@ -67,20 +67,34 @@ def step_workloads():
     ]
 
 
+def extra_workloads():
+    """Producers measured beside the step (same shapes as their broadcast
+    counterparts), reported in `per_op` with "in_step": false."""
+    return [
+        ("fp8_modfp8", synth.fp8_modfp8(4096, 3072, 2006)),
+        ("fp8_awq", synth.fp8_awq(4096, 3072, 2007)),
+        ("nvfp4_modfp8", synth.nvfp4_modfp8(5070, 3072, 2008)),
+    ]
+
+
 def alg_bytes(name: str, w) -> int:
     """Bytes the producer must move: every input element it uses read once,
     every output byte written once (per-op formulas of the design notes)."""
     R, D = w.rows, w.dim
     if name == "fp8_broadcast":
         return 2 * R * D + 4 * D + R * D + 4
+    if name == "fp8_modfp8":
+        return 2 * R * D + 2 * D + 8 + R * D + 4          # e4m3 vectors, two deq scalars
+    if name == "fp8_awq":
+        return 2 * R * D + 6 * D + R * D + 4              # scale, shift, inv_s
     if name == "fp8_layer_norm":
         return 2 * R * D + R * D + 4
     if name == "fp8_per_token":
         return 6 * R * D + R * D + 4
     if name == "fp8_table":
         return 2 * R * D + 4 * R * D + 8 * D + R * D + 4   # 2 of the temb chunks, 2 table rows
-    if name in ("nvfp4_broadcast", "nvfp4_layer_norm"):
-        mod = 4 * D if name == "nvfp4_broadcast" else 0
+    if name in ("nvfp4_broadcast", "nvfp4_layer_norm", "nvfp4_modfp8"):
+        mod = {"nvfp4_broadcast": 4 * D, "nvfp4_layer_norm": 0, "nvfp4_modfp8": 2 * D + 8}[name]
         sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
         return 2 * R * D + mod + R * D // 2 + sf
     if name == "modulation6":
@@ -122,6 +136,16 @@ class DeviceOp:
                                                         packed=o[0], sf_swizzled=o[1])
         elif n == "nvfp4_layer_norm":
             ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(d["x"], p["eps"], packed=o[0], sf_swizzled=o[1])
+        elif n == "fp8_modfp8":
+            ap.ada_layer_norm_quant_fp8_modfp8_bf16(d["x"], d["scale_fp8"], d["shift_fp8"], d["scale_deq"],
+                                                    d["shift_deq"], d["act_scale"], p["eps"], out=o[0])
+        elif n == "fp8_awq":
+            ap.awq_ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["inv_s"], d["act_scale"],
+                                                 p["eps"], out=o[0])
+        elif n == "nvfp4_modfp8":
+            ap.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(d["x"], d["scale_fp8"], d["shift_fp8"],
+                                                               d["scale_deq"], d["shift_deq"], p["eps"],
+                                                               packed=o[0], sf_swizzled=o[1])
         elif n == "modulation6":
             ap.adaln_modulation6_bf16(d["params"], d["modulation"], out=o[0])
 
@@ -152,6 +176,18 @@ class DeviceOp:
         elif n == "nvfp4_layer_norm":
             fn, a = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16, (P(d["x"]), p["eps"], P(o[0]), P(o[1]), R, D,
                                                                        stream)
+        elif n == "fp8_modfp8":
+            fn, a = L.ada_layer_norm_quant_fp8_modfp8_bf16, (P(d["x"]), P(d["scale_fp8"]), P(d["shift_fp8"]),
+                                                             P(d["scale_deq"]), P(d["shift_deq"]), P(d["act_scale"]),
+                                                             p["eps"], P(o[0]), R, D, stream)
+        elif n == "fp8_awq":
+            fn, a = L.awq_ada_layer_norm_quant_fp8_bf16, (P(d["x"]), P(d["scale"]), P(d["shift"]), P(d["inv_s"]),
+                                                          P(d["act_scale"]), p["eps"], P(o[0]), R, D, stream)
+        elif n == "nvfp4_modfp8":
+            fn, a = L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16, (P(d["x"]), P(d["scale_fp8"]),
+                                                                        P(d["shift_fp8"]), P(d["scale_deq"]),
+                                                                        P(d["shift_deq"]), p["eps"], P(o[0]), P(o[1]),
+                                                                        R, D, stream)
         else:
             self._outs6 = (ctypes.c_void_p * 6)(*[o[0][i].data_ptr() for i in range(6)])
             fn, a = L.adaln_modulation6_bf16, (P(d["params"]), P(d["modulation"]), self._outs6, 1, R, D, stream)
@@ -270,10 +306,15 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     works = step_workloads()
+    extras = [] if args.no_extra else extra_workloads()
     if args.only:
         keep = set(args.only.split(","))
         works = [(n, w) for n, w in works if n in keep]
+        extras = [(n, w) for n, w in extras if n in keep]
+    if not works:  # only producers outside the step were asked for: time them as the step
+        works, extras = extras, []
     ops = [DeviceOp(ap, n, w, dev) for n, w in works]
+    extra_ops = [DeviceOp(ap, n, w, dev) for n, w in extras]
     stream = torch.cuda.Stream(dev)
     step_bytes = sum(o.bytes for o in ops)
 
@@ -285,7 +326,7 @@ def run_ours(args, rank, world, local_rank):
     calls = [o.bind_raw(stream.cuda_stream) for o in ops]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            for o in ops:
+            for o in ops + extra_ops:
                 o.api_call()       # the public API once per op and warm-up step
             for c in calls:
                 c()
@@ -313,7 +354,7 @@ def run_ours(args, rank, world, local_rank):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size if hasattr(
         torch.cuda.get_device_properties(dev), "L2_cache_size") else 129 * 2 ** 20
     per_op_graphs = []
-    for o in ops:
+    for o in ops + extra_ops:
         nsets = max(2, -(-3 * l2 // o.bytes))
         copies = [o] + [DeviceOp(ap, o.name, o.w, dev) for _ in range(nsets - 1)]
         ccalls = [c.bind_raw(stream.cuda_stream) for c in copies]
@@ -372,12 +413,13 @@ def run_ours(args, rank, world, local_rank):
     peak_src = "measured" if hbm else "fallback"
     hbm = hbm or 6800.0
     per_op = []
-    for i, o in enumerate(ops):
+    for i, o in enumerate(ops + extra_ops):
         n = args.per_op_launches
         us = statistics.median(e0.elapsed_time(e1) for e0, e1 in op_events[i]) * 1e3 / n
         gbs = o.bytes / (us * 1e-6) / 1e9
         per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
-                       "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4)})
+                       "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4),
+                       "in_step": i < len(ops)})
     dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])  # largest share of the step
     d = per_op[dom]
     roofline = {"bound": "hbm", "kernel": d["op"], "achieved": d["gbs"], "peak": hbm, "peak_source": peak_src,
@@ -517,6 +559,17 @@ def oracle_sample_step(works, frac_rows: int, nthreads: int):
                                   shift=synth.u16(w.inputs["shift"]))
         elif name == "nvfp4_layer_norm":
             oracle.ln_quant_nvfp4(x, oracle.MOD_NONE, eps, nthreads)
+        elif name in ("fp8_modfp8", "nvfp4_modfp8"):
+            src = dict(scale_fp8=w.inputs["scale_fp8"].view(torch.uint8).numpy(),
+                       shift_fp8=w.inputs["shift_fp8"].view(torch.uint8).numpy(),
+                       scale_deq=float(w.inputs["scale_deq"][0]), shift_deq=float(w.inputs["shift_deq"][0]))
+            if name == "fp8_modfp8":
+                oracle.ln_quant_fp8(x, 0.025, oracle.MOD_MODFP8, eps, nthreads, **src)
+            else:
+                oracle.ln_quant_nvfp4(x, oracle.MOD_MODFP8, eps, nthreads, **src)
+        elif name == "fp8_awq":
+            oracle.ln_quant_fp8(x, 0.025, oracle.MOD_AWQ, eps, nthreads, scale=synth.u16(w.inputs["scale"]),
+                                shift=synth.u16(w.inputs["shift"]), inv_s=synth.u16(w.inputs["inv_s"]))
         elif name == "modulation6":
             oracle.adaln_modulation6(w.inputs["params"][:, :n].numpy(), w.inputs["modulation"].numpy(), nthreads)
         sub = synth.Workload(w.op, n, w.dim)
@@ -618,6 +671,8 @@ def main():
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
     ap_.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap_.add_argument("--no-extra", action="store_true",
+                     help="skip the producers measured beside the step (modfp8, AWQ)")
     ap_.add_argument("--sweep", action="store_true", help="also time the FP8 broadcast row sweep")
     ap_.add_argument("--out", default=None, help="also write the JSON line (and the sweep) to this file")
     args = ap_.parse_args()

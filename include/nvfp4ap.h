@@ -28,6 +28,10 @@
  *    of 8; the FP8 ops otherwise fall back to a 4-byte (bf16 pair) path that
  *    needs 4-byte aligned bf16 inputs and 2-byte aligned outputs.  The NVFP4
  *    ops need 16-byte aligned x/scale/shift and an 8-byte aligned `packed`.
+ *    e4m3 (dim,) inputs (scale_fp8, shift_fp8) count as aligned for the
+ *    vector path at 8 bytes and for the pair path at 2 bytes (NVFP4: 8 bytes,
+ *    else NVFP4AP_ERR_ALIGN); inv_s follows the bf16 rules; fp32 scalars
+ *    (act_scale, scale_deq, shift_deq) must be 4-byte aligned.
  *    A pointer that violates its op's rule gives NVFP4AP_ERR_ALIGN.
  *  - dim must be at most NVFP4AP_MAX_DIM for the LayerNorm ops (a whole row
  *    is held in registers); the six-way op has no such limit.
@@ -142,6 +146,33 @@ int ada_layer_norm_quant_fp8_ptok_table_bf16(const void* x, const void* temb, co
                                              const float* act_scale, float eps, void* out,
                                              int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
+/* README "Available Functions": ada_layer_norm_quant_fp8_modfp8_bf16;
+ * "Tensor Contract": scale_fp8, shift_fp8 e4m3fn (dim,); scale_deq,
+ * shift_deq fp32 scalars.
+ * scale_fp8, shift_fp8: device (dim,) e4m3fn bytes, broadcast over rows.
+ * scale_deq, shift_deq: device pointers to ONE fp32 each.  The modulation is
+ *   scale[d] = decode(scale_fp8[d]) * (*scale_deq)
+ *   shift[d] = decode(shift_fp8[d]) * (*shift_deq)
+ * taken as one fp32 product each (exact whenever the scalar has at most 20
+ * significant bits); the rest as ada_layer_norm_quant_fp8_bf16.  e4m3 NaN
+ * bytes (0x7F, 0xFF) are out of contract.  A NULL pointer gives
+ * NVFP4AP_ERR_NULL, a misaligned scalar NVFP4AP_ERR_ALIGN. */
+int ada_layer_norm_quant_fp8_modfp8_bf16(const void* x, const void* scale_fp8, const void* shift_fp8,
+                                         const float* scale_deq, const float* shift_deq,
+                                         const float* act_scale, float eps, void* out, int64_t rows,
+                                         int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions": awq_ada_layer_norm_quant_fp8_bf16;
+ * "Tensor Contract": inv_s bf16 (dim,).
+ * scale, shift, inv_s: device (dim,) bf16, broadcast over rows.  The pages
+ * do not say where inv_s applies; this library multiplies the modulated
+ * activation by it before the quantiser (the AWQ smoothing of a GEMM input):
+ *   out[r,d] = e4m3fn(y[d] * inv_s[d] / act_scale)
+ * computed as y * (inv_s * (1 / act_scale)) in fp32. */
+int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
+                                      const void* inv_s, const float* act_scale, float eps, void* out,
+                                      int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
 /* README "Available Functions": layer_norm_no_affine_quant_fp8_static_bf16.
  * No modulation: y = (x - mean) * rstd. */
 int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
@@ -170,6 +201,16 @@ int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_s
 int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const void* scale, const void* shift,
                                              float eps, void* packed, void* sf_swizzled,
                                              int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* README "Available Functions": ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.
+ * scale_fp8, shift_fp8: device (dim,) e4m3fn bytes (8-byte aligned);
+ * scale_deq, shift_deq: device pointers to ONE fp32 each; the modulation is
+ * decode(code) * deq as for ada_layer_norm_quant_fp8_modfp8_bf16, the output
+ * as ada_layer_norm_quant_nvfp4_swizzled_bf16. */
+int ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(const void* x, const void* scale_fp8, const void* shift_fp8,
+                                                    const float* scale_deq, const float* shift_deq, float eps,
+                                                    void* packed, void* sf_swizzled, int64_t rows, int64_t dim,
+                                                    nvfp4ap_stream_t stream);
 
 /* README "Available Functions": layer_norm_no_affine_quant_nvfp4_swizzled_bf16. */
 int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,

@@ -21,8 +21,11 @@ __all__ = [
     "ada_layer_norm_quant_fp8_bf16",
     "ada_layer_norm_quant_fp8_ptok_bf16",
     "ada_layer_norm_quant_fp8_ptok_table_bf16",
+    "ada_layer_norm_quant_fp8_modfp8_bf16",
+    "awq_ada_layer_norm_quant_fp8_bf16",
     "layer_norm_no_affine_quant_fp8_static_bf16",
     "ada_layer_norm_quant_nvfp4_swizzled_bf16",
+    "ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16",
     "layer_norm_no_affine_quant_nvfp4_swizzled_bf16",
     "adaln_modulation6_bf16",
     "swizzled_sf_size",
@@ -71,6 +74,12 @@ def _load() -> ctypes.CDLL:
     L.ada_layer_norm_quant_fp8_bf16_noalloc.argtypes = [p, p, p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_fp8_ptok_table_bf16.restype = i32
     L.ada_layer_norm_quant_fp8_ptok_table_bf16.argtypes = [p, p, p, i64, i64, i64, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_fp8_modfp8_bf16.restype = i32
+    L.ada_layer_norm_quant_fp8_modfp8_bf16.argtypes = [p, p, p, p, p, p, f32, p, i64, i64, p]
+    L.awq_ada_layer_norm_quant_fp8_bf16.restype = i32
+    L.awq_ada_layer_norm_quant_fp8_bf16.argtypes = [p, p, p, p, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.restype = i32
+    L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.argtypes = [p, p, p, p, p, f32, p, p, i64, i64, p]
     L.layer_norm_no_affine_quant_fp8_static_bf16.restype = i32
     L.layer_norm_no_affine_quant_fp8_static_bf16.argtypes = [p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_nvfp4_swizzled_bf16.restype = i32
@@ -199,6 +208,39 @@ def ada_layer_norm_quant_fp8_ptok_table_bf16(x, temb, table, act_scale, shift_id
     return out
 
 
+def ada_layer_norm_quant_fp8_modfp8_bf16(x, scale_fp8, shift_fp8, scale_deq, shift_deq, act_scale,
+                                         eps: float = 1e-5, out=None):
+    """Broadcast form with e4m3 (dim,) scale/shift, each times its fp32 scalar:
+    scale = scale_fp8 * scale_deq, shift = shift_fp8 * shift_deq."""
+    rows, dim, dev = _x(x)
+    _need(scale_fp8, "scale_fp8", torch.float8_e4m3fn, (dim,), dev)
+    _need(shift_fp8, "shift_fp8", torch.float8_e4m3fn, (dim,), dev)
+    _scalar(scale_deq, "scale_deq", dev)
+    _scalar(shift_deq, "shift_deq", dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_fp8_modfp8_bf16(_ptr(x), _ptr(scale_fp8), _ptr(shift_fp8), _ptr(scale_deq),
+                                                      _ptr(shift_deq), _ptr(act_scale), eps, _ptr(out), rows, dim,
+                                                      _stream(dev))
+    _raise("ada_layer_norm_quant_fp8_modfp8_bf16", rc)
+    return out
+
+
+def awq_ada_layer_norm_quant_fp8_bf16(x, scale, shift, inv_s, act_scale, eps: float = 1e-5, out=None):
+    """Broadcast form with a bf16 (dim,) AWQ smoothing vector:
+    e4m3fn((LayerNorm(x)*(1+scale)+shift) * inv_s / act_scale)."""
+    rows, dim, dev = _x(x)
+    _need(scale, "scale", torch.bfloat16, (dim,), dev)
+    _need(shift, "shift", torch.bfloat16, (dim,), dev)
+    _need(inv_s, "inv_s", torch.bfloat16, (dim,), dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().awq_ada_layer_norm_quant_fp8_bf16(_ptr(x), _ptr(scale), _ptr(shift), _ptr(inv_s),
+                                                   _ptr(act_scale), eps, _ptr(out), rows, dim, _stream(dev))
+    _raise("awq_ada_layer_norm_quant_fp8_bf16", rc)
+    return out
+
+
 def layer_norm_no_affine_quant_fp8_static_bf16(x, act_scale, eps: float = 1e-5, out=None):
     """LayerNorm(x) (no affine) -> e4m3fn(. / act_scale)."""
     rows, dim, dev = _x(x)
@@ -249,6 +291,23 @@ def ada_layer_norm_quant_nvfp4_swizzled_bf16(x, scale, shift, eps: float = 1e-5,
     rc = _load().ada_layer_norm_quant_nvfp4_swizzled_bf16(_ptr(x), _ptr(scale), _ptr(shift), eps, _ptr(packed),
                                                           _ptr(sf_swizzled), rows, dim, _stream(dev))
     _raise("ada_layer_norm_quant_nvfp4_swizzled_bf16", rc)
+    return packed, sf_swizzled
+
+
+def ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(x, scale_fp8, shift_fp8, scale_deq, shift_deq,
+                                                    eps: float = 1e-5, packed=None, sf_swizzled=None):
+    """NVFP4 broadcast form with e4m3 (dim,) scale/shift times fp32 scalars."""
+    rows, dim, dev = _x(x)
+    _need(scale_fp8, "scale_fp8", torch.float8_e4m3fn, (dim,), dev)
+    _need(shift_fp8, "shift_fp8", torch.float8_e4m3fn, (dim,), dev)
+    _scalar(scale_deq, "scale_deq", dev)
+    _scalar(shift_deq, "shift_deq", dev)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(_ptr(x), _ptr(scale_fp8), _ptr(shift_fp8),
+                                                                 _ptr(scale_deq), _ptr(shift_deq), eps,
+                                                                 _ptr(packed), _ptr(sf_swizzled), rows, dim,
+                                                                 _stream(dev))
+    _raise("ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16", rc)
     return packed, sf_swizzled
 
 

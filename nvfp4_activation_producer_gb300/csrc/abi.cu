@@ -133,7 +133,16 @@ int check_common(int64_t rows, int64_t dim, float eps) {
   return NVFP4AP_OK;
 }
 
-// FP8 family: validation shared by K1-K4, then variant + shape + launch.
+// The modfp8 source: non-null e4m3 vectors and fp32 scalars; the scalars
+// 4-byte aligned.
+int check_modfp8(const LnArgs& a) {
+  if (!a.scale8 || !a.shift8 || !a.scale_deq || !a.shift_deq) return NVFP4AP_ERR_NULL;
+  if (!aligned(a.scale_deq, 4) || !aligned(a.shift_deq, 4)) return NVFP4AP_ERR_ALIGN;
+  return NVFP4AP_OK;
+}
+
+// FP8 family: validation shared by every modulation source, then variant +
+// shape + launch.
 int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -143,16 +152,24 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     return NVFP4AP_ERR_INDEX;
   if (a.rows == 0) return NVFP4AP_OK;
   if (!a.x || !a.out || !a.act_scale) return NVFP4AP_ERR_NULL;
-  if ((mod == MOD_BCAST || mod == MOD_PTOK) && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if ((mod == MOD_BCAST || mod == MOD_PTOK || mod == MOD_AWQ) && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_AWQ && !a.inv_s) return NVFP4AP_ERR_NULL;
   if (mod == MOD_TABLE && (!a.temb || !a.table)) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_MODFP8 && (rc = check_modfp8(a)) != NVFP4AP_OK) return rc;
   if (!aligned(a.act_scale, 4)) return NVFP4AP_ERR_ALIGN;
 
   // 16-byte vector path or bf16-pair path
-  const void* bf_in[3] = {a.x, nullptr, nullptr};
-  if (mod == MOD_BCAST || mod == MOD_PTOK) { bf_in[1] = a.scale; bf_in[2] = a.shift; }
+  const void* bf_in[4] = {a.x, nullptr, nullptr, nullptr};
+  if (mod == MOD_BCAST || mod == MOD_PTOK || mod == MOD_AWQ) { bf_in[1] = a.scale; bf_in[2] = a.shift; }
+  if (mod == MOD_AWQ) bf_in[3] = a.inv_s;
   if (mod == MOD_TABLE) bf_in[1] = a.temb;
   bool vec8 = (a.dim % 8 == 0) && aligned(a.out, 8) && (mod != MOD_TABLE || aligned(a.table, 16));
   bool pair_ok = aligned(a.out, 2) && (mod != MOD_TABLE || aligned(a.table, 8));
+  if (mod == MOD_MODFP8) {
+    // e4m3 vectors: 8 bytes per 8-column chunk, 2 bytes per pair
+    vec8 = vec8 && aligned(a.scale8, 8) && aligned(a.shift8, 8);
+    pair_ok = pair_ok && aligned(a.scale8, 2) && aligned(a.shift8, 2);
+  }
   for (const void* p : bf_in) {
     if (!p) continue;
     vec8 = vec8 && aligned(p, 16);
@@ -164,9 +181,12 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   // NVFP4AP_KERNEL: 0 auto (default: the TMA pipeline for the table form,
   // the register row kernels otherwise -- the faster family for each form on
   // GB300 at 2,520-32,768 rows), 1 warp-per-row TMA ring, 2 first register
-  // kernel, 3 register row kernels for every form, 4 TMA pipeline for every form
+  // kernel, 3 register row kernels for every form, 4 TMA pipeline for every
+  // form.  The ring and TMA kernels have no modfp8 / AWQ source: those run
+  // on the register kernels.
   int kernel = env_int("NVFP4AP_KERNEL");
   if (kernel == 0) kernel = (mod == MOD_TABLE) ? 4 : 3;
+  if (kernel == 1 && (mod == MOD_MODFP8 || mod == MOD_AWQ)) kernel = 3;
   RingShape rs{};
   if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
@@ -179,8 +199,9 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     if (kernel == 4 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
       return finish(launch_ln_tma(a, false, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
                                   env_int("NVFP4AP_TMA_CTAS"), st));
-    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0)
-      return finish(launch_ln_bcast_persistent(a, false, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
+    if (mod_is_bcast(mod) && persist_ok(rows_shape) && sms > 0)
+      return finish(
+          launch_ln_bcast_persistent(a, false, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     return finish(launch_ln_rows(a, false, mod, rows_shape, st));
   }
 
@@ -208,11 +229,15 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (a.rows == 0) return NVFP4AP_OK;
   if (!a.x || !a.out || !a.sf) return NVFP4AP_ERR_NULL;
   if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_MODFP8 && (rc = check_modfp8(a)) != NVFP4AP_OK) return rc;
   if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
+  if (mod == MOD_MODFP8 && (!aligned(a.scale8, 8) || !aligned(a.shift8, 8))) return NVFP4AP_ERR_ALIGN;
 
   int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8; auto = row kernels
   if (kernel == 0) kernel = 3;
+  // the modfp8 source runs on the register kernels only
+  if (mod == MOD_MODFP8 && kernel != 3 && kernel != 4) kernel = 3;
   RingShape rs{};
   if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
@@ -229,9 +254,10 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
     // four rows of a scale tile per CTA (whole 16-byte scale chunks): opt-in
     // with NVFP4AP_TILE4=1 -- measured slower on GB300 than one row per CTA
     const bool tile4 = env_int("NVFP4AP_TILE4") > 0 && rows_shape.tpr <= 128 && rows_shape.per_thread <= 4 &&
-                       aligned(a.sf, 16);
-    if (mod == MOD_BCAST && persist_ok(rows_shape) && sms > 0 && !tile4)
-      return finish(launch_ln_bcast_persistent(a, true, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
+                       aligned(a.sf, 16) && (mod == MOD_NONE || mod == MOD_BCAST);
+    if (mod_is_bcast(mod) && persist_ok(rows_shape) && sms > 0 && !tile4)
+      return finish(
+          launch_ln_bcast_persistent(a, true, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     if (tile4) return finish(launch_ln_rows_tile4(a, mod, rows_shape, st));
     return finish(launch_ln_rows(a, true, mod, rows_shape, st));
   }
@@ -350,6 +376,30 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_table_bf16(const void* x, const
   return run_fp8(a, MOD_TABLE, reinterpret_cast<cudaStream_t>(stream));
 }
 
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_modfp8_bf16(const void* x, const void* scale_fp8, const void* shift_fp8,
+                                                        const float* scale_deq, const float* shift_deq,
+                                                        const float* act_scale, float eps, void* out, int64_t rows,
+                                                        int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.scale8 = static_cast<const uint8_t*>(scale_fp8);
+  a.shift8 = static_cast<const uint8_t*>(shift_fp8);
+  a.scale_deq = scale_deq;
+  a.shift_deq = shift_deq;
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_MODFP8, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
+                                                     const void* inv_s, const float* act_scale, float eps, void* out,
+                                                     int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.inv_s = static_cast<const uint16_t*>(inv_s);
+  a.act_scale = act_scale;
+  return run_fp8(a, MOD_AWQ, reinterpret_cast<cudaStream_t>(stream));
+}
+
 NVFP4AP_EXPORT int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
                                                               void* out, int64_t rows, int64_t dim,
                                                               nvfp4ap_stream_t stream) {
@@ -366,6 +416,20 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const
   a.shift = static_cast<const uint16_t*>(shift);
   a.sf = sf_swizzled;
   return run_nvfp4(a, MOD_BCAST, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(const void* x, const void* scale_fp8,
+                                                                   const void* shift_fp8, const float* scale_deq,
+                                                                   const float* shift_deq, float eps, void* packed,
+                                                                   void* sf_swizzled, int64_t rows, int64_t dim,
+                                                                   nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.scale8 = static_cast<const uint8_t*>(scale_fp8);
+  a.shift8 = static_cast<const uint8_t*>(shift_fp8);
+  a.scale_deq = scale_deq;
+  a.shift_deq = shift_deq;
+  a.sf = sf_swizzled;
+  return run_nvfp4(a, MOD_MODFP8, reinterpret_cast<cudaStream_t>(stream));
 }
 
 NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,

@@ -28,7 +28,15 @@ cudaError_t launch_maybe_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
 }
 
 // modulation source of a LayerNorm producer
-enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3 };
+//   MOD_BCAST   bf16 (dim,) scale/shift
+//   MOD_PTOK    bf16 (rows, dim) scale/shift
+//   MOD_TABLE   temb[r, idx, :] (bf16) + table[idx, :] (fp32)
+//   MOD_MODFP8  e4m3 (dim,) scale/shift times fp32 device scalars scale_deq/shift_deq
+//   MOD_AWQ     bf16 (dim,) scale/shift, output multiplied by bf16 (dim,) inv_s
+enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3, MOD_MODFP8 = 4, MOD_AWQ = 5 };
+
+// sources whose scale/shift are the same (dim,) vector for every row
+constexpr bool mod_is_bcast(int mod) { return mod == MOD_BCAST || mod == MOD_MODFP8 || mod == MOD_AWQ; }
 
 // Arguments of one LayerNorm producer launch (device pointers, element counts).
 struct LnArgs {
@@ -39,6 +47,11 @@ struct LnArgs {
   const float* table;     // TABLE: (chunks, dim) fp32
   int64_t chunks, shift_idx, scale_idx;
   const float* act_scale; // FP8: device scalar
+  const uint8_t* scale8;  // MODFP8: (dim,) e4m3
+  const uint8_t* shift8;
+  const float* scale_deq; // MODFP8: device scalars
+  const float* shift_deq;
+  const uint16_t* inv_s;  // AWQ: (dim,) bf16
   float eps;
   void* out;              // FP8: (rows, dim) e4m3; NVFP4: packed (rows, dim/2)
   void* sf;               // NVFP4: swizzled scales
@@ -51,7 +64,8 @@ struct RowShape {
   int tpr, per_thread, rpc;
 };
 
-// FP8 producers (K1-K4).  `vec` is 8 (16-byte vectors) or 2 (bf16 pairs).
+// FP8 producers (every modulation source).  `vec` is 8 (16-byte vectors) or 2
+// (bf16 pairs).
 cudaError_t launch_ln_fp8(const LnArgs& a, int mod, int vec, RowShape s, cudaStream_t st);
 // Largest threads-per-row (and threads-per-CTA) the (vec, per_thread)
 // instance accepts; 0 if there is no such instance.
@@ -69,8 +83,8 @@ cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStrea
 // next row prefetched, fp32 modulation in registers): tpr <= 256, rpc == 1,
 // per_thread in {1, 2, 3, 4, 6}; at most `ctas_per_sm` CTAs per SM (0 = as
 // many as fit).
-cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, RowShape s, int sms, int ctas_per_sm,
-                                       cudaStream_t st);
+cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms,
+                                       int ctas_per_sm, cudaStream_t st);
 
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);

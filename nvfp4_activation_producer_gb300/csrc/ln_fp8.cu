@@ -6,6 +6,8 @@
 //   ada_layer_norm_quant_fp8_ptok_bf16       per-token (rows, dim) scale/shift
 //   ada_layer_norm_quant_fp8_ptok_table_bf16 scale/shift = temb[r,idx,:] + table[idx,:]
 //   layer_norm_no_affine_quant_fp8_static_bf16   no modulation
+//   ada_layer_norm_quant_fp8_modfp8_bf16     e4m3 (dim,) scale/shift times fp32 deq scalars
+//   awq_ada_layer_norm_quant_fp8_bf16        broadcast, y multiplied by inv_s
 // For each row: mean and biased variance over dim, rstd = 1/sqrt(var+eps),
 // y = (x - mean) * rstd * (1 + scale) + shift, out = e4m3fn(y / act_scale)
 // rounded to nearest-even and saturated to +-448.
@@ -22,6 +24,7 @@
 // vector leaves as one 8-byte streaming store.
 #include "device.cuh"
 #include "kernels.h"
+#include "modsrc.cuh"
 
 namespace nvfp4ap {
 namespace {
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(fp8_max_tpr(NV, VEC)) ln_fp8_kernel(const LnAr
   const float rstd = 1.0f / sqrtf(var + a.eps);
   const float inv_act = 1.0f / __ldg(a.act_scale);
   const float2 rstd2 = splat2(rstd), inv2 = splat2(inv_act), rinv2 = splat2(rstd * inv_act);
+  const float2 deq = source_deq<MOD>(a);
 
   // ---- normalise, modulate, quantise, store -------------------------------
   uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) + row * D;
@@ -144,9 +148,11 @@ __global__ void __launch_bounds__(fp8_max_tpr(NV, VEC)) ln_fp8_kernel(const LnAr
     if (j >= nvec) continue;
     const int64_t col = (int64_t)j * VEC;
     uint32_t sc[W], sh[W];
-    if constexpr (MOD == MOD_BCAST) {
-      load_reuse<VEC>(sc, a.scale + col);
-      load_reuse<VEC>(sh, a.shift + col);
+    BcastCols<mod_is_bcast(MOD) ? MOD : MOD_BCAST, VEC> bc;
+    AwqCols<VEC> aw;
+    if constexpr (mod_is_bcast(MOD)) {
+      bc.load(a, col);
+      if constexpr (MOD == MOD_AWQ) aw.load(a, col);
     } else if constexpr (kPerTokenRegs) {
 #pragma unroll
       for (int i = 0; i < W; ++i) { sc[i] = scw[k][i]; sh[i] = shw[k][i]; }
@@ -164,6 +170,9 @@ __global__ void __launch_bounds__(fp8_max_tpr(NV, VEC)) ln_fp8_kernel(const LnAr
       float2 q;
       if constexpr (MOD == MOD_NONE) {
         q = mul2(d[k][i], rinv2);
+      } else if constexpr (mod_is_bcast(MOD)) {
+        const float2 f = MOD == MOD_AWQ ? mul2(aw.mult(i), inv2) : inv2;
+        q = mul2(fma2(d[k][i], fma2(bc.scale(i, deq), rstd2, rstd2), bc.shift(i, deq)), f);
       } else {
         float2 s = bf16x2_to_f2(sc[i]);
         float2 h = bf16x2_to_f2(sh[i]);
@@ -222,6 +231,8 @@ cudaError_t launch_vec(const LnArgs& a, int mod, RowShape s, cudaStream_t st) {
     case MOD_BCAST: return launch_mod<MOD_BCAST, VEC>(a, s, st);
     case MOD_PTOK: return launch_mod<MOD_PTOK, VEC>(a, s, st);
     case MOD_TABLE: return launch_mod<MOD_TABLE, VEC>(a, s, st);
+    case MOD_MODFP8: return launch_mod<MOD_MODFP8, VEC>(a, s, st);
+    case MOD_AWQ: return launch_mod<MOD_AWQ, VEC>(a, s, st);
     default: return cudaErrorInvalidValue;
   }
 }

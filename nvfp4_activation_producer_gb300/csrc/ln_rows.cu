@@ -4,7 +4,9 @@
 // Operations (adaptive-layernorm-producers README, "Available Functions",
 // "Tensor Contract", "Validation"; NVFP4 encoding facts from the
 // h3-blackwell-runtime compare page):
-//   y = (x - mean) * rstd * (1 + scale) + shift, rstd = 1/sqrt(var + eps)
+//   y = (x - mean) * rstd * (1 + scale) + shift, rstd = 1/sqrt(var + eps),
+//   scale/shift from one of the modulation sources of kernels.h (the AWQ
+//   source also multiplies y by inv_s)
 //   FP8:   out = e4m3fn(y / act_scale), nearest-even, saturating
 //   NVFP4: v = bf16(y); per 16 elements s = e4m3fn(amax/6); e2m1 codes of
 //          v/s, two per byte (low nibble first); s in the 128x4 tiled layout
@@ -29,6 +31,7 @@
 
 #include "device.cuh"
 #include "kernels.h"
+#include "modsrc.cuh"
 
 namespace nvfp4ap {
 namespace {
@@ -152,15 +155,18 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
     // ---- FP8: q = (x - mean) * rstd * (1 + scale) + shift) / act_scale ------
     const float inv_act = 1.0f / __ldg(a.act_scale);
     const float2 rstd2 = splat2(rstd), inv2 = splat2(inv_act), rinv2 = splat2(rstd * inv_act);
+    const float2 deq = source_deq<MOD>(a);
     uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) + row * D;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
       if (j >= nch) continue;
       uint32_t sc[4], sh[4];
-      if constexpr (MOD == MOD_BCAST) {
-        unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
-        unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
+      BcastCols<MOD, 8> bc;
+      AwqCols<8> aw;
+      if constexpr (mod_is_bcast(MOD)) {
+        bc.load(a, (int64_t)j * 8);
+        if constexpr (MOD == MOD_AWQ) aw.load(a, (int64_t)j * 8);
       } else if constexpr (kPerToken) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) { sc[i] = sw[k][i]; sh[i] = hw[k][i]; }
@@ -183,6 +189,10 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
         float2 y;
         if constexpr (MOD == MOD_NONE) {
           y = mul2(d, rinv2);
+        } else if constexpr (mod_is_bcast(MOD)) {
+          // AWQ: y * inv_s / act_scale as y * (inv_s * (1 / act_scale))
+          const float2 f = MOD == MOD_AWQ ? mul2(aw.mult(i), inv2) : inv2;
+          y = mul2(fma2(d, fma2(bc.scale(i, deq), rstd2, rstd2), bc.shift(i, deq)), f);
         } else {
           float2 g = bf16x2_to_f2(sc[i]), h = bf16x2_to_f2(sh[i]);
           if constexpr (MOD == MOD_TABLE) {
@@ -207,27 +217,25 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
     // Phase by phase over the thread's chunks, so that the chunks' dependency
     // chains (stage -> block max -> partner shuffle -> scale -> quotient ->
     // conversion) interleave instead of running one after another.
+    const float2 deq = source_deq<MOD>(a);
     uint32_t vb[NV][4];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
       const bool valid = j < nch;
-      uint32_t sc[4], sh[4];
-      if constexpr (MOD == MOD_BCAST) {
-        if (valid) {
-          unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
-          unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sc[i] = sh[i] = 0u;
-        }
+      BcastCols<MOD, 8> bc;
+      if constexpr (mod_is_bcast(MOD)) {
+        if (valid)
+          bc.load(a, (int64_t)j * 8);
+        else
+          bc.clear();
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 d = add2(dk[k][i], nm1);
         float2 y;
-        if constexpr (MOD == MOD_BCAST)
-          y = fma2(d, fma2(bf16x2_to_f2(sc[i]), rstd2, rstd2), bf16x2_to_f2(sh[i]));
+        if constexpr (mod_is_bcast(MOD))
+          y = fma2(d, fma2(bc.scale(i, deq), rstd2, rstd2), bc.shift(i, deq));
         else
           y = mul2(d, rstd2);
         vb[k][i] = valid ? f2_to_bf16x2(y) : 0u;
@@ -319,8 +327,9 @@ __global__ void __launch_bounds__(512) ln_rows_kernel(const LnArgs a, const floa
 //
 // The broadcast scale/shift are the same for every row, so a CTA that walks
 // many rows with a fixed thread -> column mapping converts them to fp32 once
-// (g = 1 + scale and h = shift, FP8 pre-multiplied by 1/act_scale) and keeps
-// them in registers; per element the output then costs two packed fp32 ops.
+// (g = 1 + scale and h = shift from any broadcast source; FP8 pre-multiplied
+// by 1/act_scale, AWQ by inv_s) and keeps them in registers; per element the
+// output then costs two packed fp32 ops whatever the source.
 // The CTA processes rows blockIdx.x, blockIdx.x + gridDim.x, ...; while one
 // row is reduced and written, the next row's loads are already in flight in a
 // second register buffer.  Statistics and encodings as in ln_rows_kernel.
@@ -340,7 +349,7 @@ __device__ __forceinline__ void load_x(uint32_t (&w)[NV][4], const uint16_t* xr,
   }
 }
 
-template <int KIND, int NV>
+template <int KIND, int MOD, int NV>
 __global__ void __launch_bounds__(256, 2) ln_bcast_persist_kernel(const LnArgs a, const float inv_d) {
   __shared__ float2 red[2][8];  // [row parity][warp]
   const int tpr = blockDim.x;
@@ -351,21 +360,31 @@ __global__ void __launch_bounds__(256, 2) ln_bcast_persist_kernel(const LnArgs a
 
   // per-thread fp32 modulation of its columns
   const float inv_act = KIND == KIND_FP8 ? 1.0f / __ldg(a.act_scale) : 1.0f;
+  const float2 deq = source_deq<MOD>(a);
   float2 G[NV][4], H[NV][4];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int j = t + k * tpr;
-    uint32_t sc[4] = {0u, 0u, 0u, 0u}, sh[4] = {0u, 0u, 0u, 0u};
+    BcastCols<MOD, 8> bc;
+    AwqCols<8> aw;
+    bc.clear();
     if (j < nch) {
-      unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
-      unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
+      bc.load(a, (int64_t)j * 8);
+      if constexpr (MOD == MOD_AWQ) aw.load(a, (int64_t)j * 8);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 g = add2(bf16x2_to_f2(sc[i]), splat2(1.0f));
-      const float2 h = bf16x2_to_f2(sh[i]);
-      G[k][i] = KIND == KIND_FP8 ? mul2(g, splat2(inv_act)) : g;
-      H[k][i] = KIND == KIND_FP8 ? mul2(h, splat2(inv_act)) : h;
+      const float2 g = add2(bc.scale(i, deq), splat2(1.0f));
+      const float2 h = bc.shift(i, deq);
+      if constexpr (KIND == KIND_FP8) {
+        // output multiplier 1/act_scale, times inv_s for AWQ
+        const float2 f = (MOD == MOD_AWQ && j < nch) ? mul2(aw.mult(i), splat2(inv_act)) : splat2(inv_act);
+        G[k][i] = mul2(g, f);
+        H[k][i] = mul2(h, f);
+      } else {
+        G[k][i] = g;
+        H[k][i] = h;
+      }
     }
   }
 
@@ -505,13 +524,13 @@ int persist_occupancy(K k, int threads) {
   return occ;
 }
 
-template <int KIND>
+template <int KIND, int MOD>
 cudaError_t launch_persist(const LnArgs& a, RowShape s, int sms, int ctas_per_sm, cudaStream_t st) {
   const float inv_d = (float)(1.0 / (double)a.dim);
   const int64_t work_rows = KIND == KIND_NVFP4 ? (a.rows + 127) / 128 * 128 : a.rows;
 #define NVFP4AP_CASE(N)                                                                        \
   case N: {                                                                                    \
-    auto k = ln_bcast_persist_kernel<KIND, N>;                                                 \
+    auto k = ln_bcast_persist_kernel<KIND, MOD, N>;                                            \
     int occ = persist_occupancy(k, s.tpr);                                                     \
     if (occ < 1) return cudaErrorInvalidConfiguration;                                         \
     if (ctas_per_sm > 0 && ctas_per_sm < occ) occ = ctas_per_sm;                               \
@@ -577,11 +596,22 @@ int ln_rows_max_tpr(int mod, int per_thread) {
   }
 }
 
-cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, RowShape s, int sms, int ctas_per_sm,
-                                       cudaStream_t st) {
+cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms,
+                                       int ctas_per_sm, cudaStream_t st) {
   if (s.tpr > 256 || s.rpc != 1) return cudaErrorInvalidValue;
-  return nvfp4 ? launch_persist<KIND_NVFP4>(a, s, sms, ctas_per_sm, st)
-               : launch_persist<KIND_FP8>(a, s, sms, ctas_per_sm, st);
+  if (nvfp4) {
+    switch (mod) {
+      case MOD_BCAST: return launch_persist<KIND_NVFP4, MOD_BCAST>(a, s, sms, ctas_per_sm, st);
+      case MOD_MODFP8: return launch_persist<KIND_NVFP4, MOD_MODFP8>(a, s, sms, ctas_per_sm, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (mod) {
+    case MOD_BCAST: return launch_persist<KIND_FP8, MOD_BCAST>(a, s, sms, ctas_per_sm, st);
+    case MOD_MODFP8: return launch_persist<KIND_FP8, MOD_MODFP8>(a, s, sms, ctas_per_sm, st);
+    case MOD_AWQ: return launch_persist<KIND_FP8, MOD_AWQ>(a, s, sms, ctas_per_sm, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStream_t st) {
@@ -618,6 +648,7 @@ cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cud
     switch (mod) {
       case MOD_NONE: return launch_nv<KIND_NVFP4, MOD_NONE>(a, s, st);
       case MOD_BCAST: return launch_nv<KIND_NVFP4, MOD_BCAST>(a, s, st);
+      case MOD_MODFP8: return launch_nv<KIND_NVFP4, MOD_MODFP8>(a, s, st);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -626,6 +657,8 @@ cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cud
     case MOD_BCAST: return launch_nv<KIND_FP8, MOD_BCAST>(a, s, st);
     case MOD_PTOK: return launch_nv<KIND_FP8, MOD_PTOK>(a, s, st);
     case MOD_TABLE: return launch_nv<KIND_FP8, MOD_TABLE>(a, s, st);
+    case MOD_MODFP8: return launch_nv<KIND_FP8, MOD_MODFP8>(a, s, st);
+    case MOD_AWQ: return launch_nv<KIND_FP8, MOD_AWQ>(a, s, st);
     default: return cudaErrorInvalidValue;
   }
 }

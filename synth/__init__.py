@@ -111,6 +111,48 @@ def nvfp4_ln(rows: int, dim: int, seed: int, eps: float = 1e-5) -> Workload:
                     {"x": bf16(x)}, {"eps": eps})
 
 
+def e4m3(a: np.ndarray) -> torch.Tensor:
+    """float32 -> torch.float8_e4m3fn (torch's conversion; |a| kept below 448)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+
+
+def fp8_modfp8(rows: int, dim: int, seed: int, act_scale: float = 0.025, eps: float = 1e-5,
+               scale_deq: float = 0.05, shift_deq: float = 0.05) -> Workload:
+    """modfp8 broadcast form: scale_fp8/shift_fp8 are e4m3 draws of N(0, 2), so that
+    code * 0.05 has the spread N(0, 0.1) of the bf16 broadcast vectors."""
+    x = normal(seed, 0, (rows, dim), 1.0)
+    return Workload("ada_layer_norm_quant_fp8_modfp8_bf16", rows, dim,
+                    {"x": bf16(x), "scale_fp8": e4m3(normal(seed, 1, (dim,), 2.0)),
+                     "shift_fp8": e4m3(normal(seed, 2, (dim,), 2.0)),
+                     "scale_deq": torch.tensor([scale_deq], dtype=torch.float32),
+                     "shift_deq": torch.tensor([shift_deq], dtype=torch.float32),
+                     "act_scale": torch.tensor([act_scale], dtype=torch.float32)},
+                    {"eps": eps})
+
+
+def nvfp4_modfp8(rows: int, dim: int, seed: int, eps: float = 1e-5,
+                 scale_deq: float = 0.05, shift_deq: float = 0.05) -> Workload:
+    x = normal(seed, 0, (rows, dim), 1.0)
+    return Workload("ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16", rows, dim,
+                    {"x": bf16(x), "scale_fp8": e4m3(normal(seed, 1, (dim,), 2.0)),
+                     "shift_fp8": e4m3(normal(seed, 2, (dim,), 2.0)),
+                     "scale_deq": torch.tensor([scale_deq], dtype=torch.float32),
+                     "shift_deq": torch.tensor([shift_deq], dtype=torch.float32)},
+                    {"eps": eps})
+
+
+def fp8_awq(rows: int, dim: int, seed: int, act_scale: float = 0.025, eps: float = 1e-5) -> Workload:
+    """AWQ broadcast form: inv_s = exp(N(0, 0.5)) per channel (positive smoothing
+    factors around 1, spread over about a factor of 3 each way)."""
+    x = normal(seed, 0, (rows, dim), 1.0)
+    return Workload("awq_ada_layer_norm_quant_fp8_bf16", rows, dim,
+                    {"x": bf16(x), "scale": bf16(normal(seed, 1, (dim,), 0.1)),
+                     "shift": bf16(normal(seed, 2, (dim,), 0.1)),
+                     "inv_s": bf16(np.exp(normal(seed, 3, (dim,), 0.5))),
+                     "act_scale": torch.tensor([act_scale], dtype=torch.float32)},
+                    {"eps": eps})
+
+
 def modulation6(batch: int, seq: int, dim: int, seed: int) -> Workload:
     return Workload("adaln_modulation6_bf16", batch * seq, dim,
                     {"params": torch.from_numpy(normal(seed, 0, (batch, seq, 6, dim), 1.0)),

@@ -39,7 +39,7 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 12
+    assert len(declared) == 15
 
 
 def test_status_strings_and_version(lib):
@@ -112,6 +112,30 @@ def test_nvfp4_argument_errors(lib):
     g = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16
     assert g(A, 1e-5, A, A, -3, 64, NULL) == 2
     assert g(A, float("inf"), A, A, 3, 64, NULL) == 7
+
+
+def test_modfp8_and_awq_argument_errors(lib):
+    L, _ = lib
+    m = L.ada_layer_norm_quant_fp8_modfp8_bf16  # x, s8, h8, sdeq, hdeq, act, eps, out, rows, dim
+    assert m(A, NULL, A, A, A, A, 1e-5, A, 4, 64, NULL) == 1      # null scale_fp8
+    assert m(A, A, A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1      # null shift_deq
+    assert m(A, A, A, A + 2, A, A, 1e-5, A, 4, 64, NULL) == 5     # scale_deq misaligned
+    assert m(A, A + 1, A, A, A, A, 1e-5, A, 4, 64, NULL) == 5     # e4m3 vector at an odd address
+    assert m(A, A, A, A, A, A, 1e-5, A, 4, 63, NULL) == 3         # odd dim
+    assert m(A, A, A, A, A, A, -2.0, A, 4, 64, NULL) == 7
+    assert m(NULL, NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0
+    w = L.awq_ada_layer_norm_quant_fp8_bf16  # x, scale, shift, inv_s, act, eps, out, rows, dim
+    assert w(A, A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1         # null inv_s
+    assert w(A, A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1         # null shift
+    assert w(A, A, A, A + 2, A, 1e-5, A, 4, 64, NULL) == 5        # inv_s not 4-byte aligned
+    assert w(A, A, A, A, A, float("nan"), A, 4, 64, NULL) == 7
+    assert w(A, A, A, A, A, 1e-5, A, 4, 32770, NULL) == 3
+    n = L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16  # x, s8, h8, sdeq, hdeq, eps, packed, sf, rows, dim
+    assert n(A, A, A, A, A, 1e-5, A, A, 4, 40, NULL) == 3         # dim % 16
+    assert n(A, A, A, A, NULL, 1e-5, A, A, 4, 64, NULL) == 1      # null shift_deq
+    assert n(A, A + 4, A, A, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_fp8 not 8-byte aligned
+    assert n(A, A, A, A + 1, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_deq misaligned
+    assert n(NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, NULL, 0, 64, NULL) == 0
 
 
 def test_modulation6_argument_errors(lib):

@@ -11,6 +11,13 @@ every case that can matter, and compare with exact rational arithmetic:
    reciprocal, allowed to be off by up to 2 ulp) and r_lo = r_hi * (1 - s*r_hi)
    rounds to the same e2m1 code as the exact v/s, for every e4m3 scale s, at
    every midpoint (ties) and on bf16 values around them.
+
+And one decode the modfp8 kernels use:
+
+3. e4m3 decode by moving the byte's sign to bit 31 and its exponent/mantissa
+   fields to bits 30..20 of an fp32 pattern, then multiplying by 2^120 (the
+   code-0 exponent lands on fp32 subnormals, which the multiply keeps): equal
+   to torch's float8_e4m3fn decoder for every finite code.
 """
 from fractions import Fraction
 
@@ -85,3 +92,15 @@ def test_e2m1_quotient_is_exact_at_midpoints_for_every_scale():
             got = _code_rne32(q)
             exp = np.array([_code_exact(Fraction(float(x)), Fraction(float(s))) for x in v])
             assert np.array_equal(got, exp), (s, ulps)
+
+
+def test_e4m3_field_move_decode_is_exact():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint32)
+    bits = ((codes & 0x80) << 24) | ((codes & 0x7F) << 20)
+    moved = bits.view(np.float32)
+    with np.errstate(over="raise", under="raise"):
+        decoded = moved * F32(2.0**120)  # float32 multiply, subnormal inputs kept
+    ref = torch.from_numpy(codes.astype(np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(decoded.view(np.uint32), ref.view(np.uint32))  # signs of zero included
+    # the smallest subnormal 2^-9 and the largest normal 448 are among them
+    assert decoded[codes == 0x01][0] == 2.0**-9 and decoded[codes == 0x7E][0] == 448.0
