@@ -26,6 +26,12 @@ int env_int(const char* name) {
   return v ? std::atoi(v) : 0;
 }
 
+// true when the variable is set to 0 (a default-on choice switched off)
+bool env_off(const char* name) {
+  const char* v = std::getenv(name);
+  return v && v[0] == '0';
+}
+
 // Launch shape for a row of `nvec` units (vectors or blocks): the candidate
 // per-thread counts are tried in order of preference and the one that wastes
 // the fewest thread slots (tpr * per_thread - nvec, tpr a multiple of 32 not
@@ -259,6 +265,11 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
       return finish(
           launch_ln_bcast_persistent(a, true, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
     if (tile4) return finish(launch_ln_rows_tile4(a, mod, rows_shape, st));
+    // rows that exactly fill the CTA's chunks: the register-capped instance
+    // (NVFP4AP_FULL=0 turns it off)
+    if (!env_off("NVFP4AP_FULL") && rows_shape.tpr <= 128 && rows_shape.per_thread >= 2 && rows_shape.per_thread <= 4 &&
+        (int64_t)rows_shape.tpr * rows_shape.per_thread * 8 == a.dim)
+      return finish(launch_ln_rows_full(a, true, mod, rows_shape, st));
     return finish(launch_ln_rows(a, true, mod, rows_shape, st));
   }
 

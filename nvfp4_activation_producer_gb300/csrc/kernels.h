@@ -75,6 +75,10 @@ int ln_fp8_max_tpr(int vec, int per_thread);
 // NVFP4: `per_thread` 8-element chunks per thread.
 cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
 int ln_rows_max_tpr(int mod, int per_thread);
+// NVFP4 row kernel for rows that exactly fill tpr * per_thread chunks: one
+// row per CTA of tpr <= 128 threads, registers capped at 40 per thread;
+// per_thread 2..4; mod MOD_NONE, MOD_BCAST or MOD_MODFP8.
+cudaError_t launch_ln_rows_full(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
 // NVFP4 row kernel with four rows of one 128-row tile per CTA (rows r, r+32,
 // r+64, r+96): scale bytes leave as whole 16-byte chunks.  tpr <= 128,
 // per_thread 1..4, 16-byte aligned scale buffer.

@@ -54,7 +54,8 @@ def path(request, monkeypatch):
     """Run a LayerNorm-producer test on each kernel family: the default choice
     (TMA pipeline for the table form, register row kernels otherwise), the
     register row kernels for every form (NVFP4AP_KERNEL=3) with and without
-    the persistent broadcast variant (NVFP4AP_PERSIST=-1), the NVFP4
+    the persistent broadcast variant and the register-capped NVFP4 instance
+    (NVFP4AP_PERSIST=-1, NVFP4AP_FULL=0), the NVFP4
     four-row-tile variant (NVFP4AP_TILE4=1), the TMA pipeline
     for every form (4), the warp-per-row TMA ring (1) and the first register
     kernels (2)."""
@@ -66,8 +67,10 @@ def path(request, monkeypatch):
         monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
     if request.param == "rows_flat":
         monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
+        monkeypatch.setenv("NVFP4AP_FULL", "0")
     else:
         monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
+        monkeypatch.delenv("NVFP4AP_FULL", raising=False)
     if request.param == "tile4":
         monkeypatch.setenv("NVFP4AP_TILE4", "1")
     else:

@@ -107,8 +107,10 @@ def same_kernel(request, monkeypatch):
     monkeypatch.delenv("NVFP4AP_TILE4", raising=False)
     if request.param == "rows_flat":
         monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
+        monkeypatch.setenv("NVFP4AP_FULL", "0")
     else:
         monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
+        monkeypatch.delenv("NVFP4AP_FULL", raising=False)
     return request.param
 
 
