@@ -45,7 +45,8 @@ __device__ __forceinline__ void unpack4(uint4 v, uint32_t (&w)[4]) {
   w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
 }
 
-template <int KIND, int MOD, int NV>
+// FULL: the row is exactly NV * tpr chunks (no chunk-validity checks).
+template <int KIND, int MOD, int NV, bool FULL = false>
 __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float inv_d, const int S) {
   constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
   constexpr bool kConst = (MOD == MOD_BCAST || MOD == MOD_TABLE);
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
       uint32_t sc[4] = {0u, 0u, 0u, 0u}, sh[4] = {0u, 0u, 0u, 0u};
-      if (j < nch) {
+      if (FULL || j < nch) {
         unpack4(ld_reuse_v4(a.scale + (int64_t)j * 8), sc);
         unpack4(ld_reuse_v4(a.shift + (int64_t)j * 8), sh);
       }
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
       float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0, u0 = t0, u1 = t0;
-      if (j < nch) {
+      if (FULL || j < nch) {
         const float* ts = a.table + a.scale_idx * D + (int64_t)j * 8;
         const float* th = a.table + a.shift_idx * D + (int64_t)j * 8;
         t0 = ld_reuse_f4(ts); t1 = ld_reuse_f4(ts + 4); u0 = ld_reuse_f4(th); u1 = ld_reuse_f4(th + 4);
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j = t + k * tpr;
-      const bool valid = j < nch;
+      const bool valid = FULL || j < nch;
       uint32_t xw[4] = {0u, 0u, 0u, 0u};
       if (valid) unpack4(xs[j], xw);
       if constexpr (kPerToken) {
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int j = t + k * tpr;
-        if (j >= nch) continue;
+        if (!FULL && j >= nch) continue;
         uint32_t q[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) q[i] = f2_to_e4m3x2(y_of(k, i));
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
       uint32_t vb[NV][4];
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
-        const bool valid = t + k * tpr < nch;
+        const bool valid = FULL || t + k * tpr < nch;
 #pragma unroll
         for (int i = 0; i < 4; ++i) vb[k][i] = valid ? f2_to_bf16x2(y_of(k, i)) : 0u;
       }
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
           q[i] = fma2(v, rh2, mul2(v, rl2));
         }
         const uint32_t codes = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
-        if (j < nch) {
+        if (FULL || j < nch) {
           st_stream_b32(prow + (int64_t)j * 4, codes);
           if ((j & 1) == 0) st_b8(sfrow + ((j >> 1) >> 2) * 512 + ((j >> 1) & 3), sbyte);
         }
@@ -299,27 +300,27 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
 using TmaKernel = void (*)(const LnArgs, const float, const int);
 
 template <int KIND, int MOD>
-TmaKernel pick_nv(int nv) {
+TmaKernel pick_nv(int nv, bool full) {
   switch (nv) {
     case 1: return ln_tma_kernel<KIND, MOD, 1>;
-    case 2: return ln_tma_kernel<KIND, MOD, 2>;
-    case 3: return ln_tma_kernel<KIND, MOD, 3>;
-    case 4: return ln_tma_kernel<KIND, MOD, 4>;
+    case 2: return full ? ln_tma_kernel<KIND, MOD, 2, true> : ln_tma_kernel<KIND, MOD, 2>;
+    case 3: return full ? ln_tma_kernel<KIND, MOD, 3, true> : ln_tma_kernel<KIND, MOD, 3>;
+    case 4: return full ? ln_tma_kernel<KIND, MOD, 4, true> : ln_tma_kernel<KIND, MOD, 4>;
     default: return nullptr;
   }
 }
 
-TmaKernel pick(bool nvfp4, int mod, int nv) {
+TmaKernel pick(bool nvfp4, int mod, int nv, bool full = false) {
   if (nvfp4) {
-    if (mod == MOD_NONE) return pick_nv<KIND_NVFP4, MOD_NONE>(nv);
-    if (mod == MOD_BCAST) return pick_nv<KIND_NVFP4, MOD_BCAST>(nv);
+    if (mod == MOD_NONE) return pick_nv<KIND_NVFP4, MOD_NONE>(nv, full);
+    if (mod == MOD_BCAST) return pick_nv<KIND_NVFP4, MOD_BCAST>(nv, full);
     return nullptr;
   }
   switch (mod) {
-    case MOD_NONE: return pick_nv<KIND_FP8, MOD_NONE>(nv);
-    case MOD_BCAST: return pick_nv<KIND_FP8, MOD_BCAST>(nv);
-    case MOD_PTOK: return pick_nv<KIND_FP8, MOD_PTOK>(nv);
-    case MOD_TABLE: return pick_nv<KIND_FP8, MOD_TABLE>(nv);
+    case MOD_NONE: return pick_nv<KIND_FP8, MOD_NONE>(nv, full);
+    case MOD_BCAST: return pick_nv<KIND_FP8, MOD_BCAST>(nv, full);
+    case MOD_PTOK: return pick_nv<KIND_FP8, MOD_PTOK>(nv, full);
+    case MOD_TABLE: return pick_nv<KIND_FP8, MOD_TABLE>(nv, full);
     default: return nullptr;
   }
 }
@@ -390,7 +391,11 @@ bool ln_tma_supported(bool nvfp4, int mod, RowShape s) {
 
 cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
                           int ctas_per_sm, cudaStream_t st) {
-  TmaKernel k = pick(nvfp4, mod, s.per_thread);
+  // rows that exactly fill the threads' chunks take the FULL instance
+  // (NVFP4AP_FULL=0 turns it off)
+  const char* full_env = std::getenv("NVFP4AP_FULL");
+  const bool full = !(full_env && full_env[0] == '0') && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
+  TmaKernel k = pick(nvfp4, mod, s.per_thread, full);
   if (!k || s.tpr > 256 || s.rpc != 1) return cudaErrorInvalidValue;
   const TmaPlan p = tma_plan(k, mod, a.dim, s.tpr, forced_stages);
   if (p.stages < 1 || p.occ < 1) return cudaErrorInvalidConfiguration;
