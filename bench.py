@@ -428,6 +428,8 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the Python API with host buffers (pinned), fewer steps
     e2e = None if args.no_e2e else run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier)
+    # the NVFP4 producer feeding a block-scaled GEMM (context, outside the step)
+    chain = None if (args.no_chain or args.only) else run_chain(ap, dev, stream)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -436,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "step_alg_bytes": step_bytes,
                    "l2": "no flush: each step streams ~0.9 GB of distinct buffers (> 129 MB L2) between repeats "
                          "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
-        "roofline": roofline, "per_op": per_op, "e2e": e2e,
+        "roofline": roofline, "per_op": per_op, "e2e": e2e, "chain": chain,
         "gpu_launches": launches, "clocks": clocks.summary(),
         "timing": ("step: CUDA graph of %d steps replayed %d times; per_op: graph of %d back-to-back calls per "
                    "producer over rotating buffers > 3x L2, median of 3 replays" % (M, R, args.per_op_launches)),
@@ -444,6 +446,58 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
     return result
+
+
+def run_chain(ap, dev, stream, reps: int = 16):
+    """NVFP4 broadcast producer (5070x3072) followed by cuBLASLt's NVFP4
+    block-scaled GEMM against a (3072, 3072) NVFP4 weight made by the plain
+    producer: the chain and the GEMM alone, each a CUDA graph of `reps`
+    iterations timed with CUDA events.  The GEMM is library code; it is here
+    to show the producer's output consumed in place and what the producer adds
+    in front of its consumer."""
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        return {"unavailable": "this torch build has no float4_e2m1fn_x2 (no NVFP4 scaled GEMM)"}
+    M, N, K = 5070, 3072, 3072
+    wa, wb = synth.nvfp4_broadcast(M, K, 1004), synth.nvfp4_ln(N, K, 2009)
+    x, sc, sh = (wa.inputs[k].to(dev) for k in ("x", "scale", "shift"))
+    a_pk = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    a_sf = torch.empty((ap.swizzled_sf_size(M, K),), dtype=torch.uint8, device=dev)
+    fp4, e4 = torch.float4_e2m1fn_x2, torch.float8_e4m3fn
+    with torch.cuda.stream(stream):
+        b_pk, b_sf = ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(wb.inputs["x"].to(dev))
+
+        def produce():
+            ap.ada_layer_norm_quant_nvfp4_swizzled_bf16(x, sc, sh, packed=a_pk, sf_swizzled=a_sf)
+
+        def gemm():
+            return torch._scaled_mm(a_pk.view(fp4), b_pk.view(fp4).t(), a_sf.view(e4), b_sf.view(e4),
+                                    out_dtype=torch.bfloat16)
+        produce()
+        gemm()
+        graphs = {}
+        for name, body in (("gemm", gemm), ("chain", lambda: (produce(), gemm()))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    body()
+            g.replay()
+            graphs[name] = g
+        stream.synchronize()
+        us = {}
+        for name in ("gemm", "chain", "gemm", "chain"):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graphs[name].replay()
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e3 / reps
+            us[name] = min(us.get(name, t), t)
+    return {"producer": f"ada_layer_norm_quant_nvfp4_swizzled_bf16 {M}x{K}",
+            "consumer": f"cuBLASLt NVFP4 block-scaled GEMM (torch._scaled_mm) {M}x{N}x{K}, bf16 out",
+            "us_gemm": round(us["gemm"], 3), "us_chain": round(us["chain"], 3),
+            "us_producer_in_chain": round(us["chain"] - us["gemm"], 3),
+            "gemm_tflops": round(2.0 * M * N * K / (us["gemm"] * 1e-6) / 1e12, 1),
+            "timing": f"CUDA graphs of {reps} iterations, best of 2 replays"}
 
 
 def run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier):
@@ -671,6 +725,7 @@ def main():
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
     ap_.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap_.add_argument("--no-chain", action="store_true", help="skip the producer -> NVFP4 GEMM chain leg")
     ap_.add_argument("--no-extra", action="store_true",
                      help="skip the producers measured beside the step (modfp8, AWQ)")
     ap_.add_argument("--sweep", action="store_true", help="also time the FP8 broadcast row sweep")
