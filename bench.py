@@ -299,6 +299,24 @@ class ClockSampler:
 # our implementation
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank runs the same step on its own rows
+    (replicas, no data-path collective), so the job takes as long as the
+    slowest.  `device` is where the reduction tensor lives (the rank's GPU
+    under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the algorithmic bytes all ranks moved per step
+    over the (slowest rank's) step time."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import nvfp4_activation_producer_gb300 as ap
     from nvfp4_activation_producer_gb300 import build as b
@@ -397,13 +415,9 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clocks.mark("t1")
     clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_per_step = elapsed_ms / steps
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(step_bytes, world, ms_per_step)
     args.steps = steps
     launches = len(ops) * steps + sum(n * 3 for _, _, n, _, _ in per_op_graphs)
     del per_op_graphs
@@ -572,13 +586,9 @@ def run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier):
     with torch.cuda.stream(s_out):
         t1.record(s_out)
     barrier()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms / steps
-    return {"value": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+    return {"value": round(job_gbs(step_bytes, world, ms_step), 1), "unit": "GB/s",
             "ms_per_step": round(ms_step, 4), "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": "h2d / producers / d2h on three streams, two device buffer sets"}
 
