@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "orc.c")
 _HDR = os.path.join(_HERE, "orc.h")
 _SO = os.path.join(_HERE, "liborc.so")
 
-MOD_NONE, MOD_BCAST, MOD_PTOK, MOD_TABLE, MOD_MODFP8, MOD_AWQ = 0, 1, 2, 3, 4, 5
+MOD_NONE, MOD_BCAST, MOD_PTOK, MOD_TABLE, MOD_MODFP8, MOD_AWQ, MOD_SEG = 0, 1, 2, 3, 4, 5, 6
 
 
 def build(force: bool = False) -> str:
@@ -49,7 +49,9 @@ class _Mod(ctypes.Structure):
                 ("scale_idx", ctypes.c_int64),
                 ("scale_fp8", ctypes.c_void_p), ("shift_fp8", ctypes.c_void_p),
                 ("scale_deq", ctypes.c_float), ("shift_deq", ctypes.c_float),
-                ("inv_s", ctypes.c_void_p)]
+                ("inv_s", ctypes.c_void_p),
+                ("seg_idx", ctypes.c_void_p), ("seg_scale", ctypes.c_void_p), ("seg_shift", ctypes.c_void_p),
+                ("nseg", ctypes.c_int64)]
 
 
 _lib = None
@@ -89,6 +91,13 @@ def lib() -> ctypes.CDLL:
         L.orc_ln_quant_nvfp4.argtypes = [p, ctypes.POINTER(_Mod), f32, p, p, i64, i64, i32]
         L.orc_ln_quant_nvfp4_swizzled.restype = i32
         L.orc_ln_quant_nvfp4_swizzled.argtypes = [p, ctypes.POINTER(_Mod), f32, p, p, i64, i64, i32]
+        L.orc_ln_staged_bf16.restype = i32
+        L.orc_ln_staged_bf16.argtypes = [p, ctypes.POINTER(_Mod), f32, p, i64, i64, i32]
+        L.orc_nvfp4_2level.restype = i32
+        L.orc_nvfp4_2level.argtypes = [p, i64, i64, p, p, ctypes.POINTER(ctypes.c_float), i32]
+        L.orc_ln_quant_nvfp4_2level.restype = i32
+        L.orc_ln_quant_nvfp4_2level.argtypes = [p, ctypes.POINTER(_Mod), f32, p, p,
+                                                ctypes.POINTER(ctypes.c_float), i64, i64, i32]
         L.orc_adaln_modulation6.restype = i32
         L.orc_adaln_modulation6.argtypes = [p, p, p, i64, i64, i32]
         _lib = L
@@ -177,7 +186,8 @@ class _Keep:
 
 def _mod(keep: _Keep, kind: int, scale=None, shift=None, temb=None, table=None,
          shift_idx: int = 0, scale_idx: int = 0, scale_fp8=None, shift_fp8=None,
-         scale_deq: float = 1.0, shift_deq: float = 1.0, inv_s=None) -> _Mod:
+         scale_deq: float = 1.0, shift_deq: float = 1.0, inv_s=None, seg_idx=None, seg_scale=None,
+         seg_shift=None) -> _Mod:
     m = _Mod()
     m.kind = kind
     m.scale = keep.ptr(scale, np.uint16)
@@ -192,6 +202,10 @@ def _mod(keep: _Keep, kind: int, scale=None, shift=None, temb=None, table=None,
     m.scale_deq = float(scale_deq)
     m.shift_deq = float(shift_deq)
     m.inv_s = keep.ptr(inv_s, np.uint16)
+    m.seg_idx = keep.ptr(seg_idx, np.int32)
+    m.seg_scale = keep.ptr(seg_scale, np.uint16)
+    m.seg_shift = keep.ptr(seg_shift, np.uint16)
+    m.nseg = int(np.asarray(seg_scale).shape[0]) if seg_scale is not None else 0
     return m
 
 
@@ -245,6 +259,44 @@ def ln_quant_nvfp4(x, kind=MOD_NONE, eps=1e-5, nthreads=None, swizzled=True, **m
         _check(lib().orc_ln_quant_nvfp4(x.ctypes.data, ctypes.byref(m), eps,
                                         packed.ctypes.data, sf.ctypes.data, rows, dim, nt))
     return packed, sf
+
+
+def staged(x, kind=MOD_NONE, eps=1e-5, nthreads=None, **mod) -> np.ndarray:
+    """bf16 bits (rows, dim) of v = bf16(fp32(y)), the NVFP4 producers' staged values."""
+    keep = _Keep()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    rows, dim = x.shape
+    m = _mod(keep, kind, **mod)
+    v = np.empty((rows, dim), dtype=np.uint16)
+    _check(lib().orc_ln_staged_bf16(x.ctypes.data, ctypes.byref(m), eps, v.ctypes.data, rows, dim,
+                                    nthreads or default_threads()))
+    return v
+
+
+def nvfp4_2level(v, nthreads=None):
+    """Two-level NVFP4 of bf16 bits v (rows, dim): (packed, swizzled scales, tensor scale)."""
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    rows, dim = v.shape
+    packed = np.empty((rows, dim // 2), dtype=np.uint8)
+    sf = np.empty(max(swizzled_sf_size(rows, dim), 0), dtype=np.uint8)
+    ts = ctypes.c_float()
+    _check(lib().orc_nvfp4_2level(v.ctypes.data, rows, dim, packed.ctypes.data, sf.ctypes.data, ctypes.byref(ts),
+                                  nthreads or default_threads()))
+    return packed, sf, ts.value
+
+
+def ln_quant_nvfp4_2level(x, kind=MOD_NONE, eps=1e-5, nthreads=None, **mod):
+    """LayerNorm producer with two-level NVFP4 output: (packed, swizzled scales, tensor scale)."""
+    keep = _Keep()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    rows, dim = x.shape
+    m = _mod(keep, kind, **mod)
+    packed = np.empty((rows, dim // 2), dtype=np.uint8)
+    sf = np.empty(max(swizzled_sf_size(rows, dim), 0), dtype=np.uint8)
+    ts = ctypes.c_float()
+    _check(lib().orc_ln_quant_nvfp4_2level(x.ctypes.data, ctypes.byref(m), eps, packed.ctypes.data, sf.ctypes.data,
+                                           ctypes.byref(ts), rows, dim, nthreads or default_threads()))
+    return packed, sf, ts.value
 
 
 def adaln_modulation6(params, modulation, nthreads=None) -> np.ndarray:

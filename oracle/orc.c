@@ -47,6 +47,9 @@
  *   R16 AWQ producer: the bf16 smoothing vector inv_s multiplies the modulated
  *      activation, y * inv_s, before the FP8 quantiser (which then divides by
  *      act_scale as in R3).
+ *   R17-R19 two-level NVFP4: see orc_nvfp4_2level.
+ *   R20 segmented modulation: row r uses row seg_idx[r] of (nseg, dim) bf16
+ *      scale/shift tables, with the broadcast producers' arithmetic.
  */
 #include "orc.h"
 
@@ -237,6 +240,15 @@ static void mod_at(const orc_mod_t* m, int64_t r, int64_t d, int64_t dim,
       *scale = orc_bf16_to_f64(m->scale[d]);
       *shift = orc_bf16_to_f64(m->shift[d]);
       return;
+    case ORC_MOD_SEG: {
+      /* segmented modulation (h3-blackwell-runtime compare page: "segment-
+       * specific shift and scale selection", the request-layout segment index
+       * of Phase 1): row r takes row seg_idx[r] of the (nseg, dim) tables. */
+      const int64_t g = m->seg_idx[r];
+      *scale = orc_bf16_to_f64(m->seg_scale[g * dim + d]);
+      *shift = orc_bf16_to_f64(m->seg_shift[g * dim + d]);
+      return;
+    }
     default:
       *scale = 0.0;
       *shift = 0.0;
@@ -383,6 +395,103 @@ int orc_ln_quant_nvfp4_swizzled(const uint16_t* x, const orc_mod_t* mod, float e
   int rc = orc_ln_quant_nvfp4(x, mod, eps, packed, logical, rows, dim, nthreads);
   if (rc == 0) orc_swizzle_scales(logical, rows, dim, sf_swizzled);
   free(logical);
+  return rc;
+}
+
+/* ---- staged values and the two-level NVFP4 contract ---------------------- */
+
+typedef struct {
+  const uint16_t* x; const orc_mod_t* mod; float eps; int64_t dim; uint16_t* v;
+} stage_ctx;
+
+static void row_stage(void* p, int64_t r, double* y) {
+  stage_ctx* c = (stage_ctx*)p;
+  modulated_row(c->x + r * c->dim, c->mod, r, c->eps, y, c->dim);
+  for (int64_t d = 0; d < c->dim; ++d) c->v[r * c->dim + d] = orc_bf16_from_f32((float)y[d]);
+}
+
+int orc_ln_staged_bf16(const uint16_t* x, const orc_mod_t* mod, float eps, uint16_t* v,
+                       int64_t rows, int64_t dim, int nthreads) {
+  if (rows < 0 || dim <= 0) return -1;
+  stage_ctx c = {x, mod, eps, dim, v};
+  for_rows(row_stage, &c, rows, dim, nthreads);
+  return 0;
+}
+
+/* Two-level NVFP4 (h3-blackwell-runtime compare page: NVFP4_STREAMING_DESIGN.md
+ * "Numerical Constraint" -- one exact global bf16 absolute maximum, one fp32
+ * tensor scale derived from it, e4m3 block scales per 16 values, e2m1 codes
+ * using both scales; the P1 producer-consumer checkpoint's
+ * "numerical_contract" -- block scale (amax / 6.0f) / global_scale clamped by
+ * fminf(., 448.0f)).  Readings:
+ *   R17 tensor scale ts = bf16(fp32(amax_g / 2688)), 2688 = 6 (largest e2m1)
+ *       x 448 (largest e4m3); every tensor scale the page prints is a bf16
+ *       value.  All-zero input: ts = 0.
+ *   R18 block scale s = e4m3(fminf(fp32(fp32(amax_b / 6) / ts), 448)), both
+ *       divisions fp32 as printed; fminf returns 448 for the 0/0 of an
+ *       all-zero tensor, which reproduces the page's scale byte 126 there.
+ *   R19 code = e2m1 nearest of v / (decode(s) * ts), exact quotient (the
+ *       product is exact); a zero denominator gives signed zeros.  The page's
+ *       approximate reciprocal is replaced by the exact quotient, as in R5. */
+typedef struct {
+  const uint16_t* v; int64_t dim; uint8_t* packed; uint8_t* sf; float ts;
+} tl_ctx;
+
+static void row_2level(void* p, int64_t r, double* scratch) {
+  tl_ctx* c = (tl_ctx*)p;
+  (void)scratch;
+  const int64_t dim = c->dim, nblk = dim / 16;
+  const uint16_t* vr = c->v + r * dim;
+  uint8_t* pk = c->packed + r * (dim / 2);
+  uint8_t* sf = c->sf + r * nblk;
+  for (int64_t b = 0; b < nblk; ++b) {
+    double amax = 0.0;
+    for (int k = 0; k < 16; ++k) {
+      const double a = fabs(orc_bf16_to_f64(vr[b * 16 + k]));
+      if (a > amax) amax = a;
+    }
+    float q = (float)amax / 6.0f;
+    q = q / c->ts;
+    q = fminf(q, 448.0f);
+    const uint8_t s = orc_e4m3_encode((double)q);
+    sf[b] = s;
+    const double den = orc_e4m3_decode(s) * (double)c->ts;
+    for (int k = 0; k < 16; k += 2) {
+      const uint8_t lo = orc_e2m1_encode(orc_bf16_to_f64(vr[b * 16 + k]), den);
+      const uint8_t hi = orc_e2m1_encode(orc_bf16_to_f64(vr[b * 16 + k + 1]), den);
+      pk[b * 8 + k / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+int orc_nvfp4_2level(const uint16_t* v, int64_t rows, int64_t dim, uint8_t* packed,
+                     uint8_t* sf_swizzled, float* tensor_scale, int nthreads) {
+  if (rows < 0 || dim <= 0 || dim % 16 != 0) return -1;
+  double amax = 0.0;
+  for (int64_t i = 0; i < rows * dim; ++i) {
+    const double a = fabs(orc_bf16_to_f64(v[i]));
+    if (a > amax) amax = a;
+  }
+  const float ts = (float)orc_bf16_to_f64(orc_bf16_from_f32((float)amax / 2688.0f));
+  uint8_t* logical = (uint8_t*)malloc((size_t)(rows * (dim / 16) + 1));
+  if (!logical) return -2;
+  tl_ctx c = {v, dim, packed, logical, ts};
+  for_rows(row_2level, &c, rows, dim, nthreads);
+  orc_swizzle_scales(logical, rows, dim, sf_swizzled);
+  free(logical);
+  *tensor_scale = ts;
+  return 0;
+}
+
+int orc_ln_quant_nvfp4_2level(const uint16_t* x, const orc_mod_t* mod, float eps, uint8_t* packed,
+                              uint8_t* sf_swizzled, float* tensor_scale, int64_t rows, int64_t dim,
+                              int nthreads) {
+  if (rows < 0 || dim <= 0 || dim % 16 != 0) return -1;
+  uint16_t* v = (uint16_t*)malloc((size_t)(rows * dim + 1) * sizeof(uint16_t));
+  if (!v) return -2;
+  int rc = orc_ln_staged_bf16(x, mod, eps, v, rows, dim, nthreads);
+  if (rc == 0) rc = orc_nvfp4_2level(v, rows, dim, packed, sf_swizzled, tensor_scale, nthreads);
+  free(v);
   return rc;
 }
 

@@ -49,7 +49,7 @@ void orc_row_stats(const uint16_t* x, int64_t dim, float eps, double* mean, doub
 /* ---- producers ---------------------------------------------------------- */
 /* modulation sources */
 enum { ORC_MOD_NONE = 0, ORC_MOD_BCAST = 1, ORC_MOD_PTOK = 2, ORC_MOD_TABLE = 3,
-       ORC_MOD_MODFP8 = 4, ORC_MOD_AWQ = 5 };
+       ORC_MOD_MODFP8 = 4, ORC_MOD_AWQ = 5, ORC_MOD_SEG = 6 };
 
 typedef struct {
   int kind;
@@ -62,6 +62,10 @@ typedef struct {
   const uint8_t*  shift_fp8;
   float scale_deq, shift_deq; /* MODFP8: fp32 multipliers of the decoded codes */
   const uint16_t* inv_s;      /* AWQ: (dim,) bf16 smoothing multipliers    */
+  const int32_t*  seg_idx;    /* SEG: (rows,) segment of each row          */
+  const uint16_t* seg_scale;  /* SEG: (nseg, dim) bf16                      */
+  const uint16_t* seg_shift;
+  int64_t nseg;
 } orc_mod_t;
 
 /* y = LN(x) * (1 + scale) + shift, as double, for all rows (rows, dim);
@@ -82,6 +86,21 @@ int orc_ln_quant_nvfp4(const uint16_t* x, const orc_mod_t* mod, float eps,
 int orc_ln_quant_nvfp4_swizzled(const uint16_t* x, const orc_mod_t* mod, float eps,
                                 uint8_t* packed, uint8_t* sf_swizzled,
                                 int64_t rows, int64_t dim, int nthreads);
+
+/* The bf16-staged modulated values v = bf16(fp32(y)) of the NVFP4 producers. */
+int orc_ln_staged_bf16(const uint16_t* x, const orc_mod_t* mod, float eps, uint16_t* v,
+                       int64_t rows, int64_t dim, int nthreads);
+
+/* Two-level NVFP4 of bf16 values v (rows, dim): global amax -> fp32 tensor
+ * scale (bf16-valued), e4m3 block scales relative to it, e2m1 codes.  Writes
+ * packed (rows, dim/2), the swizzled scale buffer and *tensor_scale. */
+int orc_nvfp4_2level(const uint16_t* v, int64_t rows, int64_t dim, uint8_t* packed,
+                     uint8_t* sf_swizzled, float* tensor_scale, int nthreads);
+
+/* LayerNorm producer with the two-level NVFP4 output. */
+int orc_ln_quant_nvfp4_2level(const uint16_t* x, const orc_mod_t* mod, float eps, uint8_t* packed,
+                              uint8_t* sf_swizzled, float* tensor_scale, int64_t rows, int64_t dim,
+                              int nthreads);
 
 /* six-way: out is (6, batch*seq, dim) bf16 bits; params (batch*seq, 6, dim). */
 int orc_adaln_modulation6(const float* params, const float* modulation, uint16_t* out,
