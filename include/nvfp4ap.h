@@ -65,6 +65,10 @@ enum nvfp4ap_status {
 
 #define NVFP4AP_MAX_DIM 32768
 
+/* Bytes of the caller-owned device workspace of the two-level NVFP4
+ * producers (one word; 4-byte aligned). */
+#define NVFP4AP_2LEVEL_WORKSPACE_BYTES 4
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvfp4ap_status_string(int status);
 
@@ -75,7 +79,8 @@ int nvfp4ap_version(void);
  * asynchronous bulk copies and wait on them with a bounded wait (about one
  * second).  If a wait ever runs out, the kernel stops early, leaves its
  * output incomplete and sets a fault word on the current device instead of
- * hanging.  This call reads and clears that word: NVFP4AP_ERR_FAULT if any
+ * hanging.  The segmented producers set it too when a row's segment index is
+ * out of range.  This call reads and clears that word: NVFP4AP_ERR_FAULT if any
  * kernel on the current device has set it since the last call, NVFP4AP_OK if
  * not, NVFP4AP_ERR_LAUNCH if the device could not be read.  Unlike every
  * other entry point it synchronises with the device (a blocking copy). */
@@ -173,6 +178,19 @@ int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const vo
                                       const void* inv_s, const float* act_scale, float eps, void* out,
                                       int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
+/* Segmented modulation (h3-blackwell-runtime compare page: segment-specific
+ * shift and scale selection with a per-row segment index).
+ * seg_idx: device (rows,) int32, 4-byte aligned; row r takes row seg_idx[r] of
+ * seg_scale, seg_shift: device (nseg, dim) bf16, 16-byte aligned.
+ *   y[d] = (x[r,d] - mean) * rstd * (1 + seg_scale[g,d]) + seg_shift[g,d]
+ * dim % 8 == 0 and x 16-byte aligned (NVFP4AP_ERR_DIM / _ALIGN otherwise).
+ * nseg < 1 gives NVFP4AP_ERR_INDEX.  An index outside [0, nseg) cannot be
+ * checked on the host: that row is produced with zero modulation and the
+ * device fault word is set (nvfp4ap_take_device_fault). */
+int ada_layer_norm_quant_fp8_seg_bf16(const void* x, const int32_t* seg_idx, const void* seg_scale,
+                                      const void* seg_shift, int64_t nseg, const float* act_scale, float eps,
+                                      void* out, int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
 /* README "Available Functions": layer_norm_no_affine_quant_fp8_static_bf16.
  * No modulation: y = (x - mean) * rstd. */
 int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
@@ -216,6 +234,45 @@ int ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(const void* x, const void* s
 int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,
                                                    void* sf_swizzled, int64_t rows, int64_t dim,
                                                    nvfp4ap_stream_t stream);
+
+/* Single-level NVFP4 with the segmented modulation of
+ * ada_layer_norm_quant_fp8_seg_bf16 (same index and table rules). */
+int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* seg_idx, const void* seg_scale,
+                                                 const void* seg_shift, int64_t nseg, float eps, void* packed,
+                                                 void* sf_swizzled, int64_t rows, int64_t dim,
+                                                 nvfp4ap_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Two-level NVFP4 producers (h3-blackwell-runtime compare page:
+ * NVFP4_STREAMING_DESIGN.md "Numerical Constraint" -- one exact global bf16
+ * absolute maximum, one fp32 tensor scale derived from it, e4m3 block scales,
+ * e2m1 codes using both; the P1 checkpoint's numerical contract -- block
+ * scale (amax / 6) / global scale, clamped at 448).  For the staged values
+ * v = bf16(y) of the whole (rows, dim) tensor:
+ *   amax = max |v|;  ts = bf16(fp32(amax / 2688))   (2688 = 6 * 448)
+ *   per 16-element block b: s = e4m3fn(fminf(fp32(fp32(amax_b / 6) / ts), 448))
+ *   code_k = e2m1 nearest of v_k / (decode(s) * ts), ties to even, saturating;
+ *            a zero divisor gives +-0 codes
+ * The library divides exactly where the page's runtime multiplies by an
+ * approximate reciprocal.  Outputs: packed and sf_swizzled as for the
+ * single-level producers, and *tensor_scale = ts (device fp32, 4-byte
+ * aligned) -- the dequantised value is e2m1 * decode(s) * ts.
+ * workspace: caller-owned device memory of NVFP4AP_2LEVEL_WORKSPACE_BYTES,
+ * 4-byte aligned, cleared and used by the call (two calls on concurrent
+ * streams need two workspaces).  Three operations on `stream`: a clear of the
+ * workspace, the maximum pass, the quantising pass (graph-capturable). */
+int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed, void* sf_swizzled,
+                                                 float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
+                                                 nvfp4ap_stream_t stream);
+/* broadcast scale, shift: (dim,) bf16, 16-byte aligned */
+int ada_layer_norm_quant_nvfp4_2level_bf16(const void* x, const void* scale, const void* shift, float eps,
+                                           void* packed, void* sf_swizzled, float* tensor_scale, void* workspace,
+                                           int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+/* segmented modulation as in ada_layer_norm_quant_fp8_seg_bf16 */
+int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, const int32_t* seg_idx, const void* seg_scale,
+                                               const void* seg_shift, int64_t nseg, float eps, void* packed,
+                                               void* sf_swizzled, float* tensor_scale, void* workspace,
+                                               int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
 /* README "Available Functions" / "Tensor Contract": swizzled_sf_size.
  * Bytes of the swizzled scale buffer: ceil(rows/128)*128 * ceil(dim/16/4)*4.

@@ -26,6 +26,12 @@ __all__ = [
     "layer_norm_no_affine_quant_fp8_static_bf16",
     "ada_layer_norm_quant_nvfp4_swizzled_bf16",
     "ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16",
+    "ada_layer_norm_quant_fp8_seg_bf16",
+    "ada_layer_norm_quant_nvfp4_swizzled_seg_bf16",
+    "layer_norm_no_affine_quant_nvfp4_2level_bf16",
+    "ada_layer_norm_quant_nvfp4_2level_bf16",
+    "ada_layer_norm_quant_nvfp4_2level_seg_bf16",
+    "WORKSPACE_2LEVEL_BYTES",
     "layer_norm_no_affine_quant_nvfp4_swizzled_bf16",
     "adaln_modulation6_bf16",
     "swizzled_sf_size",
@@ -38,6 +44,7 @@ LIB_PATH = _build.LIB
 
 OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT, ERR_SCRATCH = range(10)
 MAX_DIM = 32768
+WORKSPACE_2LEVEL_BYTES = 4
 
 
 class NvFp4ApError(RuntimeError):
@@ -80,6 +87,16 @@ def _load() -> ctypes.CDLL:
     L.awq_ada_layer_norm_quant_fp8_bf16.argtypes = [p, p, p, p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.restype = i32
     L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.argtypes = [p, p, p, p, p, f32, p, p, i64, i64, p]
+    L.ada_layer_norm_quant_fp8_seg_bf16.restype = i32
+    L.ada_layer_norm_quant_fp8_seg_bf16.argtypes = [p, p, p, p, i64, p, f32, p, i64, i64, p]
+    L.ada_layer_norm_quant_nvfp4_swizzled_seg_bf16.restype = i32
+    L.ada_layer_norm_quant_nvfp4_swizzled_seg_bf16.argtypes = [p, p, p, p, i64, f32, p, p, i64, i64, p]
+    L.layer_norm_no_affine_quant_nvfp4_2level_bf16.restype = i32
+    L.layer_norm_no_affine_quant_nvfp4_2level_bf16.argtypes = [p, f32, p, p, p, p, i64, i64, p]
+    L.ada_layer_norm_quant_nvfp4_2level_bf16.restype = i32
+    L.ada_layer_norm_quant_nvfp4_2level_bf16.argtypes = [p, p, p, f32, p, p, p, p, i64, i64, p]
+    L.ada_layer_norm_quant_nvfp4_2level_seg_bf16.restype = i32
+    L.ada_layer_norm_quant_nvfp4_2level_seg_bf16.argtypes = [p, p, p, p, i64, f32, p, p, p, p, i64, i64, p]
     L.layer_norm_no_affine_quant_fp8_static_bf16.restype = i32
     L.layer_norm_no_affine_quant_fp8_static_bf16.argtypes = [p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_nvfp4_swizzled_bf16.restype = i32
@@ -319,6 +336,101 @@ def layer_norm_no_affine_quant_nvfp4_swizzled_bf16(x, eps: float = 1e-5, packed=
                                                                 rows, dim, _stream(dev))
     _raise("layer_norm_no_affine_quant_nvfp4_swizzled_bf16", rc)
     return packed, sf_swizzled
+
+
+# ---------------------------------------------------------------------------
+# segmented modulation and two-level NVFP4
+# ---------------------------------------------------------------------------
+
+def _seg(seg_idx, seg_scale, seg_shift, rows, dim, dev):
+    if not isinstance(seg_scale, torch.Tensor) or seg_scale.dim() != 2:
+        raise ValueError("seg_scale must be a 2-D (nseg, dim) tensor")
+    nseg = seg_scale.shape[0]
+    _need(seg_idx, "seg_idx", torch.int32, (rows,), dev)
+    _need(seg_scale, "seg_scale", torch.bfloat16, (nseg, dim), dev)
+    _need(seg_shift, "seg_shift", torch.bfloat16, (nseg, dim), dev)
+    return nseg
+
+
+def ada_layer_norm_quant_fp8_seg_bf16(x, seg_idx, seg_scale, seg_shift, act_scale, eps: float = 1e-5, out=None):
+    """Segmented modulation: row r uses row seg_idx[r] of the (nseg, dim) bf16 scale/shift tables."""
+    rows, dim, dev = _x(x)
+    nseg = _seg(seg_idx, seg_scale, seg_shift, rows, dim, dev)
+    _scalar(act_scale, "act_scale", dev)
+    out = _fp8_out(out, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_fp8_seg_bf16(_ptr(x), _ptr(seg_idx), _ptr(seg_scale), _ptr(seg_shift), nseg,
+                                                   _ptr(act_scale), eps, _ptr(out), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_fp8_seg_bf16", rc)
+    return out
+
+
+def ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(x, seg_idx, seg_scale, seg_shift, eps: float = 1e-5, packed=None,
+                                                 sf_swizzled=None):
+    """Single-level NVFP4 with segmented modulation."""
+    rows, dim, dev = _x(x)
+    nseg = _seg(seg_idx, seg_scale, seg_shift, rows, dim, dev)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    rc = _load().ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(_ptr(x), _ptr(seg_idx), _ptr(seg_scale),
+                                                              _ptr(seg_shift), nseg, eps, _ptr(packed),
+                                                              _ptr(sf_swizzled), rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_nvfp4_swizzled_seg_bf16", rc)
+    return packed, sf_swizzled
+
+
+def _twolevel_extra(tensor_scale, workspace, dev):
+    if tensor_scale is None:
+        tensor_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    else:
+        _scalar(tensor_scale, "tensor_scale", dev)
+    if workspace is None:
+        workspace = torch.empty((WORKSPACE_2LEVEL_BYTES,), dtype=torch.uint8, device=dev)
+    elif (not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or workspace.device != dev or
+          workspace.numel() * workspace.element_size() < WORKSPACE_2LEVEL_BYTES):
+        raise ValueError(f"workspace must be a CUDA tensor of at least {WORKSPACE_2LEVEL_BYTES} bytes on {dev}")
+    return tensor_scale, workspace
+
+
+def layer_norm_no_affine_quant_nvfp4_2level_bf16(x, eps: float = 1e-5, packed=None, sf_swizzled=None,
+                                                 tensor_scale=None, workspace=None):
+    """LayerNorm (no affine) -> two-level NVFP4: (packed, sf_swizzled, tensor_scale)."""
+    rows, dim, dev = _x(x)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    rc = _load().layer_norm_no_affine_quant_nvfp4_2level_bf16(_ptr(x), eps, _ptr(packed), _ptr(sf_swizzled),
+                                                              _ptr(tensor_scale), _ptr(workspace), rows, dim,
+                                                              _stream(dev))
+    _raise("layer_norm_no_affine_quant_nvfp4_2level_bf16", rc)
+    return packed, sf_swizzled, tensor_scale
+
+
+def ada_layer_norm_quant_nvfp4_2level_bf16(x, scale, shift, eps: float = 1e-5, packed=None, sf_swizzled=None,
+                                           tensor_scale=None, workspace=None):
+    """Broadcast modulation -> two-level NVFP4: (packed, sf_swizzled, tensor_scale)."""
+    rows, dim, dev = _x(x)
+    _need(scale, "scale", torch.bfloat16, (dim,), dev)
+    _need(shift, "shift", torch.bfloat16, (dim,), dev)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    rc = _load().ada_layer_norm_quant_nvfp4_2level_bf16(_ptr(x), _ptr(scale), _ptr(shift), eps, _ptr(packed),
+                                                        _ptr(sf_swizzled), _ptr(tensor_scale), _ptr(workspace),
+                                                        rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_nvfp4_2level_bf16", rc)
+    return packed, sf_swizzled, tensor_scale
+
+
+def ada_layer_norm_quant_nvfp4_2level_seg_bf16(x, seg_idx, seg_scale, seg_shift, eps: float = 1e-5, packed=None,
+                                               sf_swizzled=None, tensor_scale=None, workspace=None):
+    """Segmented modulation -> two-level NVFP4: (packed, sf_swizzled, tensor_scale)."""
+    rows, dim, dev = _x(x)
+    nseg = _seg(seg_idx, seg_scale, seg_shift, rows, dim, dev)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    rc = _load().ada_layer_norm_quant_nvfp4_2level_seg_bf16(_ptr(x), _ptr(seg_idx), _ptr(seg_scale),
+                                                            _ptr(seg_shift), nseg, eps, _ptr(packed),
+                                                            _ptr(sf_swizzled), _ptr(tensor_scale), _ptr(workspace),
+                                                            rows, dim, _stream(dev))
+    _raise("ada_layer_norm_quant_nvfp4_2level_seg_bf16", rc)
+    return packed, sf_swizzled, tensor_scale
 
 
 # ---------------------------------------------------------------------------

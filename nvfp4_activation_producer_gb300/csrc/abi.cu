@@ -228,6 +228,55 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   return finish(launch_ln_fp8(a, mod, vec, s, st));
 }
 
+// Segmented modulation: index and tables present and aligned.
+int check_seg(const LnArgs& a) {
+  if (!a.seg_idx || !a.seg_scale || !a.seg_shift) return NVFP4AP_ERR_NULL;
+  if (a.nseg < 1) return NVFP4AP_ERR_INDEX;
+  if (!aligned(a.seg_idx, 4) || !aligned(a.seg_scale, 16) || !aligned(a.seg_shift, 16)) return NVFP4AP_ERR_ALIGN;
+  return NVFP4AP_OK;
+}
+
+// Segmented modulation producers (FP8 and single-level NVFP4) on the register
+// row kernels: dim % 8 (FP8) or % 16 (NVFP4), 16-byte aligned x and outputs.
+int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
+  int rc = check_common(a.rows, a.dim, a.eps);
+  if (rc) return rc;
+  if (a.dim % (nvfp4 ? 16 : 8) != 0) return NVFP4AP_ERR_DIM;
+  if (a.rows == 0) return NVFP4AP_OK;
+  if (!a.x || !a.out || (nvfp4 ? !a.sf : !a.act_scale)) return NVFP4AP_ERR_NULL;
+  if ((rc = check_seg(a)) != NVFP4AP_OK) return rc;
+  if (!aligned(a.x, 16) || !aligned(a.out, 8) || (!nvfp4 && !aligned(a.act_scale, 4))) return NVFP4AP_ERR_ALIGN;
+  RowShape s{};
+  if (!pick_rows(MOD_SEG, a.dim, &s)) return NVFP4AP_ERR_DIM;
+  const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
+  if (!grid_ok(work, s.rpc)) return NVFP4AP_ERR_SHAPE;
+  return finish(launch_ln_seg(a, nvfp4, s, st));
+}
+
+// Two-level NVFP4 producers: as the NVFP4 producers, plus a 4-byte aligned
+// tensor-scale output and workspace word.
+int run_2level(LnArgs& a, int mod, cudaStream_t st) {
+  int rc = check_common(a.rows, a.dim, a.eps);
+  if (rc) return rc;
+  if (a.dim % 16 != 0) return NVFP4AP_ERR_DIM;
+  if (a.rows == 0) return NVFP4AP_OK;
+  if (!a.x || !a.out || !a.sf || !a.tensor_scale || !a.amax_ws) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
+  if (mod == MOD_SEG && (rc = check_seg(a)) != NVFP4AP_OK) return rc;
+  if (!aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.tensor_scale, 4) || !aligned(a.amax_ws, 4))
+    return NVFP4AP_ERR_ALIGN;
+  if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
+  RowShape s{};
+  if (!pick_rows(mod, a.dim, &s)) return NVFP4AP_ERR_DIM;
+  if (!grid_ok((a.rows + 127) / 128 * 128, s.rpc)) return NVFP4AP_ERR_SHAPE;
+  // the register-capped instances for rows that exactly fill the CTA's
+  // chunks (NVFP4AP_FULL=0 turns them off); unmodulated rows only -- the
+  // broadcast instances spill at 40 registers
+  const bool full = !env_off("NVFP4AP_FULL") && mod == MOD_NONE && s.tpr <= 128 && s.per_thread >= 2 &&
+                    s.per_thread <= 4 && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
+  return finish(launch_ln_2level(a, mod, s, full, st));
+}
+
 int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -315,7 +364,8 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
     case NVFP4AP_ERR_ALIGN: return "a pointer misses its alignment rule";
     case NVFP4AP_ERR_LAUNCH: return "CUDA launch failed";
     case NVFP4AP_ERR_VALUE: return "eps is negative or not finite";
-    case NVFP4AP_ERR_FAULT: return "a producer kernel's bounded wait ran out (its output is incomplete)";
+    case NVFP4AP_ERR_FAULT:
+      return "a producer kernel's bounded wait ran out, or a segment index was out of range (see the output)";
     case NVFP4AP_ERR_SCRATCH: return "the call needs more per-CTA words than the library's static scratch array holds";
     default: return "unknown status";
   }
@@ -324,12 +374,12 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
-  unsigned int f = 0u, g = 0u;
-  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess) {
+  unsigned int f = 0u, g = 0u, h = 0u;
+  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  return (f | g) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  return (f | g | h) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
@@ -449,6 +499,74 @@ NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x,
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.sf = sf_swizzled;
   return run_nvfp4(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_seg_bf16(const void* x, const int32_t* seg_idx, const void* seg_scale,
+                                                     const void* seg_shift, int64_t nseg, const float* act_scale,
+                                                     float eps, void* out, int64_t rows, int64_t dim,
+                                                     nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, out, rows, dim);
+  a.seg_idx = seg_idx;
+  a.seg_scale = static_cast<const uint16_t*>(seg_scale);
+  a.seg_shift = static_cast<const uint16_t*>(seg_shift);
+  a.nseg = nseg;
+  a.act_scale = act_scale;
+  return run_seg(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* seg_idx,
+                                                                const void* seg_scale, const void* seg_shift,
+                                                                int64_t nseg, float eps, void* packed,
+                                                                void* sf_swizzled, int64_t rows, int64_t dim,
+                                                                nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.seg_idx = seg_idx;
+  a.seg_scale = static_cast<const uint16_t*>(seg_scale);
+  a.seg_shift = static_cast<const uint16_t*>(seg_shift);
+  a.nseg = nseg;
+  a.sf = sf_swizzled;
+  return run_seg(a, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed,
+                                                                void* sf_swizzled, float* tensor_scale,
+                                                                void* workspace, int64_t rows, int64_t dim,
+                                                                nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.sf = sf_swizzled;
+  a.tensor_scale = tensor_scale;
+  a.amax_ws = static_cast<unsigned int*>(workspace);
+  return run_2level(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_bf16(const void* x, const void* scale, const void* shift,
+                                                          float eps, void* packed, void* sf_swizzled,
+                                                          float* tensor_scale, void* workspace, int64_t rows,
+                                                          int64_t dim, nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.sf = sf_swizzled;
+  a.tensor_scale = tensor_scale;
+  a.amax_ws = static_cast<unsigned int*>(workspace);
+  return run_2level(a, MOD_BCAST, reinterpret_cast<cudaStream_t>(stream));
+}
+
+NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, const int32_t* seg_idx,
+                                                              const void* seg_scale, const void* seg_shift,
+                                                              int64_t nseg, float eps, void* packed,
+                                                              void* sf_swizzled, float* tensor_scale,
+                                                              void* workspace, int64_t rows, int64_t dim,
+                                                              nvfp4ap_stream_t stream) {
+  LnArgs a = ln_args(x, eps, packed, rows, dim);
+  a.seg_idx = seg_idx;
+  a.seg_scale = static_cast<const uint16_t*>(seg_scale);
+  a.seg_shift = static_cast<const uint16_t*>(seg_shift);
+  a.nseg = nseg;
+  a.sf = sf_swizzled;
+  a.tensor_scale = tensor_scale;
+  a.amax_ws = static_cast<unsigned int*>(workspace);
+  return run_2level(a, MOD_SEG, reinterpret_cast<cudaStream_t>(stream));
 }
 
 NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {

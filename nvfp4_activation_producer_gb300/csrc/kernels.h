@@ -33,7 +33,8 @@ cudaError_t launch_maybe_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
 //   MOD_TABLE   temb[r, idx, :] (bf16) + table[idx, :] (fp32)
 //   MOD_MODFP8  e4m3 (dim,) scale/shift times fp32 device scalars scale_deq/shift_deq
 //   MOD_AWQ     bf16 (dim,) scale/shift, output multiplied by bf16 (dim,) inv_s
-enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3, MOD_MODFP8 = 4, MOD_AWQ = 5 };
+//   MOD_SEG     row r takes row seg_idx[r] of bf16 (nseg, dim) scale/shift tables
+enum ModKind { MOD_NONE = 0, MOD_BCAST = 1, MOD_PTOK = 2, MOD_TABLE = 3, MOD_MODFP8 = 4, MOD_AWQ = 5, MOD_SEG = 6 };
 
 // sources whose scale/shift are the same (dim,) vector for every row
 constexpr bool mod_is_bcast(int mod) { return mod == MOD_BCAST || mod == MOD_MODFP8 || mod == MOD_AWQ; }
@@ -52,6 +53,12 @@ struct LnArgs {
   const float* scale_deq; // MODFP8: device scalars
   const float* shift_deq;
   const uint16_t* inv_s;  // AWQ: (dim,) bf16
+  const int32_t* seg_idx;     // SEG: (rows,) segment of each row
+  const uint16_t* seg_scale;  // SEG: (nseg, dim) bf16
+  const uint16_t* seg_shift;
+  int64_t nseg;
+  unsigned int* amax_ws;      // two-level: one device word (the tensor's largest |v| as fp32 bits)
+  float* tensor_scale;        // two-level: device fp32 output
   float eps;
   void* out;              // FP8: (rows, dim) e4m3; NVFP4: packed (rows, dim/2)
   void* sf;               // NVFP4: swizzled scales
@@ -118,6 +125,17 @@ bool ln_tma_supported(bool nvfp4, int mod, RowShape s);
 cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
                           int ctas_per_sm, cudaStream_t st);
 cudaError_t take_tma_fault(unsigned int* fault);
+
+// Segmented modulation (MOD_SEG) on the register row kernels: FP8 (dim % 8
+// == 0, 16-byte aligned inputs) or single-level NVFP4.
+cudaError_t launch_ln_seg(const LnArgs& a, bool nvfp4, RowShape s, cudaStream_t st);
+// Two-level NVFP4: clears a.amax_ws, runs the maximum pass, then the
+// quantising pass (writes packed, sf and *a.tensor_scale); mod MOD_NONE,
+// MOD_BCAST or MOD_SEG.  `full`: rows exactly fill tpr * per_thread chunks
+// (tpr <= 128) -- the register-capped instances.
+cudaError_t launch_ln_2level(const LnArgs& a, int mod, RowShape s, bool full, cudaStream_t st);
+// Reads and clears the word set when a segment index was out of range.
+cudaError_t take_seg_fault(unsigned int* fault);
 
 // Six-way modulation (K7).
 struct Mod6Args {

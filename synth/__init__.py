@@ -153,6 +153,38 @@ def fp8_awq(rows: int, dim: int, seed: int, act_scale: float = 0.025, eps: float
                     {"eps": eps})
 
 
+# The segment layout of the h3-blackwell-runtime compare page's attention-output
+# record (37,810 packed tokens): rows [0, 100) use table row 1, [100, 514) row 2,
+# the rest row 0.
+H3_SEGMENTS = ((0, 100, 1), (100, 514, 2), (514, 37810, 0))
+
+
+def segment_index(rows: int, segments=H3_SEGMENTS) -> np.ndarray:
+    """(rows,) int32 table row per row; the ranges are scaled to `rows` when
+    rows differs from the layout's 37,810 (at least one row per range)."""
+    total = segments[-1][1]
+    idx = np.empty(rows, dtype=np.int32)
+    start = 0
+    for n, (lo, hi, g) in enumerate(segments):
+        end = rows if n == len(segments) - 1 else max(start + 1, min(rows, round(hi * rows / total)))
+        idx[start:end] = g
+        start = end
+    return idx
+
+
+def segmented(rows: int, dim: int, seed: int, nseg: int = 3, act_scale: float = 0.025,
+              eps: float = 1e-5) -> Workload:
+    """Segmented modulation: x N(0, 1); (nseg, dim) bf16 scale/shift tables
+    N(0, 0.1); the page's segment layout scaled to `rows`."""
+    x = normal(seed, 0, (rows, dim), 1.0)
+    return Workload("ada_layer_norm_quant_*_seg_bf16", rows, dim,
+                    {"x": bf16(x), "seg_idx": torch.from_numpy(segment_index(rows)),
+                     "seg_scale": bf16(normal(seed, 1, (nseg, dim), 0.1)),
+                     "seg_shift": bf16(normal(seed, 2, (nseg, dim), 0.1)),
+                     "act_scale": torch.tensor([act_scale], dtype=torch.float32)},
+                    {"eps": eps})
+
+
 def modulation6(batch: int, seq: int, dim: int, seed: int) -> Workload:
     return Workload("adaln_modulation6_bf16", batch * seq, dim,
                     {"params": torch.from_numpy(normal(seed, 0, (batch, seq, 6, dim), 1.0)),

@@ -137,9 +137,12 @@ def _bf16_neighbours(a: np.ndarray):
 
 
 def check_nvfp4(gpu_packed: np.ndarray, gpu_sf: np.ndarray, orc_packed: np.ndarray, orc_sf: np.ndarray,
-                rows: int, dim: int, v_orc: np.ndarray | None = None, what: str = "nvfp4") -> dict:
+                rows: int, dim: int, v_orc: np.ndarray | None = None, what: str = "nvfp4",
+                ts: float | None = None) -> dict:
     """Compare packed codes and the swizzled scale buffer.  v_orc: the oracle's
-    staged bf16 values (rows, dim) as float64, used to explain scale mismatches."""
+    staged bf16 values (rows, dim) as float64, used to explain scale mismatches.
+    ts: the tensor scale of the two-level contract (block scale
+    e4m3(min(fp32(fp32(amax / 6) / ts), 448))), None for single level."""
     nblk = dim // 16
     gcodes, ocodes = oracle.unpack_e2m1(gpu_packed), oracle.unpack_e2m1(orc_packed)
     st = check_codes(gcodes, ocodes, 0x8, what + " codes")
@@ -153,7 +156,13 @@ def check_nvfp4(gpu_packed: np.ndarray, gpu_sf: np.ndarray, orc_packed: np.ndarr
         assert v_orc is not None, f"{what}: {int(diff.sum())} scale bytes differ"
         amax = np.abs(v_orc).reshape(rows, nblk, 16).max(axis=2)
         lo, hi = _bf16_neighbours(amax)
-        enc = lambda a: torch.from_numpy((a / 6).astype(np.float32)).clamp(max=448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if ts is None:
+            enc = lambda a: torch.from_numpy((a / 6).astype(np.float32)).clamp(max=448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        else:
+            def enc(a):
+                q = ((a.astype(np.float32) / np.float32(6.0)).astype(np.float32) / np.float32(ts)).astype(np.float32)
+                q = np.where(np.isnan(q), np.float32(448.0), np.minimum(q, np.float32(448.0)))
+                return torch.from_numpy(q.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         ok = (gs == enc(lo)) | (gs == enc(hi))
         bad = diff & ~ok
         assert not bad.any(), f"{what}: scale bytes differ without an amax explanation at {np.argwhere(bad)[:5].tolist()}"

@@ -39,7 +39,7 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 15
+    assert len(declared) == 20
 
 
 def test_status_strings_and_version(lib):
@@ -136,6 +136,33 @@ def test_modfp8_and_awq_argument_errors(lib):
     assert n(A, A + 4, A, A, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_fp8 not 8-byte aligned
     assert n(A, A, A, A + 1, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_deq misaligned
     assert n(NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, NULL, 0, 64, NULL) == 0
+
+
+def test_seg_and_two_level_argument_errors(lib):
+    L, _ = lib
+    f = L.ada_layer_norm_quant_fp8_seg_bf16  # x, seg_idx, seg_scale, seg_shift, nseg, act, eps, out, rows, dim
+    assert f(A, A, A, A, 0, A, 1e-5, A, 4, 64, NULL) == 4          # no segments
+    assert f(A, NULL, A, A, 3, A, 1e-5, A, 4, 64, NULL) == 1       # null index
+    assert f(A, A, A, A + 8, 3, A, 1e-5, A, 4, 64, NULL) == 5      # shift table not 16-byte aligned
+    assert f(A, A + 2, A, A, 3, A, 1e-5, A, 4, 64, NULL) == 5      # index not 4-byte aligned
+    assert f(A, A, A, A, 3, A, 1e-5, A, 4, 60, NULL) == 3          # dim % 8
+    assert f(NULL, NULL, NULL, NULL, 0, NULL, 1e-5, NULL, 0, 64, NULL) == 0
+    g = L.ada_layer_norm_quant_nvfp4_swizzled_seg_bf16  # x, idx, s, h, nseg, eps, packed, sf, rows, dim
+    assert g(A, A, A, A, 3, 1e-5, A, A, 4, 40, NULL) == 3          # dim % 16
+    assert g(A, A, A, A, 3, 1e-5, A, NULL, 4, 64, NULL) == 1
+    n = L.layer_norm_no_affine_quant_nvfp4_2level_bf16  # x, eps, packed, sf, ts, ws, rows, dim
+    assert n(A, 1e-5, A, A, NULL, A, 4, 64, NULL) == 1             # null tensor scale
+    assert n(A, 1e-5, A, A, A, NULL, 4, 64, NULL) == 1             # null workspace
+    assert n(A, 1e-5, A, A, A + 2, A, 4, 64, NULL) == 5            # tensor scale misaligned
+    assert n(A, 1e-5, A, A, A, A + 1, 4, 64, NULL) == 5            # workspace misaligned
+    assert n(A, 1e-5, A, A, A, A, 4, 72, NULL) == 3
+    assert n(NULL, 1e-5, NULL, NULL, NULL, NULL, 0, 64, NULL) == 0
+    b = L.ada_layer_norm_quant_nvfp4_2level_bf16  # x, scale, shift, eps, packed, sf, ts, ws, rows, dim
+    assert b(A, NULL, A, 1e-5, A, A, A, A, 4, 64, NULL) == 1
+    assert b(A, A, A + 4, 1e-5, A, A, A, A, 4, 64, NULL) == 5
+    c = L.ada_layer_norm_quant_nvfp4_2level_seg_bf16  # x, idx, s, h, nseg, eps, packed, sf, ts, ws, rows, dim
+    assert c(A, A, A, A, -1, 1e-5, A, A, A, A, 4, 64, NULL) == 4
+    assert c(A, A, A, A, 2, float("nan"), A, A, A, A, 4, 64, NULL) == 7
 
 
 def test_modulation6_argument_errors(lib):

@@ -1,0 +1,172 @@
+"""GPU parity of the segmented and two-level NVFP4 producers (C ABI).
+
+Segmented modulation: row r takes row seg_idx[r] of (nseg, dim) tables
+(h3-blackwell-runtime compare page).  Two-level NVFP4 (same page,
+"Numerical Constraint" and the P1 checkpoint's numerical contract): global
+bf16 amax -> tensor scale ts = bf16(amax / 2688); block scales e4m3(min((amax_b
+/ 6) / ts, 448)); codes e2m1(v / (s * ts)).  Tolerance: tests/parity.py; the
+tensor scale must equal the oracle's exactly.  Cases: ragged rows (padding of
+the last scale tile), several dims (capped and uncapped kernels), the page's
+segment layout and random segment assignments, an all-zero tensor, a tensor
+whose maximum is 2688 (ts = 1), an out-of-range segment index (zero
+modulation for that row plus the device fault word), workspace reuse, a CUDA
+graph capture of the three operations.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import check_fp8, check_nvfp4
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (130, 4096), (5, 32768), (257, 1536)]
+
+
+def _u(t):
+    return synth.u16(t)
+
+
+def _seg_src(w):
+    return dict(seg_idx=w.inputs["seg_idx"].numpy(), seg_scale=_u(w.inputs["seg_scale"]),
+                seg_shift=_u(w.inputs["seg_shift"]))
+
+
+def _v(x, kind, **mod):
+    """The oracle's staged bf16 values as float64 (explains scale-byte mismatches)."""
+    return torch.from_numpy(oracle.staged(x, kind, **mod).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("rows,dim", [(1, 32), (40, 16), (127, 1536), (129, 3072), (300, 2048), (5, 32768),
+                                      (33, 6144)])
+def test_fp8_segmented(ap, dev, rows, dim):
+    w = synth.segmented(rows, dim, seed=rows + dim)
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    out = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
+                                               d["act_scale"])
+    ref = oracle.ln_quant_fp8(_u(w.inputs["x"]), 0.025, oracle.MOD_SEG, **_seg_src(w))
+    check_fp8(out.view(torch.uint8).cpu().numpy(), ref, 0.025, "fp8 seg")
+
+
+@pytest.mark.parametrize("rows,dim", SHAPES)
+def test_nvfp4_segmented(ap, dev, rows, dim):
+    w = synth.segmented(rows, dim, seed=3 * rows + dim)
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    pk, sf = ap.ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"])
+    x, src = _u(w.inputs["x"]), _seg_src(w)
+    opk, osf = oracle.ln_quant_nvfp4(x, oracle.MOD_SEG, **src)
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(x, oracle.MOD_SEG, **src), "nvfp4 seg")
+
+
+def _two_level(ap, dev, kind, w):
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    rows, dim = w.rows, w.dim
+    n = ap.swizzled_sf_size(rows, dim)
+    guard = 256
+    sfbuf = torch.full((n + 2 * guard,), 0xFF, dtype=torch.uint8, device=dev)
+    sf = sfbuf[guard:guard + n]
+    if kind == "none":
+        pk, _, ts = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(d["x"], sf_swizzled=sf)
+        mk, mod = oracle.MOD_NONE, {}
+    elif kind == "bcast":
+        pk, _, ts = ap.ada_layer_norm_quant_nvfp4_2level_bf16(d["x"], d["scale"], d["shift"], sf_swizzled=sf)
+        mk, mod = oracle.MOD_BCAST, dict(scale=_u(w.inputs["scale"]), shift=_u(w.inputs["shift"]))
+    else:
+        pk, _, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"],
+                                                                  d["seg_shift"], sf_swizzled=sf)
+        mk, mod = oracle.MOD_SEG, _seg_src(w)
+    sb = sfbuf.cpu().numpy()
+    assert np.all(sb[:guard] == 0xFF) and np.all(sb[-guard:] == 0xFF)
+    x = _u(w.inputs["x"])
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(x, mk, **mod)
+    return pk.cpu().numpy(), sb[guard:guard + n], float(ts.cpu()[0]), opk, osf, ots, _v(x, mk, **mod)
+
+
+@pytest.mark.parametrize("rows,dim", SHAPES)
+@pytest.mark.parametrize("kind", ["none", "bcast", "seg"])
+def test_nvfp4_two_level(ap, dev, kind, rows, dim):
+    seed = 5 * rows + dim
+    w = synth.segmented(rows, dim, seed) if kind == "seg" else \
+        (synth.nvfp4_broadcast(rows, dim, seed) if kind == "bcast" else synth.nvfp4_ln(rows, dim, seed))
+    gpk, gsf, gts, opk, osf, ots, v = _two_level(ap, dev, kind, w)
+    assert gts == ots, (gts, ots)
+    check_nvfp4(gpk, gsf, opk, osf, rows, dim, v, f"two-level {kind}", ts=ots)
+
+
+def test_two_level_zero_tensor(ap, dev):
+    rows, dim = 130, 96
+    x = torch.zeros((rows, dim), dtype=torch.bfloat16, device=dev)
+    pk, sf, ts = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x)
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(np.zeros((rows, dim), dtype=np.uint16))
+    assert float(ts.cpu()[0]) == ots == 0.0
+    assert np.array_equal(pk.cpu().numpy(), opk) and np.array_equal(sf.cpu().numpy(), osf)
+
+
+def test_two_level_tensor_scale_one(ap, dev):
+    # shift 2688 in one column with scale 0 there: the global maximum is 2688, ts = 1
+    rng = np.random.default_rng(8)
+    rows, dim = 77, 3072
+    x = synth.bf16(rng.standard_normal((rows, dim)).astype(np.float32))
+    sc = rng.normal(0, 0.1, dim).astype(np.float32)
+    sh = rng.normal(0, 0.1, dim).astype(np.float32)
+    sc[7], sh[7] = 0.0, 2688.0
+    scale, shift = synth.bf16(sc), synth.bf16(sh)
+    pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_bf16(x.to(dev), scale.to(dev), shift.to(dev))
+    mod = dict(scale=_u(scale), shift=_u(shift))
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(_u(x), oracle.MOD_BCAST, **mod)
+    assert ots == 1.0 and float(ts.cpu()[0]) == 1.0
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(_u(x), oracle.MOD_BCAST, **mod),
+                "two-level ts=1", ts=1.0)
+
+
+def test_out_of_range_segment_index(ap, dev):
+    import nvfp4_activation_producer_gb300 as m
+    assert m._load().nvfp4ap_take_device_fault() == 0
+    w = synth.segmented(64, 1536, seed=9)
+    idx = w.inputs["seg_idx"].clone()
+    idx[5], idx[40] = 3, -1                      # nseg = 3: both out of range
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    out = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], idx.to(dev), d["seg_scale"], d["seg_shift"], d["act_scale"])
+    assert m._load().nvfp4ap_take_device_fault() == m.ERR_FAULT
+    assert m._load().nvfp4ap_take_device_fault() == 0          # read and cleared
+    # the two rows carry no modulation; the others the oracle's segmented output
+    x = _u(w.inputs["x"])
+    got = out.view(torch.uint8).cpu().numpy()
+    plain = oracle.ln_quant_fp8(x, 0.025, oracle.MOD_NONE)
+    check_fp8(got[[5, 40]], plain[[5, 40]], 0.025, "zero modulation rows")
+    keep = np.setdiff1d(np.arange(64), [5, 40])
+    src = _seg_src(w)
+    src["seg_idx"] = src["seg_idx"][keep]
+    check_fp8(got[keep], oracle.ln_quant_fp8(x[keep], 0.025, oracle.MOD_SEG, **src), 0.025, "valid rows")
+
+
+def test_two_level_workspace_reuse_and_graph(ap, dev):
+    w = synth.segmented(515, 5376, seed=11)
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    rows, dim = w.rows, w.dim
+    ws = torch.zeros(8, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(2):
+        outs.append(ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"],
+                                                                  d["seg_shift"], workspace=ws))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    pk = torch.empty((rows, dim // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((ap.swizzled_sf_size(rows, dim),), dtype=torch.uint8, device=dev)
+    ts = torch.empty((1,), dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(dev)
+    with torch.cuda.stream(st):
+        ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
+                                                      packed=pk, sf_swizzled=sf, tensor_scale=ts, workspace=ws)
+        st.synchronize()
+        pk.zero_(); sf.zero_(); ts.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
+                                                          packed=pk, sf_swizzled=sf, tensor_scale=ts, workspace=ws)
+        g.replay()
+        g.replay()
+    st.synchronize()
+    assert torch.equal(pk, outs[0][0]) and torch.equal(sf, outs[0][1]) and torch.equal(ts, outs[0][2])

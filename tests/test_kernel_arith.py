@@ -12,6 +12,10 @@ every case that can matter, and compare with exact rational arithmetic:
    rounds to the same e2m1 code as the exact v/s, for every e4m3 scale s, at
    every midpoint (ties) and on bf16 values around them.
 
+4. the same quotient for the two-level contract, whose divisor is s * ts with
+   ts a bf16 tensor scale (up to 12 significant bits): every pair of e4m3 and
+   bf16 mantissas, at every tie and its bf16 neighbours.
+
 And one decode the modfp8 kernels use:
 
 3. e4m3 decode by moving the byte's sign to bit 31 and its exponent/mantissa
@@ -104,3 +108,44 @@ def test_e4m3_field_move_decode_is_exact():
     assert np.array_equal(decoded.view(np.uint32), ref.view(np.uint32))  # signs of zero included
     # the smallest subnormal 2^-9 and the largest normal 448 are among them
     assert decoded[codes == 0x01][0] == 2.0**-9 and decoded[codes == 0x7E][0] == 448.0
+
+
+def test_two_level_quotient_is_exact_for_every_divisor_mantissa():
+    # divisor D = s * ts: e4m3 mantissas 1 + k/8 times bf16 mantissas 1 + m/128
+    # (exponents only shift D and v together); exact codes from float64
+    # comparisons of |v| with mid * D (exact: at most 3 + 12 + 8 bits)
+    sm = np.arange(8, 16, dtype=np.float64) / 8
+    tm = np.arange(128, 256, dtype=np.float64) / 128
+    D = np.unique((sm[:, None] * tm[None, :]).reshape(-1))
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    upper_even = np.array([False, True, False, True, False, True, False])  # upper neighbour's code is even
+
+    def exact_code(v, d):
+        a = np.abs(v)[:, None]
+        th = mids[None, :] * d[:, None]
+        up = (a > th) | ((a == th) & upper_even[None, :])
+        return up.sum(axis=1)
+
+    for ulps in (-2, -1, 0, 1, 2):
+        d32 = D.astype(np.float32)
+        assert np.array_equal(d32.astype(np.float64), D)          # exact in fp32
+        rh = (F32(1.0) / d32).astype(np.float32)
+        for _ in range(abs(ulps)):
+            rh = np.nextafter(rh, F32(np.inf if ulps > 0 else -np.inf), dtype=np.float32)
+        rl = (rh * _fma32(-d32, rh, np.ones_like(d32))).astype(np.float32)
+        # candidate v: the bf16 values nearest mid * D and their neighbours
+        tie = (mids[None, :] * D[:, None]).reshape(-1)
+        dd = np.repeat(D, len(mids)).astype(np.float64)
+        bits = torch.from_numpy(tie.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().astype(np.int64)
+        vs, ds, rhs, rls = [], [], [], []
+        for k in (-1, 0, 1):
+            b = torch.from_numpy((bits + k).astype(np.int16)).view(torch.bfloat16).double().numpy()
+            vs.append(b); ds.append(dd)
+            rhs.append(np.repeat(rh, len(mids))); rls.append(np.repeat(rl, len(mids)))
+        v = np.concatenate(vs); v = np.concatenate([v, -v])
+        d = np.concatenate(ds * 2)
+        r_h = np.concatenate(rhs * 2); r_l = np.concatenate(rls * 2)
+        v32 = v.astype(np.float32)
+        assert np.array_equal(v32.astype(np.float64), v)
+        q = _fma32(v32, r_h, (v32 * r_l).astype(np.float32))
+        assert np.array_equal(_code_rne32(q), exact_code(v, d)), ulps
