@@ -74,6 +74,9 @@ def extra_workloads():
         ("fp8_modfp8", synth.fp8_modfp8(4096, 3072, 2006)),
         ("fp8_awq", synth.fp8_awq(4096, 3072, 2007)),
         ("nvfp4_modfp8", synth.nvfp4_modfp8(5070, 3072, 2008)),
+        ("fp8_seg_h3", synth.segmented(37810, 5376, 2010)),
+        ("nvfp4_2level_seg_h3", synth.segmented(37810, 5376, 2011)),
+        ("nvfp4_2level_layer_norm", synth.nvfp4_ln(5070, 3072, 2012)),
     ]
 
 
@@ -87,6 +90,17 @@ def alg_bytes(name: str, w) -> int:
         return 2 * R * D + 2 * D + 8 + R * D + 4          # e4m3 vectors, two deq scalars
     if name == "fp8_awq":
         return 2 * R * D + 6 * D + R * D + 4              # scale, shift, inv_s
+    if name == "fp8_seg_h3":
+        nseg = w.inputs["seg_scale"].shape[0]
+        return 2 * R * D + 4 * R + 4 * nseg * D + R * D + 4   # x, segment index, tables, codes
+    if name in ("nvfp4_2level_seg_h3", "nvfp4_2level_layer_norm"):
+        # two passes over the input (no block can be encoded before the whole
+        # tensor's maximum is known), then codes, scales and the tensor scale
+        sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
+        src = 0
+        if name == "nvfp4_2level_seg_h3":
+            src = 4 * R + 4 * w.inputs["seg_scale"].shape[0] * D
+        return 2 * (2 * R * D + src) + R * D // 2 + sf + 4
     if name == "fp8_layer_norm":
         return 2 * R * D + R * D + 4
     if name == "fp8_per_token":
@@ -111,6 +125,11 @@ class DeviceOp:
         R, D = w.rows, w.dim
         if name.startswith("fp8"):
             self.out = (torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev),)
+        elif name.startswith("nvfp4_2level"):
+            self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
+                        torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev),
+                        torch.empty((1,), dtype=torch.float32, device=dev),
+                        torch.zeros((ap.WORKSPACE_2LEVEL_BYTES,), dtype=torch.uint8, device=dev))
         elif name.startswith("nvfp4"):
             self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
                         torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev))
@@ -146,6 +165,16 @@ class DeviceOp:
             ap.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(d["x"], d["scale_fp8"], d["shift_fp8"],
                                                                d["scale_deq"], d["shift_deq"], p["eps"],
                                                                packed=o[0], sf_swizzled=o[1])
+        elif n == "fp8_seg_h3":
+            ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
+                                                 d["act_scale"], p["eps"], out=o[0])
+        elif n == "nvfp4_2level_seg_h3":
+            ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
+                                                          p["eps"], packed=o[0], sf_swizzled=o[1], tensor_scale=o[2],
+                                                          workspace=o[3])
+        elif n == "nvfp4_2level_layer_norm":
+            ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(d["x"], p["eps"], packed=o[0], sf_swizzled=o[1],
+                                                            tensor_scale=o[2], workspace=o[3])
         elif n == "modulation6":
             ap.adaln_modulation6_bf16(d["params"], d["modulation"], out=o[0])
 
@@ -188,6 +217,18 @@ class DeviceOp:
                                                                         P(d["shift_fp8"]), P(d["scale_deq"]),
                                                                         P(d["shift_deq"]), p["eps"], P(o[0]), P(o[1]),
                                                                         R, D, stream)
+        elif n == "fp8_seg_h3":
+            fn, a = L.ada_layer_norm_quant_fp8_seg_bf16, (P(d["x"]), P(d["seg_idx"]), P(d["seg_scale"]),
+                                                          P(d["seg_shift"]), d["seg_scale"].shape[0], P(d["act_scale"]),
+                                                          p["eps"], P(o[0]), R, D, stream)
+        elif n == "nvfp4_2level_seg_h3":
+            fn, a = L.ada_layer_norm_quant_nvfp4_2level_seg_bf16, (P(d["x"]), P(d["seg_idx"]), P(d["seg_scale"]),
+                                                                   P(d["seg_shift"]), d["seg_scale"].shape[0],
+                                                                   p["eps"], P(o[0]), P(o[1]), P(o[2]), P(o[3]),
+                                                                   R, D, stream)
+        elif n == "nvfp4_2level_layer_norm":
+            fn, a = L.layer_norm_no_affine_quant_nvfp4_2level_bf16, (P(d["x"]), p["eps"], P(o[0]), P(o[1]), P(o[2]),
+                                                                     P(o[3]), R, D, stream)
         else:
             self._outs6 = (ctypes.c_void_p * 6)(*[o[0][i].data_ptr() for i in range(6)])
             fn, a = L.adaln_modulation6_bf16, (P(d["params"]), P(d["modulation"]), self._outs6, 1, R, D, stream)
@@ -634,6 +675,15 @@ def oracle_sample_step(works, frac_rows: int, nthreads: int):
         elif name == "fp8_awq":
             oracle.ln_quant_fp8(x, 0.025, oracle.MOD_AWQ, eps, nthreads, scale=synth.u16(w.inputs["scale"]),
                                 shift=synth.u16(w.inputs["shift"]), inv_s=synth.u16(w.inputs["inv_s"]))
+        elif name in ("fp8_seg_h3", "nvfp4_2level_seg_h3"):
+            src = dict(seg_idx=w.inputs["seg_idx"][:n].numpy(), seg_scale=synth.u16(w.inputs["seg_scale"]),
+                       seg_shift=synth.u16(w.inputs["seg_shift"]))
+            if name == "fp8_seg_h3":
+                oracle.ln_quant_fp8(x, 0.025, oracle.MOD_SEG, eps, nthreads, **src)
+            else:
+                oracle.ln_quant_nvfp4_2level(x, oracle.MOD_SEG, eps, nthreads, **src)
+        elif name == "nvfp4_2level_layer_norm":
+            oracle.ln_quant_nvfp4_2level(x, oracle.MOD_NONE, eps, nthreads)
         elif name == "modulation6":
             oracle.adaln_modulation6(w.inputs["params"][:, :n].numpy(), w.inputs["modulation"].numpy(), nthreads)
         sub = synth.Workload(w.op, n, w.dim)

@@ -259,7 +259,7 @@ int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* s
  * aligned) -- the dequantised value is e2m1 * decode(s) * ts.
  * workspace: caller-owned device memory of NVFP4AP_2LEVEL_WORKSPACE_BYTES,
  * 4-byte aligned, cleared and used by the call (two calls on concurrent
- * streams need two workspaces).  Three operations on `stream`: a clear of the
+ * streams need two workspaces).  Three kernels on `stream`: a clear of the
  * workspace, the maximum pass, the quantising pass (graph-capturable). */
 int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed, void* sf_swizzled,
                                                  float* tensor_scale, void* workspace, int64_t rows, int64_t dim,

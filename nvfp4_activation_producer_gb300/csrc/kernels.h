@@ -129,7 +129,7 @@ cudaError_t take_tma_fault(unsigned int* fault);
 // Segmented modulation (MOD_SEG) on the register row kernels: FP8 (dim % 8
 // == 0, 16-byte aligned inputs) or single-level NVFP4.
 cudaError_t launch_ln_seg(const LnArgs& a, bool nvfp4, RowShape s, cudaStream_t st);
-// Two-level NVFP4: clears a.amax_ws, runs the maximum pass, then the
+// Two-level NVFP4: clears a.amax_ws (a kernel), runs the maximum pass, then the
 // quantising pass (writes packed, sf and *a.tensor_scale); mod MOD_NONE,
 // MOD_BCAST or MOD_SEG.  `full`: rows exactly fill tpr * per_thread chunks
 // (tpr <= 128) -- the register-capped instances.

@@ -309,13 +309,17 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
       amax[k] = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
     }
     if constexpr (KIND == KIND_AMAX) {
-      // first pass of the two-level contract: the tensor's largest |v|
+      // first pass of the two-level contract: the tensor's largest |v|.  One
+      // value per warp, and the atomic only when it beats the word's current
+      // value (read through L2): same-address atomics serialise in L2, and
+      // after the first rows almost none are needed.  No barrier here: rows
+      // past the end of the tensor have already returned.
       float m = amax[0];
 #pragma unroll
       for (int k = 1; k < NV; ++k) m = fmaxf(m, amax[k]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      if (lane == 0) atomicMax(a.amax_ws, __float_as_uint(m));
+      if (lane == 0 && m > __uint_as_float(__ldcg(a.amax_ws))) atomicMax(a.amax_ws, __float_as_uint(m));
       return;
     }
 #pragma unroll

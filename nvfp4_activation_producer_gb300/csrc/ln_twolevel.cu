@@ -12,10 +12,9 @@
 // is known -- so two launches): the maximum pass writes the tensor's largest
 // |v| to a caller-owned device word, the quantising pass derives the tensor
 // scale from it and writes codes, block scales and the tensor scale.  The
-// word is cleared on the stream first.  The maximum pass is launched without
-// programmatic serialisation, so it starts only after the clear; the
-// quantising pass may overlap its ramp with the maximum pass's tail and waits
-// (griddepcontrol.wait) before reading the word.
+// word is cleared first by a one-thread kernel.  All three launches use
+// programmatic serialisation: each may start while the previous drains, and
+// each waits (griddepcontrol.wait) before it touches the word.
 #include "ln_rows.cuh"
 
 namespace nvfp4ap {
@@ -40,51 +39,24 @@ cudaError_t launch_full(const LnArgs& a, RowShape s, bool pdl, cudaStream_t st) 
   }
 }
 
-// the maximum pass without programmatic serialisation (it must follow the clear)
-template <int MOD>
-cudaError_t launch_amax_plain(const LnArgs& a, RowShape s, cudaStream_t st) {
-  const dim3 block(s.tpr, s.rpc), grid((unsigned)((a.rows + s.rpc - 1) / s.rpc));
-  const float inv_d = (float)(1.0 / (double)a.dim);
-  constexpr bool kPerToken = false;  // the two-level sources (none, broadcast, segmented) keep no rows in registers
-#define NVFP4AP_CASE(N)                                              \
-  case N:                                                            \
-    ln_rows_kernel<KIND_AMAX, MOD, N><<<grid, block, 0, st>>>(a, inv_d); \
-    return cudaGetLastError();
-  if constexpr (kPerToken) {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(1)
-      NVFP4AP_CASE(2)
-      NVFP4AP_CASE(3)
-      NVFP4AP_CASE(4)
-      NVFP4AP_CASE(6)
-      default: return cudaErrorInvalidValue;
-    }
-  } else {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(1)
-      NVFP4AP_CASE(2)
-      NVFP4AP_CASE(3)
-      NVFP4AP_CASE(4)
-      NVFP4AP_CASE(6)
-      NVFP4AP_CASE(8)
-      NVFP4AP_CASE(12)
-      default: return cudaErrorInvalidValue;
-    }
-  }
-#undef NVFP4AP_CASE
+// Clears the maximum word: waits for the previous kernel on the stream (which
+// may still read the word) before writing it.
+__global__ void clear_word_kernel(unsigned int* w) {
+  pdl_enter();
+  *w = 0u;
 }
 
 template <int MOD>
 cudaError_t run_2level(const LnArgs& a, RowShape s, bool full, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(a.amax_ws, 0, sizeof(unsigned int), st);
+  cudaError_t e = launch_maybe_pdl(clear_word_kernel, dim3(1), dim3(1), 0, st, a.amax_ws);
   if (e != cudaSuccess) return e;
   if constexpr (MOD == MOD_NONE) {  // the modulated forms spill at the capped register count
     if (full) {
-      e = launch_full<KIND_AMAX, MOD>(a, s, false, st);
+      e = launch_full<KIND_AMAX, MOD>(a, s, true, st);
       return e != cudaSuccess ? e : launch_full<KIND_NV2L, MOD>(a, s, true, st);
     }
   }
-  e = launch_amax_plain<MOD>(a, s, st);
+  e = launch_nv<KIND_AMAX, MOD>(a, s, st);
   return e != cudaSuccess ? e : launch_nv<KIND_NV2L, MOD>(a, s, st);
 }
 
