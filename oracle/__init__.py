@@ -98,6 +98,10 @@ def lib() -> ctypes.CDLL:
         L.orc_ln_quant_nvfp4_2level.restype = i32
         L.orc_ln_quant_nvfp4_2level.argtypes = [p, ctypes.POINTER(_Mod), f32, p, p,
                                                 ctypes.POINTER(ctypes.c_float), i64, i64, i32]
+        L.orc_swiglu_values.restype = i32
+        L.orc_swiglu_values.argtypes = [p, p, i64, p, i64, i64, i32]
+        L.orc_swiglu_quant_nvfp4_2level.restype = i32
+        L.orc_swiglu_quant_nvfp4_2level.argtypes = [p, p, i64, p, p, ctypes.POINTER(ctypes.c_float), i64, i64, i32]
         L.orc_adaln_modulation6.restype = i32
         L.orc_adaln_modulation6.argtypes = [p, p, p, i64, i64, i32]
         _lib = L
@@ -296,6 +300,32 @@ def ln_quant_nvfp4_2level(x, kind=MOD_NONE, eps=1e-5, nthreads=None, **mod):
     ts = ctypes.c_float()
     _check(lib().orc_ln_quant_nvfp4_2level(x.ctypes.data, ctypes.byref(m), eps, packed.ctypes.data, sf.ctypes.data,
                                            ctypes.byref(ts), rows, dim, nthreads or default_threads()))
+    return packed, sf, ts.value
+
+
+def swiglu_values(gate, up, nthreads=None) -> np.ndarray:
+    """bf16 bits (rows, dim) of v = bf16(bf16(silu(gate)) * up); gate, up bf16 bits (rows, dim)."""
+    gate = np.ascontiguousarray(gate, dtype=np.uint16)
+    up = np.ascontiguousarray(up, dtype=np.uint16)
+    rows, dim = gate.shape
+    assert up.shape == gate.shape
+    v = np.empty((rows, dim), dtype=np.uint16)
+    _check(lib().orc_swiglu_values(gate.ctypes.data, up.ctypes.data, dim, v.ctypes.data, rows, dim,
+                                   nthreads or default_threads()))
+    return v
+
+
+def swiglu_quant_nvfp4_2level(gate, up, nthreads=None):
+    """SwiGLU producer, two-level NVFP4: (packed, swizzled scales, tensor scale)."""
+    gate = np.ascontiguousarray(gate, dtype=np.uint16)
+    up = np.ascontiguousarray(up, dtype=np.uint16)
+    rows, dim = gate.shape
+    packed = np.empty((rows, dim // 2), dtype=np.uint8)
+    sf = np.empty(max(swizzled_sf_size(rows, dim), 0), dtype=np.uint8)
+    ts = ctypes.c_float()
+    _check(lib().orc_swiglu_quant_nvfp4_2level(gate.ctypes.data, up.ctypes.data, dim, packed.ctypes.data,
+                                               sf.ctypes.data, ctypes.byref(ts), rows, dim,
+                                               nthreads or default_threads()))
     return packed, sf, ts.value
 
 

@@ -50,6 +50,7 @@
  *   R17-R19 two-level NVFP4: see orc_nvfp4_2level.
  *   R20 segmented modulation: row r uses row seg_idx[r] of (nseg, dim) bf16
  *      scale/shift tables, with the broadcast producers' arithmetic.
+ *   R21 SwiGLU: see orc_swiglu_values.
  */
 #include "orc.h"
 
@@ -490,6 +491,50 @@ int orc_ln_quant_nvfp4_2level(const uint16_t* x, const orc_mod_t* mod, float eps
   uint16_t* v = (uint16_t*)malloc((size_t)(rows * dim + 1) * sizeof(uint16_t));
   if (!v) return -2;
   int rc = orc_ln_staged_bf16(x, mod, eps, v, rows, dim, nthreads);
+  if (rc == 0) rc = orc_nvfp4_2level(v, rows, dim, packed, sf_swizzled, tensor_scale, nthreads);
+  free(v);
+  return rc;
+}
+
+/* ---- SwiGLU producer (h3-blackwell-runtime compare page:
+ * NVFP4_SWIGLU_FUSION_DESIGN.md -- the two bf16 boundaries: silu(gate)
+ * rounded to bf16, then that bf16 value times bf16 up rounded to bf16; then the
+ * tensor scale, e4m3 block scales and e2m1 codes of the two-level contract).
+ * Reading R21: silu(g) = g / (1 + exp(-g)) in double, rounded to binary32 and
+ * then to bf16 (R7: the value is first rounded to the precision in which the
+ * GPU takes the decision); the product of two bf16 values is exact in double
+ * and in binary32, then rounded to bf16. ------------------------------------ */
+typedef struct {
+  const uint16_t* gate; const uint16_t* up; int64_t ld, dim; uint16_t* v;
+} sw_ctx;
+
+static void row_swiglu(void* p, int64_t r, double* scratch) {
+  sw_ctx* c = (sw_ctx*)p;
+  (void)scratch;
+  for (int64_t d = 0; d < c->dim; ++d) {
+    const double g = orc_bf16_to_f64(c->gate[r * c->ld + d]);
+    const double u = orc_bf16_to_f64(c->up[r * c->ld + d]);
+    const double silu = g / (1.0 + exp(-g));
+    const double s = orc_bf16_to_f64(orc_bf16_from_f32((float)silu));
+    c->v[r * c->dim + d] = orc_bf16_from_f32((float)(s * u));
+  }
+}
+
+int orc_swiglu_values(const uint16_t* gate, const uint16_t* up, int64_t ld, uint16_t* v,
+                      int64_t rows, int64_t dim, int nthreads) {
+  if (rows < 0 || dim <= 0 || ld < dim) return -1;
+  sw_ctx c = {gate, up, ld, dim, v};
+  for_rows(row_swiglu, &c, rows, dim, nthreads);
+  return 0;
+}
+
+int orc_swiglu_quant_nvfp4_2level(const uint16_t* gate, const uint16_t* up, int64_t ld, uint8_t* packed,
+                                  uint8_t* sf_swizzled, float* tensor_scale, int64_t rows, int64_t dim,
+                                  int nthreads) {
+  if (rows < 0 || dim <= 0 || dim % 16 != 0 || ld < dim) return -1;
+  uint16_t* v = (uint16_t*)malloc((size_t)(rows * dim + 1) * sizeof(uint16_t));
+  if (!v) return -2;
+  int rc = orc_swiglu_values(gate, up, ld, v, rows, dim, nthreads);
   if (rc == 0) rc = orc_nvfp4_2level(v, rows, dim, packed, sf_swizzled, tensor_scale, nthreads);
   free(v);
   return rc;

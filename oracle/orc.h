@@ -102,6 +102,16 @@ int orc_ln_quant_nvfp4_2level(const uint16_t* x, const orc_mod_t* mod, float eps
                               uint8_t* sf_swizzled, float* tensor_scale, int64_t rows, int64_t dim,
                               int nthreads);
 
+/* SwiGLU values v = bf16(bf16(silu(gate)) * up) for (rows, dim) with row
+ * stride ld (elements) for both inputs; v is (rows, dim) contiguous. */
+int orc_swiglu_values(const uint16_t* gate, const uint16_t* up, int64_t ld, uint16_t* v,
+                      int64_t rows, int64_t dim, int nthreads);
+
+/* SwiGLU producer with the two-level NVFP4 output. */
+int orc_swiglu_quant_nvfp4_2level(const uint16_t* gate, const uint16_t* up, int64_t ld, uint8_t* packed,
+                                  uint8_t* sf_swizzled, float* tensor_scale, int64_t rows, int64_t dim,
+                                  int nthreads);
+
 /* six-way: out is (6, batch*seq, dim) bf16 bits; params (batch*seq, 6, dim). */
 int orc_adaln_modulation6(const float* params, const float* modulation, uint16_t* out,
                           int64_t tokens, int64_t dim, int nthreads);

@@ -151,3 +151,49 @@ def test_block_scale_division_order_does_not_change_bytes():
     printed = e4(((A / np.float32(6.0)).astype(np.float32) / T).astype(np.float32))
     reverse = e4(((A / T).astype(np.float32) / np.float32(6.0)).astype(np.float32))
     assert np.array_equal(printed[keep], reverse[keep])
+
+
+# ------------------------------------------------------------------ SwiGLU --
+
+def _silu_bf16_torch(g_bits):
+    # torch's float64 silu, rounded to binary32 and then to bf16
+    g = torch.from_numpy(_f64(g_bits))
+    return torch.nn.functional.silu(g).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_swiglu_silu_boundary_matches_torch(orc):
+    # with up = 1 the product is exact, so v is the bf16 silu value itself
+    rng = np.random.default_rng(12)
+    g = _u16((rng.standard_normal((40, 64)) * 4).astype(np.float32))
+    one = _u16(np.ones((40, 64), dtype=np.float32))
+    assert np.array_equal(orc.swiglu_values(g, one), _silu_bf16_torch(g))
+
+
+def test_swiglu_product_boundary_matches_torch(orc):
+    rng = np.random.default_rng(13)
+    g = _u16((rng.standard_normal((30, 48)) * 3).astype(np.float32))
+    u = _u16((rng.standard_normal((30, 48)) * 2).astype(np.float32))
+    s = torch.from_numpy(_silu_bf16_torch(g).view(np.int16)).view(torch.bfloat16).double()
+    ref = (s * torch.from_numpy(_f64(u))).float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.swiglu_values(g, u), ref)
+    # power-of-two up scales the bf16 silu exactly
+    two = _u16(np.full((30, 48), 0.25, dtype=np.float32))
+    assert np.array_equal(_f64(orc.swiglu_values(g, two)), _f64(_silu_bf16_torch(g)) * 0.25)
+
+
+def test_swiglu_closed_forms(orc):
+    # silu(0) = 0 (sign kept: 0 / 1), silu(-inf-like) -> -0-side tiny values, silu(large) = large
+    g = _u16(np.array([[0.0, -0.0, 64.0, 1.0]], dtype=np.float32))
+    u = _u16(np.ones((1, 4), dtype=np.float32))
+    v = _f64(orc.swiglu_values(g, u))[0]
+    assert v[0] == 0.0 and v[2] == 64.0
+    assert np.float32(v[3]) == torch.tensor(1.0 / (1.0 + np.exp(-1.0))).float().to(torch.bfloat16).float().item()
+
+
+def test_swiglu_two_level_is_the_quantiser_of_its_values(orc):
+    rng = np.random.default_rng(14)
+    g = _u16((rng.standard_normal((70, 96)) * 2).astype(np.float32))
+    u = _u16(rng.standard_normal((70, 96)).astype(np.float32))
+    p1, s1, t1 = orc.swiglu_quant_nvfp4_2level(g, u)
+    p2, s2, t2 = orc.nvfp4_2level(orc.swiglu_values(g, u))
+    assert np.array_equal(p1, p2) and np.array_equal(s1, s2) and t1 == t2
