@@ -274,6 +274,26 @@ int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, const int32_t* seg
                                                void* sf_swizzled, float* tensor_scale, void* workspace,
                                                int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
+/* SwiGLU -> two-level NVFP4 (h3-blackwell-runtime compare page,
+ * NVFP4_SWIGLU_FUSION_DESIGN.md: both bf16 boundaries kept):
+ *   v = bf16(bf16(silu(gate)) * up),  silu(g) = g / (1 + exp(-g)),
+ * the silu boundary taken on the binary32 value of silu (the library
+ * recomputes in double the few elements its fast path cannot decide), then
+ * the two-level contract above on v (no LayerNorm).  gate, up: device
+ * (rows, dim) bf16 with the common row stride ld (elements): two tensors, or
+ * the halves of one (rows, 2*dim) tensor (up = gate + dim, ld = 2*dim).  dim %
+ * 16 == 0, ld >= dim and ld % 8 == 0 (NVFP4AP_ERR_DIM / _SHAPE), gate and up
+ * 16-byte aligned.  Outputs and workspace as for the two-level producers. */
+int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* up, int64_t ld, void* packed, void* sf_swizzled,
+                                   float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
+                                   nvfp4ap_stream_t stream);
+
+/* The SwiGLU values of swiglu_quant_nvfp4_2level_bf16 themselves:
+ * out (rows, dim) bf16 contiguous, v = bf16(bf16(silu(gate)) * up) -- the
+ * materialised form.  dim % 8 == 0, gate/up/out 16-byte aligned, ld as above. */
+int swiglu_bf16(const void* gate, const void* up, int64_t ld, void* out, int64_t rows, int64_t dim,
+                nvfp4ap_stream_t stream);
+
 /* README "Available Functions" / "Tensor Contract": swizzled_sf_size.
  * Bytes of the swizzled scale buffer: ceil(rows/128)*128 * ceil(dim/16/4)*4.
  * Returns -1 when rows < 0, dim <= 0 or dim % 16 != 0.  Host only. */

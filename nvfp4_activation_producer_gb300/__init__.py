@@ -31,6 +31,8 @@ __all__ = [
     "layer_norm_no_affine_quant_nvfp4_2level_bf16",
     "ada_layer_norm_quant_nvfp4_2level_bf16",
     "ada_layer_norm_quant_nvfp4_2level_seg_bf16",
+    "swiglu_quant_nvfp4_2level_bf16",
+    "swiglu_bf16",
     "WORKSPACE_2LEVEL_BYTES",
     "layer_norm_no_affine_quant_nvfp4_swizzled_bf16",
     "adaln_modulation6_bf16",
@@ -97,6 +99,10 @@ def _load() -> ctypes.CDLL:
     L.ada_layer_norm_quant_nvfp4_2level_bf16.argtypes = [p, p, p, f32, p, p, p, p, i64, i64, p]
     L.ada_layer_norm_quant_nvfp4_2level_seg_bf16.restype = i32
     L.ada_layer_norm_quant_nvfp4_2level_seg_bf16.argtypes = [p, p, p, p, i64, f32, p, p, p, p, i64, i64, p]
+    L.swiglu_bf16.restype = i32
+    L.swiglu_bf16.argtypes = [p, p, i64, p, i64, i64, p]
+    L.swiglu_quant_nvfp4_2level_bf16.restype = i32
+    L.swiglu_quant_nvfp4_2level_bf16.argtypes = [p, p, i64, p, p, p, p, i64, i64, p]
     L.layer_norm_no_affine_quant_fp8_static_bf16.restype = i32
     L.layer_norm_no_affine_quant_fp8_static_bf16.argtypes = [p, p, f32, p, i64, i64, p]
     L.ada_layer_norm_quant_nvfp4_swizzled_bf16.restype = i32
@@ -430,6 +436,45 @@ def ada_layer_norm_quant_nvfp4_2level_seg_bf16(x, seg_idx, seg_scale, seg_shift,
                                                             _ptr(sf_swizzled), _ptr(tensor_scale), _ptr(workspace),
                                                             rows, dim, _stream(dev))
     _raise("ada_layer_norm_quant_nvfp4_2level_seg_bf16", rc)
+    return packed, sf_swizzled, tensor_scale
+
+
+def _gate_up(gate, up):
+    for name, t in (("gate", gate), ("up", up)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 2 or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a 2-D CUDA bfloat16 tensor")
+    if gate.shape != up.shape or gate.device != up.device:
+        raise ValueError("gate and up must have the same shape and device")
+    rows, dim = gate.shape
+    if gate.stride(1) != 1 or up.stride(1) != 1 or gate.stride(0) != up.stride(0):
+        raise ValueError("gate and up must have unit column stride and the same row stride")
+    return rows, dim, (gate.stride(0) if rows > 1 else dim), gate.device
+
+
+def swiglu_bf16(gate, up, out=None):
+    """bf16(bf16(silu(gate)) * up), (rows, dim) bf16 (the materialised SwiGLU values)."""
+    rows, dim, ld, dev = _gate_up(gate, up)
+    if out is None:
+        out = torch.empty((rows, dim), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", torch.bfloat16, (rows, dim), dev)
+    rc = _load().swiglu_bf16(_ptr(gate), _ptr(up), ld, _ptr(out), rows, dim, _stream(dev))
+    _raise("swiglu_bf16", rc)
+    return out
+
+
+def swiglu_quant_nvfp4_2level_bf16(gate, up, packed=None, sf_swizzled=None, tensor_scale=None, workspace=None):
+    """bf16(bf16(silu(gate)) * up) -> two-level NVFP4: (packed, sf_swizzled, tensor_scale).
+
+    gate and up are (rows, dim) bf16 views with the same row stride: two
+    contiguous tensors, or the two halves x[:, :dim], x[:, dim:] of one
+    contiguous (rows, 2*dim) tensor."""
+    rows, dim, ld, dev = _gate_up(gate, up)
+    packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    rc = _load().swiglu_quant_nvfp4_2level_bf16(_ptr(gate), _ptr(up), ld, _ptr(packed), _ptr(sf_swizzled),
+                                                _ptr(tensor_scale), _ptr(workspace), rows, dim, _stream(dev))
+    _raise("swiglu_quant_nvfp4_2level_bf16", rc)
     return packed, sf_swizzled, tensor_scale
 
 

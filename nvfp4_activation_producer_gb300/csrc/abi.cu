@@ -569,6 +569,37 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, con
   return run_2level(a, MOD_SEG, reinterpret_cast<cudaStream_t>(stream));
 }
 
+NVFP4AP_EXPORT int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* up, int64_t ld, void* packed,
+                                                  void* sf_swizzled, float* tensor_scale, void* workspace,
+                                                  int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
+  if (dim > NVFP4AP_MAX_DIM || dim % 16 != 0) return NVFP4AP_ERR_DIM;
+  if (ld < dim || ld % 8 != 0) return NVFP4AP_ERR_SHAPE;
+  if (rows == 0) return NVFP4AP_OK;
+  if (!gate || !up || !packed || !sf_swizzled || !tensor_scale || !workspace) return NVFP4AP_ERR_NULL;
+  if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(packed, 8) || !aligned(tensor_scale, 4) ||
+      !aligned(workspace, 4))
+    return NVFP4AP_ERR_ALIGN;
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4AP_ERR_LAUNCH;
+  return finish(launch_swiglu_2level(gate, up, ld, rows, dim, packed, sf_swizzled, tensor_scale,
+                                     static_cast<unsigned int*>(workspace), sms,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+NVFP4AP_EXPORT int swiglu_bf16(const void* gate, const void* up, int64_t ld, void* out, int64_t rows, int64_t dim,
+                               nvfp4ap_stream_t stream) {
+  if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
+  if (dim > NVFP4AP_MAX_DIM || dim % 8 != 0) return NVFP4AP_ERR_DIM;
+  if (ld < dim || ld % 8 != 0) return NVFP4AP_ERR_SHAPE;
+  if (rows == 0) return NVFP4AP_OK;
+  if (!gate || !up || !out) return NVFP4AP_ERR_NULL;
+  if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(out, 16)) return NVFP4AP_ERR_ALIGN;
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4AP_ERR_LAUNCH;
+  return finish(launch_swiglu_values(gate, up, ld, rows, dim, out, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {
   if (rows < 0 || dim <= 0 || dim % 16 != 0) return -1;
   const int64_t rows_pad = (rows + 127) / 128 * 128;

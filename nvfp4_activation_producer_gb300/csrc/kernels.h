@@ -137,6 +137,16 @@ cudaError_t launch_ln_2level(const LnArgs& a, int mod, RowShape s, bool full, cu
 // Reads and clears the word set when a segment index was out of range.
 cudaError_t take_seg_fault(unsigned int* fault);
 
+// SwiGLU -> two-level NVFP4 (swiglu.cu): clears ws, maximum pass, quantising
+// pass.  gate/up (rows, dim) bf16 with row stride ld (elements), 16-byte
+// aligned, ld % 8 == 0, dim % 16 == 0.
+cudaError_t launch_swiglu_2level(const void* gate, const void* up, int64_t ld, int64_t rows, int64_t dim,
+                                 void* packed, void* sf, float* tensor_scale, unsigned int* ws, int sms,
+                                 cudaStream_t st);
+// The SwiGLU values themselves, (rows, dim) bf16 contiguous (dim % 8 == 0).
+cudaError_t launch_swiglu_values(const void* gate, const void* up, int64_t ld, int64_t rows, int64_t dim, void* out,
+                                 int sms, cudaStream_t st);
+
 // Six-way modulation (K7).
 struct Mod6Args {
   const float* params;      // (tokens, 6, dim) fp32

@@ -39,7 +39,7 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 20
+    assert len(declared) == 22
 
 
 def test_status_strings_and_version(lib):
@@ -160,6 +160,17 @@ def test_seg_and_two_level_argument_errors(lib):
     b = L.ada_layer_norm_quant_nvfp4_2level_bf16  # x, scale, shift, eps, packed, sf, ts, ws, rows, dim
     assert b(A, NULL, A, 1e-5, A, A, A, A, 4, 64, NULL) == 1
     assert b(A, A, A + 4, 1e-5, A, A, A, A, 4, 64, NULL) == 5
+    w = L.swiglu_quant_nvfp4_2level_bf16  # gate, up, ld, packed, sf, ts, ws, rows, dim
+    assert w(A, A, 64, A, A, A, A, 4, 40, NULL) == 3               # dim % 16
+    assert w(A, A, 32, A, A, A, A, 4, 64, NULL) == 2               # ld < dim
+    assert w(A, A, 68, A, A, A, A, 4, 64, NULL) == 2               # ld % 8
+    assert w(A + 8, A, 64, A, A, A, A, 4, 64, NULL) == 5           # gate not 16-byte aligned
+    assert w(A, A, 64, A, A, NULL, A, 4, 64, NULL) == 1
+    assert w(NULL, NULL, 64, NULL, NULL, NULL, NULL, 0, 64, NULL) == 0
+    v = L.swiglu_bf16  # gate, up, ld, out, rows, dim
+    assert v(A, A, 64, A, 4, 60, NULL) == 3                        # dim % 8
+    assert v(A, A, 64, A + 2, 4, 64, NULL) == 5                    # out not 16-byte aligned
+    assert v(A, A, 64, NULL, 4, 64, NULL) == 1
     c = L.ada_layer_norm_quant_nvfp4_2level_seg_bf16  # x, idx, s, h, nseg, eps, packed, sf, ts, ws, rows, dim
     assert c(A, A, A, A, -1, 1e-5, A, A, A, A, 4, 64, NULL) == 4
     assert c(A, A, A, A, 2, float("nan"), A, A, A, A, 4, 64, NULL) == 7
