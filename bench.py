@@ -77,6 +77,8 @@ def extra_workloads():
         ("fp8_seg_h3", synth.segmented(37810, 5376, 2010)),
         ("nvfp4_2level_seg_h3", synth.segmented(37810, 5376, 2011)),
         ("nvfp4_2level_layer_norm", synth.nvfp4_ln(5070, 3072, 2012)),
+        ("swiglu_values_h3", synth.swiglu(37810, 14336, 2013)),
+        ("nvfp4_2level_swiglu_h3", synth.swiglu(37810, 14336, 2014)),
     ]
 
 
@@ -93,6 +95,12 @@ def alg_bytes(name: str, w) -> int:
     if name == "fp8_seg_h3":
         nseg = w.inputs["seg_scale"].shape[0]
         return 2 * R * D + 4 * R + 4 * nseg * D + R * D + 4   # x, segment index, tables, codes
+    if name == "swiglu_values_h3":
+        return 4 * R * D + 2 * R * D                       # gate and up, bf16 values
+    if name == "nvfp4_2level_swiglu_h3":
+        # two passes over gate and up (the tensor scale needs every value first)
+        sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
+        return 2 * 4 * R * D + R * D // 2 + sf + 4
     if name in ("nvfp4_2level_seg_h3", "nvfp4_2level_layer_norm"):
         # two passes over the input (no block can be encoded before the whole
         # tensor's maximum is known), then codes, scales and the tensor scale
@@ -125,6 +133,8 @@ class DeviceOp:
         R, D = w.rows, w.dim
         if name.startswith("fp8"):
             self.out = (torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev),)
+        elif name.startswith("swiglu"):
+            self.out = (torch.empty((R, D), dtype=torch.bfloat16, device=dev),)
         elif name.startswith("nvfp4_2level"):
             self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
                         torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev),
@@ -175,6 +185,11 @@ class DeviceOp:
         elif n == "nvfp4_2level_layer_norm":
             ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(d["x"], p["eps"], packed=o[0], sf_swizzled=o[1],
                                                             tensor_scale=o[2], workspace=o[3])
+        elif n == "swiglu_values_h3":
+            ap.swiglu_bf16(d["fc1"][:, :self.w.dim], d["fc1"][:, self.w.dim:], out=o[0])
+        elif n == "nvfp4_2level_swiglu_h3":
+            ap.swiglu_quant_nvfp4_2level_bf16(d["fc1"][:, :self.w.dim], d["fc1"][:, self.w.dim:], packed=o[0],
+                                              sf_swizzled=o[1], tensor_scale=o[2], workspace=o[3])
         elif n == "modulation6":
             ap.adaln_modulation6_bf16(d["params"], d["modulation"], out=o[0])
 
@@ -229,6 +244,13 @@ class DeviceOp:
         elif n == "nvfp4_2level_layer_norm":
             fn, a = L.layer_norm_no_affine_quant_nvfp4_2level_bf16, (P(d["x"]), p["eps"], P(o[0]), P(o[1]), P(o[2]),
                                                                      P(o[3]), R, D, stream)
+        elif n == "swiglu_values_h3":
+            g = P(d["fc1"])
+            fn, a = L.swiglu_bf16, (g, g + 2 * D, 2 * D, P(o[0]), R, D, stream)
+        elif n == "nvfp4_2level_swiglu_h3":
+            g = P(d["fc1"])
+            fn, a = L.swiglu_quant_nvfp4_2level_bf16, (g, g + 2 * D, 2 * D, P(o[0]), P(o[1]), P(o[2]), P(o[3]),
+                                                       R, D, stream)
         else:
             self._outs6 = (ctypes.c_void_p * 6)(*[o[0][i].data_ptr() for i in range(6)])
             fn, a = L.adaln_modulation6_bf16, (P(d["params"]), P(d["modulation"]), self._outs6, 1, R, D, stream)

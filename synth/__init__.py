@@ -185,6 +185,12 @@ def segmented(rows: int, dim: int, seed: int, nseg: int = 3, act_scale: float = 
                     {"eps": eps})
 
 
+def swiglu(rows: int, dim: int, seed: int) -> Workload:
+    """SwiGLU input in the FC1-output layout: one (rows, 2*dim) bf16 tensor
+    N(0, 1) whose halves [:, :dim] and [:, dim:] are gate and up."""
+    return Workload("swiglu_*_bf16", rows, dim, {"fc1": bf16(normal(seed, 0, (rows, 2 * dim), 1.0))}, {})
+
+
 def modulation6(batch: int, seq: int, dim: int, seed: int) -> Workload:
     return Workload("adaln_modulation6_bf16", batch * seq, dim,
                     {"params": torch.from_numpy(normal(seed, 0, (batch, seq, 6, dim), 1.0)),
