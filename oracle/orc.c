@@ -72,15 +72,20 @@ double orc_bf16_to_f64(uint16_t bits) { return (double)f32_from_bits((uint32_t)b
 /* Nearest bf16 to a finite binary32 value, ties to the even pattern.
  * The two candidates are the truncation toward zero (`lo`) and the next bf16
  * away from zero (`hi`); both and `v` are exact in double, so are the two
- * distances (each is a difference of nearby binary32 values). */
+ * distances (each is a difference of nearby binary32 values).  Past the
+ * largest finite bf16 the next candidate is the infinity pattern, which
+ * round-to-nearest treats as the value 2^128 (IEEE 754: a result at or
+ * beyond the midpoint between the largest finite value and 2^128 overflows
+ * to infinity). */
 uint16_t orc_bf16_from_f32(float v) {
   uint32_t u = bits_from_f32(v);
   uint32_t lo = u & 0xFFFF0000u;
   if (lo == u) return (uint16_t)(lo >> 16);
   uint32_t hi = lo + 0x10000u;
   double dv = (double)v;
+  double vhi = ((hi & 0x7FFFFFFFu) == 0x7F800000u) ? copysign(ldexp(1.0, 128), dv) : (double)f32_from_bits(hi);
   double dlo = fabs(dv - (double)f32_from_bits(lo));
-  double dhi = fabs((double)f32_from_bits(hi) - dv);
+  double dhi = fabs(vhi - dv);
   if (dlo < dhi) return (uint16_t)(lo >> 16);
   if (dhi < dlo) return (uint16_t)(hi >> 16);
   return ((lo >> 16) & 1u) ? (uint16_t)(hi >> 16) : (uint16_t)(lo >> 16);

@@ -33,13 +33,20 @@ def test_bf16_encode_matches_torch_rne(orc):
     # ties (low half exactly 0x8000) and exact values, both parities of the kept half
     u[:2000] = (u[:2000] & 0xFFFF0000) | 0x8000
     u[2000:3000] &= 0xFFFF0000
+    # the overflow band: every pattern from the largest finite bf16 up to the
+    # largest binary32 (round-to-nearest overflows to infinity from the midpoint on)
+    band = np.arange(0x7F7F0000, 0x7F800000, 7, dtype=np.uint64).astype(np.uint32)
+    band = np.concatenate([band, np.array([0x7F7F7FFF, 0x7F7F8000, 0x7F7F8001, 0x7F7FFFFF], dtype=np.uint32)])
+    u = np.concatenate([u, band, band | np.uint32(0x80000000)])
     f = u.view(np.float32)
-    keep = np.isfinite(f) & (np.abs(f) < 3.0e38)
-    f = f[keep]
+    f = f[np.isfinite(f)]
     ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     L = orc.lib()
     got = np.array([L.orc_bf16_from_f32(float(v)) for v in f], dtype=np.uint16)
     assert np.array_equal(got, ref)
+    # the band's midpoint 0x7F7F8000 ties to the even pattern: infinity (0x7F80)
+    assert L.orc_bf16_from_f32(float(np.uint32(0x7F7F8000).view(np.float32))) == 0x7F80
+    assert L.orc_bf16_from_f32(float(np.uint32(0x7F7F7FFF).view(np.float32))) == 0x7F7F
 
 
 # ---------------------------------------------------------------- e4m3 ----
