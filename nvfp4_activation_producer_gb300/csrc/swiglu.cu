@@ -9,13 +9,13 @@
 //   amax = max |v|;  ts = bf16(amax / 2688)
 //   per 16 elements: s = e4m3(min((amax_b / 6) / ts, 448)); codes e2m1(v / (s * ts))
 //
-// silu's bf16 boundary is taken on the binary32 value of silu.  The fast path
-// (expf, error bound 2 ulp, and an IEEE division: within a few ulp) decides
-// it whenever the fp32 result is more than 16 ulp from a bf16 rounding
-// midpoint; closer than that, and for gates below -80 (where the fp32
-// exponential leaves its range), the value is recomputed in double before
-// rounding -- about 1 element in 2,000 on normal data.  The product of two bf16
-// values is exact in fp32, so its bf16 rounding needs no care.
+// silu's bf16 boundary is taken on the binary32 value of silu.  A bf16 gate
+// has only 65,536 bit patterns, so bf16(binary32(silu(g))) is a table built
+// in float64 when the library is compiled (build.py); the kernels look the
+// gate's pattern up (128 KB, read through L1: activations cluster on a few
+// thousand patterns) instead of evaluating an exponential and a division per
+// element.  The product of two bf16 values is exact in fp32, so its bf16
+// rounding needs no care.
 //
 // Layout: gate and up are (rows, dim) bf16 with a common row stride `ld`
 // (elements): two tensors, or the two halves of one (rows, 2*dim) FC1 output.
@@ -30,17 +30,18 @@
 namespace nvfp4ap {
 namespace {
 
+// bf16(binary32(silu(g))) for every bf16 pattern g (generated, see build.py)
+__device__ const uint16_t kSiluBf16[65536] = {
+#include "silu_bf16_table.inc"
+};
+
 __device__ __forceinline__ float round_bf16(float v) { return bf16_lo(f2_to_bf16x2(make_float2(v, 0.f))); }
 
-// bf16(fp32(silu(g))), see the file comment
-__device__ __forceinline__ float silu_bf16(float g) {
-  float s = __fdiv_rn(g, 1.0f + expf(-g));
-  const uint32_t low = __float_as_uint(s) & 0xFFFFu;
-  if ((low > 0x8000u - 16u && low < 0x8000u + 16u) || g < -80.0f) {
-    const double gd = (double)g;
-    s = (float)(gd / (1.0 + exp(-gd)));
-  }
-  return round_bf16(s);
+// silu of a packed pair of bf16 gates, as a packed pair of bf16 values
+__device__ __forceinline__ uint32_t silu_bf16x2(uint32_t g) {
+  const uint32_t lo = __ldg(&kSiluBf16[g & 0xFFFFu]);
+  const uint32_t hi = __ldg(&kSiluBf16[g >> 16]);
+  return lo | (hi << 16);
 }
 
 // the 8 staged values of one chunk as four packed bf16 pairs
@@ -48,11 +49,8 @@ __device__ __forceinline__ void swiglu8(const uint16_t* g8, const uint16_t* u8, 
   const uint4 g = ld_once_v4(g8), u = ld_once_v4(u8);
   const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 gf = bf16x2_to_f2(gw[i]), uf = bf16x2_to_f2(uw[i]);
-    const float2 s = make_float2(silu_bf16(gf.x), silu_bf16(gf.y));
-    vb[i] = f2_to_bf16x2(mul2(s, uf));  // exact product, one rounding
-  }
+  for (int i = 0; i < 4; ++i)
+    vb[i] = f2_to_bf16x2(mul2(bf16x2_to_f2(silu_bf16x2(gw[i])), bf16x2_to_f2(uw[i])));  // exact product, one rounding
 }
 
 struct SwArgs {

@@ -2,11 +2,12 @@
 
 v = bf16(bf16(silu(gate)) * up) (h3-blackwell-runtime compare page,
 NVFP4_SWIGLU_FUSION_DESIGN.md), then the two-level NVFP4 contract.  The
-staged values must equal the oracle's bit for bit (swiglu_bf16): random
-gates, every gate whose binary32 silu lies within 16 ulp of a bf16 rounding
-midpoint (the kernel's double-precision path), gates beyond the fp32
-exponential's range, both memory layouts (two tensors, halves of one).  The
-two-level outputs follow tests/parity.py with the tensor scale exact.
+staged values must equal the oracle's bit for bit (swiglu_bf16): every
+finite bf16 gate pattern (times one and times random ups), random gates,
+gates whose binary32 silu lies within 16 ulp of a bf16 rounding midpoint,
+gates beyond the fp32 exponential's range, both memory layouts (two tensors,
+halves of one).  The two-level outputs follow tests/parity.py with the
+tensor scale exact.
 """
 import numpy as np
 import pytest
@@ -45,7 +46,9 @@ def _values_case(ap, dev, g, u, fused):
     out = ap.swiglu_bf16(gate, up)
     ref = oracle.swiglu_values(_bits(g), _bits(u))
     got = _bits(out)
-    assert np.array_equal(got, ref), int((got != ref).sum())
+    bad = np.argwhere(got != ref)[:8]
+    detail = [(int(r), int(c), hex(_bits(g)[r, c]), hex(_bits(u)[r, c]), hex(got[r, c]), hex(ref[r, c])) for r, c in bad]
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} differ (row, col, gate, up, got, oracle): {detail}"
 
 
 @pytest.mark.parametrize("rows,dim", [(1, 8), (37, 1536), (129, 5376), (64, 14336)])
@@ -54,6 +57,19 @@ def test_swiglu_values_bit_exact(ap, dev, rows, dim, fused):
     g = synth.bf16(synth.normal(rows + dim, 0, (rows, dim), 3.0))
     u = synth.bf16(synth.normal(rows + dim, 1, (rows, dim), 1.0))
     _values_case(ap, dev, g, u, fused)
+
+
+def test_swiglu_values_every_gate_pattern(ap, dev):
+    b = np.arange(0, 0x10000, dtype=np.uint32)
+    g32 = (b << 16).view(np.float32)
+    pats = b[np.isfinite(g32)].astype(np.uint16)
+    dim = 256
+    n = (pats.size + dim - 1) // dim * dim
+    gb = np.zeros(n, dtype=np.uint16)
+    gb[:pats.size] = pats
+    g = torch.from_numpy(gb.view(np.int16).reshape(-1, dim)).view(torch.bfloat16)
+    _values_case(ap, dev, g, synth.bf16(np.ones(g.shape, dtype=np.float32)), False)
+    _values_case(ap, dev, g, synth.bf16(synth.normal(9, 1, g.shape, 1.0)), True)
 
 
 def test_swiglu_values_near_bf16_midpoints_and_extremes(ap, dev):
