@@ -193,6 +193,19 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   int kernel = env_int("NVFP4AP_KERNEL");
   if (kernel == 0) kernel = (mod == MOD_TABLE) ? 4 : 3;
   if (kernel == 1 && (mod == MOD_MODFP8 || mod == MOD_AWQ)) kernel = 3;
+  if (kernel == 5) {
+    // block-per-lane persistent kernel where it applies, else the default
+    if (vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) && aligned(a.out, 16)) {
+      BlkShape bs{};
+      const int sms = sm_count();
+      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+        bs.ctas_per_sm = env_int("NVFP4AP_BLK_CTAS");
+        bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+        return finish(launch_ln_blk(a, false, mod, bs, sms, st));
+      }
+    }
+    kernel = (mod == MOD_TABLE) ? 4 : 3;
+  }
   RingShape rs{};
   if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
@@ -246,6 +259,15 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   if (!a.x || !a.out || (nvfp4 ? !a.sf : !a.act_scale)) return NVFP4AP_ERR_NULL;
   if ((rc = check_seg(a)) != NVFP4AP_OK) return rc;
   if (!aligned(a.x, 16) || !aligned(a.out, 8) || (!nvfp4 && !aligned(a.act_scale, 4))) return NVFP4AP_ERR_ALIGN;
+  if (env_int("NVFP4AP_KERNEL") == 5 && ln_blk_supported(nvfp4 ? BLK_NVFP4 : BLK_FP8, MOD_SEG, a.dim, a.nseg) &&
+      aligned(a.x, 32) && aligned(a.out, 16)) {
+    BlkShape bs{};
+    const int sms = sm_count();
+    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+      bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+      return finish(launch_ln_blk(a, nvfp4, MOD_SEG, bs, sms, st));
+    }
+  }
   RowShape s{};
   if (!pick_rows(MOD_SEG, a.dim, &s)) return NVFP4AP_ERR_DIM;
   const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
@@ -266,6 +288,20 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   if (!aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.tensor_scale, 4) || !aligned(a.amax_ws, 4))
     return NVFP4AP_ERR_ALIGN;
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
+  // default (and NVFP4AP_KERNEL=5): the block-per-lane kernels -- persistent,
+  // one atomic per CTA in the maximum pass -- where they apply (measured on
+  // GB300: 37810x5376 segmented 341 -> 284 us, 5070x3072 20.9 -> 18.5 us);
+  // any other NVFP4AP_KERNEL value, or a shape they do not take: the register
+  // row kernels
+  const int kernel = env_int("NVFP4AP_KERNEL");
+  if ((kernel == 0 || kernel == 5) && ln_blk_supported(BLK_2LEVEL, mod, a.dim, a.nseg) && aligned(a.x, 32)) {
+    BlkShape bs{};
+    const int sms = sm_count();
+    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+      bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+      return finish(launch_ln_2level_blk(a, mod, bs, sms, st));
+    }
+  }
   RowShape s{};
   if (!pick_rows(mod, a.dim, &s)) return NVFP4AP_ERR_DIM;
   if (!grid_ok((a.rows + 127) / 128 * 128, s.rpc)) return NVFP4AP_ERR_SHAPE;
@@ -291,6 +327,18 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
 
   int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8; auto = row kernels
   if (kernel == 0) kernel = 3;
+  if (kernel == 5) {
+    if (ln_blk_supported(BLK_NVFP4, mod, a.dim, 0) && aligned(a.x, 32)) {
+      BlkShape bs{};
+      const int sms = sm_count();
+      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+        bs.ctas_per_sm = env_int("NVFP4AP_BLK_CTAS");
+        bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+        return finish(launch_ln_blk(a, true, mod, bs, sms, st));
+      }
+    }
+    kernel = 3;
+  }
   // the modfp8 source runs on the register kernels only
   if (mod == MOD_MODFP8 && kernel != 3 && kernel != 4) kernel = 3;
   RingShape rs{};
@@ -374,12 +422,13 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
-  unsigned int f = 0u, g = 0u, h = 0u;
-  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess) {
+  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u;
+  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess ||
+      take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  return (f | g | h) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  return (f | g | h | i | j) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,

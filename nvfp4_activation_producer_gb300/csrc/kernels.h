@@ -97,6 +97,30 @@ cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStrea
 cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms,
                                        int ctas_per_sm, cudaStream_t st);
 
+// Block-per-lane persistent row kernels (ln_blk.cuh; ln_blk.cu, ln_blk2l.cu):
+// a lane owns whole 16-element blocks (`bpt` of them), `tpr` threads per row
+// (a multiple of 32, <= 256), 512-thread CTAs of 512 / tpr rows, at most
+// `ctas_per_sm` CTAs per SM (0 = as many as fit), at most `max_ctas` CTAs in
+// all (0 = no limit).  Modulation as fp32 tables in shared memory.
+// dim % 16 == 0, dim <= kBlkMaxDim; x 32-byte aligned; FP8 out 16-byte
+// aligned; broadcast bf16 sources and segment tables 16-byte aligned.
+struct BlkShape {
+  int tpr, bpt, ctas_per_sm, max_ctas;
+};
+constexpr int64_t kBlkMaxDim = 8192;
+enum { BLK_FP8 = 0, BLK_NVFP4 = 1, BLK_2LEVEL = 2 };
+// `kind` BLK_*; nseg: segments of a MOD_SEG source (their tables must fit)
+bool ln_blk_supported(int kind, int mod, int64_t dim, int64_t nseg);
+// shape for `dim` (forced_bpt > 0: only that many blocks per lane)
+bool pick_blk(int64_t dim, int forced_bpt, BlkShape* s);
+cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int sms, cudaStream_t st);
+// two-level NVFP4 on the block-per-lane kernels: clears a.amax_ws, maximum
+// pass, quantising pass; mod MOD_NONE, MOD_BCAST or MOD_SEG
+cudaError_t launch_ln_2level_blk(const LnArgs& a, int mod, BlkShape s, int sms, cudaStream_t st);
+// read and clear the segment-index fault words of the two translation units
+cudaError_t take_blk_seg_fault(unsigned int* fault);
+cudaError_t take_blk2l_seg_fault(unsigned int* fault);
+
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 int ln_nvfp4_max_tpr(int per_thread);

@@ -49,7 +49,7 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["auto", "rows", "rows_flat", "tile4", "tma", "ring", "legacy"])
+@pytest.fixture(params=["auto", "rows", "rows_flat", "tile4", "tma", "ring", "legacy", "blk"])
 def path(request, monkeypatch):
     """Run a LayerNorm-producer test on each kernel family: the default choice
     (TMA pipeline for the table form, register row kernels otherwise), the
@@ -57,10 +57,10 @@ def path(request, monkeypatch):
     the persistent broadcast variant and the register-capped NVFP4 instance
     (NVFP4AP_PERSIST=-1, NVFP4AP_FULL=0), the NVFP4
     four-row-tile variant (NVFP4AP_TILE4=1), the TMA pipeline
-    for every form (4), the warp-per-row TMA ring (1) and the first register
-    kernels (2)."""
+    for every form (4), the warp-per-row TMA ring (1), the first register
+    kernels (2) and the block-per-lane persistent kernels (5)."""
     kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tile4": "3", "tma": "4", "ring": "1",
-              "legacy": "2"}[request.param]
+              "legacy": "2", "blk": "5"}[request.param]
     if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:

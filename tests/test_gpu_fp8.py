@@ -213,6 +213,28 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
     ap.take_device_fault()  # no bounded wait ran out
 
 
+@pytest.mark.parametrize("op", ["ln", "bcast"])
+def test_blk_many_rows_per_group(ap, dev, op, monkeypatch):
+    # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows
+    # (prefetch buffer, parity slots); 17 and 192 blocks per row
+    monkeypatch.setenv("NVFP4AP_KERNEL", "5")
+    rows = 3001
+    for ctas, dim in ((1, 272), (3, 3072)):
+        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
+        if op == "bcast":
+            w = synth.fp8_broadcast(rows, dim, seed=ctas)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+        else:
+            w = synth.fp8_ln(rows, dim, seed=ctas)
+            d = _d(w, dev)
+            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
+        check_fp8(_codes(out), ref, _act(w))
+
+
 @pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
 def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
     # one CTA per SM and 1, 2 or 5 stages: each CTA walks ~40 rows, so every

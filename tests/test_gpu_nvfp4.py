@@ -159,6 +159,20 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
 
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
+def test_blk_many_rows_per_group(ap, dev, kind, monkeypatch):
+    # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows
+    # (prefetch buffer, parity slots); 17 and 192 blocks per row (one idle lane
+    # range and an exact fit), 3000 rows (row padding of the last scale tile)
+    monkeypatch.setenv("NVFP4AP_KERNEL", "5")
+    for ctas, dim in ((1, 272), (3, 3072)):
+        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
+        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(3000, dim, seed=ctas)
+        gp, gs = _run(ap, kind, w, dev)
+        op, os_, v = _oracle(w, kind)
+        check_nvfp4(gp, gs, op, os_, 3000, dim, v_orc=v)
+
+
+@pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_unaligned_scale_buffer(ap, dev, kind):
     # a scale buffer off 16-byte alignment takes the byte-store path
     w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(300, 3072, seed=17)

@@ -10,7 +10,10 @@ the last scale tile), several dims (capped and uncapped kernels), the page's
 segment layout and random segment assignments, an all-zero tensor, a tensor
 whose maximum is 2688 (ts = 1), an out-of-range segment index (zero
 modulation for that row plus the device fault word), workspace reuse, a CUDA
-graph capture of the three operations.
+graph capture of the three operations.  Every case runs on the default
+kernels (block-per-lane for the two-level forms, register row kernels for the
+single-level segmented forms), on the register row kernels
+(NVFP4AP_KERNEL=3) and on the block-per-lane kernels (NVFP4AP_KERNEL=5).
 """
 import numpy as np
 import pytest
@@ -23,6 +26,16 @@ from parity import check_fp8, check_nvfp4
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (130, 4096), (5, 32768), (257, 1536)]
+
+
+@pytest.fixture(autouse=True, params=["auto", "rows", "blk"])
+def family(request, monkeypatch):
+    if request.param == "auto":
+        monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("NVFP4AP_KERNEL", "5" if request.param == "blk" else "3")
+    monkeypatch.delenv("NVFP4AP_BLK_GRID", raising=False)
+    return request.param
 
 
 def _u(t):
@@ -170,3 +183,35 @@ def test_two_level_workspace_reuse_and_graph(ap, dev):
         g.replay()
     st.synchronize()
     assert torch.equal(pk, outs[0][0]) and torch.equal(sf, outs[0][1]) and torch.equal(ts, outs[0][2])
+
+
+@pytest.mark.parametrize("kind", ["none", "bcast", "seg"])
+def test_two_level_many_rows_per_group(ap, dev, family, kind, monkeypatch):
+    # block-per-lane kernels on 1 and 3 CTAs: each row group walks many rows and
+    # the maximum pass reduces them in one CTA
+    if family == "rows":
+        pytest.skip("grid limit of the block-per-lane kernels")
+    for ctas, dim in ((1, 272), (3, 3072)):
+        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
+        rows = 3000
+        w = synth.segmented(rows, dim, seed=ctas + 7)
+        d = {k: v.to(dev) for k, v in w.inputs.items()}
+        x = _u(w.inputs["x"])
+        if kind == "seg":
+            src = _seg_src(w)
+            pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"],
+                                                                       d["seg_shift"])
+            mk = oracle.MOD_SEG
+        elif kind == "bcast":
+            sc, sh = d["seg_scale"][1].contiguous(), d["seg_shift"][1].contiguous()
+            src = dict(scale=_u(w.inputs["seg_scale"][1]), shift=_u(w.inputs["seg_shift"][1]))
+            pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_bf16(d["x"], sc, sh)
+            mk = oracle.MOD_BCAST
+        else:
+            src = {}
+            pk, sf, ts = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(d["x"])
+            mk = oracle.MOD_NONE
+        opk, osf, ots = oracle.ln_quant_nvfp4_2level(x, mk, **src)
+        assert float(ts.cpu()[0]) == ots
+        check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(x, mk, **src),
+                    f"two-level {kind} on {ctas} CTAs", ts=ots)
