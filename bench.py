@@ -275,10 +275,12 @@ def measured_peaks():
         return None
 
 
-def kernel_sources_digest() -> str:
+def sources_digest(files) -> str:
+    """Digest of the named kernel source files (csrc/), to tell whether a
+    committed counter capture was taken on the current sources."""
     csrc = os.path.join(ROOT, "nvfp4_activation_producer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
@@ -286,15 +288,15 @@ def kernel_sources_digest() -> str:
 
 def committed_traffic(op: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the current sources of that producer's kernel (else None)."""
     try:
         t = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
-    except (OSError, ValueError):
+        rec = t.get("per_launch", {}).get(op)
+        if not rec or rec.get("sources_digest") != sources_digest(rec["sources"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
-    if t.get("kernel_sources_digest") != kernel_sources_digest():
-        return None
-    rec = t.get("per_launch", {}).get(op)
-    return rec.get("dram_bytes") if rec else None
+    return rec.get("dram_bytes")
 
 
 class ClockSampler:
