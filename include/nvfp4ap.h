@@ -282,15 +282,17 @@ int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, const int32_t* seg
  * the two-level contract above on v (no LayerNorm).  gate, up: device
  * (rows, dim) bf16 with the common row stride ld (elements): two tensors, or
  * the halves of one (rows, 2*dim) tensor (up = gate + dim, ld = 2*dim).  dim %
- * 16 == 0, ld >= dim and ld % 8 == 0 (NVFP4AP_ERR_DIM / _SHAPE), gate and up
- * 16-byte aligned.  Outputs and workspace as for the two-level producers. */
+ * 16 == 0, ld >= dim, ld % 8 == 0 and rows * (dim / 8) < 2^32 (NVFP4AP_ERR_DIM /
+ * _SHAPE), gate and up 16-byte aligned (32-byte aligned with ld % 16 == 0 takes
+ * 256-bit loads).  Outputs and workspace as for the two-level producers. */
 int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* up, int64_t ld, void* packed, void* sf_swizzled,
                                    float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
                                    nvfp4ap_stream_t stream);
 
 /* The SwiGLU values of swiglu_quant_nvfp4_2level_bf16 themselves:
  * out (rows, dim) bf16 contiguous, v = bf16(bf16(silu(gate)) * up) -- the
- * materialised form.  dim % 8 == 0, gate/up/out 16-byte aligned, ld as above. */
+ * materialised form.  dim % 8 == 0, gate/up/out 16-byte aligned, ld and rows as
+ * above. */
 int swiglu_bf16(const void* gate, const void* up, int64_t ld, void* out, int64_t rows, int64_t dim,
                 nvfp4ap_stream_t stream);
 

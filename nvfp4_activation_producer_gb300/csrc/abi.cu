@@ -623,7 +623,7 @@ NVFP4AP_EXPORT int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* 
                                                   int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
   if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (dim > NVFP4AP_MAX_DIM || dim % 16 != 0) return NVFP4AP_ERR_DIM;
-  if (ld < dim || ld % 8 != 0) return NVFP4AP_ERR_SHAPE;
+  if (ld < dim || ld % 8 != 0 || !swiglu_items_fit(rows, dim)) return NVFP4AP_ERR_SHAPE;
   if (rows == 0) return NVFP4AP_OK;
   if (!gate || !up || !packed || !sf_swizzled || !tensor_scale || !workspace) return NVFP4AP_ERR_NULL;
   if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(packed, 8) || !aligned(tensor_scale, 4) ||
@@ -640,7 +640,7 @@ NVFP4AP_EXPORT int swiglu_bf16(const void* gate, const void* up, int64_t ld, voi
                                nvfp4ap_stream_t stream) {
   if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (dim > NVFP4AP_MAX_DIM || dim % 8 != 0) return NVFP4AP_ERR_DIM;
-  if (ld < dim || ld % 8 != 0) return NVFP4AP_ERR_SHAPE;
+  if (ld < dim || ld % 8 != 0 || !swiglu_items_fit(rows, dim)) return NVFP4AP_ERR_SHAPE;
   if (rows == 0) return NVFP4AP_OK;
   if (!gate || !up || !out) return NVFP4AP_ERR_NULL;
   if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(out, 16)) return NVFP4AP_ERR_ALIGN;

@@ -161,9 +161,12 @@ cudaError_t launch_ln_2level(const LnArgs& a, int mod, RowShape s, bool full, cu
 // Reads and clears the word set when a segment index was out of range.
 cudaError_t take_seg_fault(unsigned int* fault);
 
+// SwiGLU work items (8-element chunks) of a (rows, dim) call fit the kernels'
+// 32-bit item index: rows * (dim / 8) < 2^32.
+bool swiglu_items_fit(int64_t rows, int64_t dim);
 // SwiGLU -> two-level NVFP4 (swiglu.cu): clears ws, maximum pass, quantising
 // pass.  gate/up (rows, dim) bf16 with row stride ld (elements), 16-byte
-// aligned, ld % 8 == 0, dim % 16 == 0.
+// aligned, ld % 8 == 0, dim % 16 == 0, swiglu_items_fit(rows, dim).
 cudaError_t launch_swiglu_2level(const void* gate, const void* up, int64_t ld, int64_t rows, int64_t dim,
                                  void* packed, void* sf, float* tensor_scale, unsigned int* ws, int sms,
                                  cudaStream_t st);

@@ -19,11 +19,16 @@
 //
 // Layout: gate and up are (rows, dim) bf16 with a common row stride `ld`
 // (elements): two tensors, or the two halves of one (rows, 2*dim) FC1 output.
-// Threads take 8-element chunks in a grid-stride loop whose bounds are warp-
-// uniform (full-mask shuffles); chunks 2b and 2b+1 -- the halves of NVFP4
-// block b -- sit in lanes t and t^1.  Two launches after a clear of the
-// caller's word: the maximum pass (a running maximum per thread, one gated
-// atomic per warp at the end) and the quantising pass.
+// Work items are 16-element blocks (two-level passes) or 8-element chunks
+// (materialised values) in one flat grid-stride loop; an item's row comes
+// from a multiply-high division by the invariant items-per-row count
+// (Granlund and Montgomery's unsigned division by invariant integers), so the
+// loop carries no 64-bit division.  In the two-level passes a lane owns a
+// whole NVFP4 block: its gate and up are two 32-byte reads (one 256-bit load
+// each when both are 32-byte aligned), and its maximum, scale and 16 codes are
+// computed once, with no shuffle.  Two launches after a clear of the caller's
+// word: the maximum pass (a running maximum per thread, one atomic per CTA)
+// and the quantising pass.
 #include "device.cuh"
 #include "kernels.h"
 
@@ -35,6 +40,8 @@ __device__ const uint16_t kSiluBf16[65536] = {
 #include "silu_bf16_table.inc"
 };
 
+constexpr int kSwThreads = 256;
+
 __device__ __forceinline__ float round_bf16(float v) { return bf16_lo(f2_to_bf16x2(make_float2(v, 0.f))); }
 
 // silu of a packed pair of bf16 gates, as a packed pair of bf16 values
@@ -44,13 +51,49 @@ __device__ __forceinline__ uint32_t silu_bf16x2(uint32_t g) {
   return lo | (hi << 16);
 }
 
-// the 8 staged values of one chunk as four packed bf16 pairs
-__device__ __forceinline__ void swiglu8(const uint16_t* g8, const uint16_t* u8, uint32_t (&vb)[4]) {
-  const uint4 g = ld_once_v4(g8), u = ld_once_v4(u8);
-  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    vb[i] = f2_to_bf16x2(mul2(bf16x2_to_f2(silu_bf16x2(gw[i])), bf16x2_to_f2(uw[i])));  // exact product, one rounding
+// v = bf16(silu(g) * u) for one packed pair (the product is exact, one rounding)
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t g, uint32_t u) {
+  return f2_to_bf16x2(mul2(bf16x2_to_f2(silu_bf16x2(g)), bf16x2_to_f2(u)));
+}
+
+// Unsigned 32-bit division by an invariant d >= 1 (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994, the N = 32
+// unsigned case): with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+// t = mulhi(m, n): n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) for
+// every n < 2^32.
+struct Div32 {
+  uint32_t d, m;
+  int sh1, sh2;
+};
+
+Div32 make_div(uint32_t d) {
+  int l = 0;
+  while (l < 32 && ((uint64_t)1 << l) < d) ++l;
+  Div32 v;
+  v.d = d;
+  v.m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << l) - d)) / d + 1);
+  v.sh1 = l < 1 ? l : 1;
+  v.sh2 = l - 1 > 0 ? l - 1 : 0;
+  return v;
+}
+
+__device__ __forceinline__ uint32_t div32(uint32_t n, const Div32& v) {
+  const uint32_t t = __umulhi(v.m, n);
+  return (t + ((n - t) >> v.sh1)) >> v.sh2;
+}
+
+// 32 contiguous bytes (16 bf16 values), read once
+template <bool V8>
+__device__ __forceinline__ void ld_block16(const uint16_t* p, uint32_t (&w)[8]) {
+  if constexpr (V8) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+  } else {
+    const uint4 a = ld_once_v4(p), b = ld_once_v4(p + 8);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
 }
 
 struct SwArgs {
@@ -61,6 +104,8 @@ struct SwArgs {
   uint8_t* sf;
   float* tensor_scale;
   unsigned int* amax_ws;
+  uint32_t items;  // rows * items per row
+  Div32 per_row;   // items per row (16-element blocks or 8-element chunks)
 };
 
 __global__ void sw_clear_kernel(unsigned int* w) {
@@ -68,64 +113,72 @@ __global__ void sw_clear_kernel(unsigned int* w) {
   *w = 0u;
 }
 
-template <bool QUANT>
-__global__ void __launch_bounds__(256) swiglu_kernel(const SwArgs a) {
+template <bool QUANT, bool V8>
+__global__ void __launch_bounds__(kSwThreads) swiglu_kernel(const SwArgs a) {
+  __shared__ float redm[kSwThreads / 32];
   pdl_enter();
-  const int lane = threadIdx.x & 31;
-  const int nch = (int)(a.dim >> 3);
-  const int64_t total = a.rows * nch;  // even: dim % 16 == 0
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
+  const int nblk = (int)(a.dim >> 4), padc = (nblk + 3) & ~3, ct = padc >> 2;
+  const uint32_t stride = gridDim.x * blockDim.x;
 
   float ts = 1.0f, run = 0.0f;
   if constexpr (QUANT) {
     ts = round_bf16(__fdiv_rn(__uint_as_float(__ldcg(a.amax_ws)), 2688.0f));
     if (blockIdx.x == 0 && threadIdx.x == 0) a.tensor_scale[0] = ts;
   }
-  for (int64_t c0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); c0 < total; c0 += stride) {
-    const int64_t c = c0 + lane;
-    const bool valid = c < total;
-    const int64_t r = valid ? c / nch : 0;
-    const int j = valid ? (int)(c - r * nch) : 0;
-    uint32_t vb[4] = {0u, 0u, 0u, 0u};
-    if (valid) swiglu8(a.gate + r * a.ld + (int64_t)j * 8, a.up + r * a.ld + (int64_t)j * 8, vb);
-    const uint32_t m2 = bf16x2_absmax(bf16x2_absmax(vb[0], vb[1]), bf16x2_absmax(vb[2], vb[3]));
-    float amax = fmaxf(fabsf(bf16_lo(m2)), fabsf(bf16_hi(m2)));
+  for (uint32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < a.items; n += stride) {
+    const uint32_t r = div32(n, a.per_row), b = n - r * (uint32_t)nblk;
+    const int64_t off = (int64_t)r * a.ld + (int64_t)b * 16;
+    uint32_t gw[8], uw[8], vb[8];
+    ld_block16<V8>(a.gate + off, gw);
+    ld_block16<V8>(a.up + off, uw);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vb[i] = swiglu_pair(gw[i], uw[i]);
+    const uint32_t m = bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(vb[0], vb[1]), bf16x2_absmax(vb[2], vb[3])),
+                                     bf16x2_absmax(bf16x2_absmax(vb[4], vb[5]), bf16x2_absmax(vb[6], vb[7])));
+    const float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
     if constexpr (!QUANT) {
       run = fmaxf(run, amax);
     } else {
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // the block's other half
+      // (amax_b / 6) / ts with IEEE divisions, clamped at 448 (fminf takes 448
+      // for the 0/0 of an all-zero tensor); the divisor of the codes is s * ts,
+      // exact in fp32; a divisor below 2^-64 and the values are scaled by 2^64
       const uint32_t sbyte =
           f2_to_e4m3x2(make_float2(fminf(__fdiv_rn(__fdiv_rn(amax, 6.0f), ts), 448.0f), 0.f)) & 0xFFu;
       float scl = e4m3_to_f32(sbyte) * ts, pre = 1.0f;
-      if (scl != 0.f && scl < 0x1p-64f) {  // keep the reciprocal out of the flushed range (exact rescale)
+      if (scl != 0.f && scl < 0x1p-64f) {
         scl *= 0x1p64f;
         pre = 0x1p64f;
       }
+      // v / (s * ts) as v * (r_hi + r_lo), r_lo the Newton correction of
+      // r_hi ~ 1/divisor: exact at every e2m1 midpoint (see ln_rows.cuh)
       const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
       const float rl = rh * fmaf(-scl, rh, 1.0f);
       const float2 rh2 = splat2(rh), rl2 = splat2(rl);
-      float2 q[4];
+      float2 q[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 v = mul2(bf16x2_to_f2(vb[i]), splat2(pre));
+      for (int i = 0; i < 8; ++i) {
+        float2 v = bf16x2_to_f2(vb[i]);
+        if (pre != 1.0f) v = mul2(v, splat2(pre));
         q[i] = fma2(v, rh2, mul2(v, rl2));
       }
-      const uint32_t codes = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
-      if (valid) {
-        st_stream_b32(a.packed + r * (a.dim >> 1) + (int64_t)j * 4, codes);
-        if ((j & 1) == 0) {
-          const int b = j >> 1;
-          st_b8(a.sf + ((r >> 7) * ct + (b >> 2)) * 512 + (int)((r & 31) << 4) + (int)(((r >> 5) & 3) << 2) + (b & 3),
-                sbyte);
-        }
-      }
+      st_stream_v2(a.packed + (int64_t)r * (a.dim >> 1) + (int64_t)b * 8, f8_to_e2m1x8(q[0], q[1], q[2], q[3]),
+                   f8_to_e2m1x8(q[4], q[5], q[6], q[7]));
+      st_b8(a.sf + ((int64_t)(r >> 7) * ct + (b >> 2)) * 512 + (int)((r & 31) << 4) + (int)(((r >> 5) & 3) << 2) +
+                (b & 3),
+            sbyte);
     }
   }
   if constexpr (!QUANT) {
+    // the CTA's largest |v| (non-negative fp32: its bits order like the values)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) run = fmaxf(run, __shfl_xor_sync(0xFFFFFFFFu, run, o));
-    if (lane == 0 && run > __uint_as_float(__ldcg(a.amax_ws))) atomicMax(a.amax_ws, __float_as_uint(run));
+    if ((threadIdx.x & 31) == 0) redm[threadIdx.x >> 5] = run;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mx = redm[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, redm[w]);
+      if (mx > 0.f) atomicMax(a.amax_ws, __float_as_uint(mx));
+    }
   } else {
     // padding of the swizzled scale buffer: columns nblk..padc-1 of every row,
     // and all columns of the rows up to the next multiple of 128
@@ -149,58 +202,63 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const SwArgs a) {
   }
 }
 
-// the staged values themselves (the materialised form), 16 bytes per chunk
-__global__ void __launch_bounds__(256) swiglu_values_kernel(const SwArgs a, uint16_t* out) {
+// the staged values themselves (the materialised form): 8-element chunks,
+// 16 bytes of gate, up and output each
+__global__ void __launch_bounds__(kSwThreads) swiglu_values_kernel(const SwArgs a, uint16_t* out) {
   pdl_enter();
-  const int nch = (int)(a.dim >> 3);
-  const int64_t total = a.rows * nch;
-  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = c / nch;
-    const int j = (int)(c - r * nch);
-    uint32_t vb[4];
-    swiglu8(a.gate + r * a.ld + (int64_t)j * 8, a.up + r * a.ld + (int64_t)j * 8, vb);
-    st_stream_v4(out + r * a.dim + (int64_t)j * 8, make_uint4(vb[0], vb[1], vb[2], vb[3]));
+  const uint32_t nch = (uint32_t)(a.dim >> 3);
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < a.items; n += stride) {
+    const uint32_t r = div32(n, a.per_row), j = n - r * nch;
+    const int64_t off = (int64_t)r * a.ld + (int64_t)j * 8;
+    const uint4 g = ld_once_v4(a.gate + off), u = ld_once_v4(a.up + off);
+    st_stream_v4(out + (int64_t)r * a.dim + (int64_t)j * 8,
+                 make_uint4(swiglu_pair(g.x, u.x), swiglu_pair(g.y, u.y), swiglu_pair(g.z, u.z),
+                            swiglu_pair(g.w, u.w)));
   }
 }
 
-int sw_grid(int sms) {
-  static int occ = 0;
-  if (occ == 0) {
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, swiglu_kernel<true>, 256, 0) != cudaSuccess || o < 1) o = 1;
-    occ = o;
-  }
-  return sms * occ;
+template <typename K>
+int sw_grid(K k, int sms, int64_t items) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kSwThreads, 0) != cudaSuccess || occ < 1) occ = 1;
+  int64_t grid = (int64_t)sms * occ;
+  const int64_t need = (items + kSwThreads - 1) / kSwThreads;
+  if (grid > need) grid = need < 1 ? 1 : need;
+  return (int)grid;
 }
 
 }  // namespace
 
+bool swiglu_items_fit(int64_t rows, int64_t dim) { return rows * (dim / 8) < ((int64_t)1 << 32); }
+
 cudaError_t launch_swiglu_2level(const void* gate, const void* up, int64_t ld, int64_t rows, int64_t dim,
                                  void* packed, void* sf, float* tensor_scale, unsigned int* ws, int sms,
                                  cudaStream_t st) {
+  if (!swiglu_items_fit(rows, dim)) return cudaErrorInvalidValue;
+  const uint32_t nblk = (uint32_t)(dim / 16);
   SwArgs a{static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up), ld, rows, dim,
-           static_cast<uint8_t*>(packed), static_cast<uint8_t*>(sf), tensor_scale, ws};
-  const int64_t chunks = rows * (dim / 8);
-  int64_t grid = sw_grid(sms);
-  const int64_t need = (chunks + 255) / 256;
-  if (grid > need) grid = need < 1 ? 1 : need;
+           static_cast<uint8_t*>(packed), static_cast<uint8_t*>(sf), tensor_scale, ws,
+           (uint32_t)(rows * nblk), make_div(nblk)};
+  const bool v8 = (reinterpret_cast<uintptr_t>(gate) % 32 == 0) && (reinterpret_cast<uintptr_t>(up) % 32 == 0) &&
+                  (ld % 16 == 0);
   cudaError_t e = launch_maybe_pdl(sw_clear_kernel, dim3(1), dim3(1), 0, st, ws);
   if (e != cudaSuccess) return e;
-  e = launch_maybe_pdl(swiglu_kernel<false>, dim3((unsigned)grid), dim3(256), 0, st, a);
+  auto k0 = v8 ? swiglu_kernel<false, true> : swiglu_kernel<false, false>;
+  auto k1 = v8 ? swiglu_kernel<true, true> : swiglu_kernel<true, false>;
+  e = launch_maybe_pdl(k0, dim3(sw_grid(k0, sms, a.items)), dim3(kSwThreads), 0, st, a);
   if (e != cudaSuccess) return e;
-  return launch_maybe_pdl(swiglu_kernel<true>, dim3((unsigned)grid), dim3(256), 0, st, a);
+  return launch_maybe_pdl(k1, dim3(sw_grid(k1, sms, a.items)), dim3(kSwThreads), 0, st, a);
 }
 
 cudaError_t launch_swiglu_values(const void* gate, const void* up, int64_t ld, int64_t rows, int64_t dim, void* out,
                                  int sms, cudaStream_t st) {
+  if (!swiglu_items_fit(rows, dim)) return cudaErrorInvalidValue;
+  const uint32_t nch = (uint32_t)(dim / 8);
   SwArgs a{static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up), ld, rows, dim, nullptr, nullptr,
-           nullptr, nullptr};
-  const int64_t chunks = rows * (dim / 8);
-  int64_t grid = sw_grid(sms);
-  const int64_t need = (chunks + 255) / 256;
-  if (grid > need) grid = need < 1 ? 1 : need;
-  return launch_maybe_pdl(swiglu_values_kernel, dim3((unsigned)grid), dim3(256), 0, st, a,
-                          static_cast<uint16_t*>(out));
+           nullptr, nullptr, (uint32_t)(rows * nch), make_div(nch)};
+  return launch_maybe_pdl(swiglu_values_kernel, dim3(sw_grid(swiglu_values_kernel, sms, a.items)), dim3(kSwThreads),
+                          0, st, a, static_cast<uint16_t*>(out));
 }
 
 }  // namespace nvfp4ap

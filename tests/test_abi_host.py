@@ -167,7 +167,9 @@ def test_seg_and_two_level_argument_errors(lib):
     assert w(A + 8, A, 64, A, A, A, A, 4, 64, NULL) == 5           # gate not 16-byte aligned
     assert w(A, A, 64, A, A, NULL, A, 4, 64, NULL) == 1
     assert w(NULL, NULL, 64, NULL, NULL, NULL, NULL, 0, 64, NULL) == 0
+    assert w(A, A, 64, A, A, A, A, 1 << 29, 64, NULL) == 2         # rows * dim/8 >= 2^32 work items
     v = L.swiglu_bf16  # gate, up, ld, out, rows, dim
+    assert v(A, A, 64, A, 1 << 29, 64, NULL) == 2
     assert v(A, A, 64, A, 4, 60, NULL) == 3                        # dim % 8
     assert v(A, A, 64, A + 2, 4, 64, NULL) == 5                    # out not 16-byte aligned
     assert v(A, A, 64, NULL, 4, 64, NULL) == 1

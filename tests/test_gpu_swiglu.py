@@ -112,6 +112,25 @@ def test_swiglu_two_level(ap, dev, rows, dim, fused):
     check_nvfp4(pk.cpu().numpy(), sb[guard:guard + n], opk, osf, rows, dim, v.numpy(), "swiglu two-level", ts=ots)
 
 
+def test_swiglu_two_level_16_byte_aligned_inputs(ap, dev):
+    # gate and up 16- but not 32-byte aligned: the two-load path of the kernels
+    rows, dim = 131, 1040
+    g = synth.bf16(synth.normal(31, 0, (rows, dim), 2.0))
+    u = synth.bf16(synth.normal(31, 1, (rows, dim), 1.0))
+    buf = torch.zeros((rows * 2 * dim + 8,), dtype=torch.bfloat16, device=dev)
+    x = buf[8:].view(rows, 2 * dim)
+    x[:, :dim] = g.to(dev)
+    x[:, dim:] = u.to(dev)
+    gate, up = x[:, :dim], x[:, dim:]
+    assert gate.data_ptr() % 32 == 16
+    pk, sf, ts = ap.swiglu_quant_nvfp4_2level_bf16(gate, up)
+    opk, osf, ots = oracle.swiglu_quant_nvfp4_2level(_bits(g), _bits(u))
+    assert float(ts.cpu()[0]) == ots
+    v = torch.from_numpy(oracle.swiglu_values(_bits(g), _bits(u)).view(np.int16)).view(torch.bfloat16).double()
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, v.numpy(), "swiglu 16-byte aligned", ts=ots)
+    _values_case(ap, dev, g, u, True)
+
+
 def test_swiglu_two_level_graph_and_workspace_reuse(ap, dev):
     rows, dim = 257, 7168
     g = synth.bf16(synth.normal(21, 0, (rows, dim), 2.0)).to(dev)
