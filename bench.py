@@ -124,6 +124,12 @@ def alg_bytes(name: str, w) -> int:
     raise KeyError(name)
 
 
+def launches_per_call(name: str) -> int:
+    """Kernels one call of the producer launches: the two-level producers clear
+    their word, then run the maximum and the quantising pass."""
+    return 3 if name.startswith("nvfp4_2level") else 1
+
+
 class DeviceOp:
     """Inputs resident on the device, outputs preallocated, one call = one launch."""
 
@@ -454,6 +460,29 @@ def run_ours(args, rank, world, local_rank):
         per_op_graphs.append((o, g, n, copies, nsets))
     barrier()
 
+    # Copy reference per producer: a graph of the same number of back-to-back
+    # SM copy kernels (torch's vectorised elementwise int32 "+ 0") that move the
+    # producer's algorithmic bytes (read half, write half) over rotating buffers
+    # (> 3x L2), timed the same way: the bandwidth a plain streaming kernel of
+    # that size reaches on this GPU, launch ramp and drain included.
+    copy_graphs = []
+    for o in ops + extra_ops:
+        words = max(4, (o.bytes // 8) // 4 * 4)
+        nsets = max(2, -(-3 * l2 // (8 * words)))
+        bufs = [(torch.zeros(words, dtype=torch.int32, device=dev), torch.empty(words, dtype=torch.int32, device=dev))
+                for _ in range(nsets)]
+        g = torch.cuda.CUDAGraph()
+        n = args.per_op_launches
+        with torch.cuda.stream(stream):
+            for src, dst in bufs:
+                torch.add(src, 0, out=dst)
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    torch.add(bufs[i % nsets][0], 0, out=bufs[i % nsets][1])
+            g.replay()
+        copy_graphs.append((g, n, bufs))
+    barrier()
+
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = vis.split(",")[local_rank] if vis else str(local_rank)
@@ -477,6 +506,16 @@ def run_ours(args, rank, world, local_rank):
                 e1.record(stream)
                 evs.append((e0, e1))
             op_events.append(evs)
+        copy_events = []
+        for g, n, _ in copy_graphs:
+            evs = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                evs.append((e0, e1))
+            copy_events.append(evs)
     barrier()
     clocks.mark("t1")
     clocks.stop()
@@ -484,8 +523,9 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = elapsed_ms / steps
     value = job_gbs(step_bytes, world, ms_per_step)
     args.steps = steps
-    launches = len(ops) * steps + sum(n * 3 for _, _, n, _, _ in per_op_graphs)
-    del per_op_graphs
+    launches = sum(launches_per_call(o.name) for o in ops) * steps + \
+        sum(launches_per_call(o.name) * n * 3 for o, _, n, _, _ in per_op_graphs)
+    del per_op_graphs, copy_graphs
 
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs") if peaks else None
@@ -496,8 +536,10 @@ def run_ours(args, rank, world, local_rank):
         n = args.per_op_launches
         us = statistics.median(e0.elapsed_time(e1) for e0, e1 in op_events[i]) * 1e3 / n
         gbs = o.bytes / (us * 1e-6) / 1e9
+        copy_us = statistics.median(e0.elapsed_time(e1) for e0, e1 in copy_events[i]) * 1e3 / n
         per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
                        "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4),
+                       "copy_us": round(copy_us, 3), "frac_of_copy": round(copy_us / us, 4),
                        "in_step": i < len(ops)})
     dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])  # largest share of the step
     d = per_op[dom]
@@ -520,7 +562,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline, "per_op": per_op, "e2e": e2e, "chain": chain,
         "gpu_launches": launches, "clocks": clocks.summary(),
         "timing": ("step: CUDA graph of %d steps replayed %d times; per_op: graph of %d back-to-back calls per "
-                   "producer over rotating buffers > 3x L2, median of 3 replays" % (M, R, args.per_op_launches)),
+                   "producer over rotating buffers > 3x L2, median of 3 replays; copy_us: the same for a streaming copy "
+                   "kernel (torch int32 add of 0) moving the producer's algorithmic bytes, frac_of_copy = copy_us / us_per_call"
+                   % (M, R, args.per_op_launches)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
