@@ -145,7 +145,7 @@ class DeviceOp:
             self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
                         torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev),
                         torch.empty((1,), dtype=torch.float32, device=dev),
-                        torch.zeros((ap.WORKSPACE_2LEVEL_BYTES,), dtype=torch.uint8, device=dev))
+                        torch.zeros((ap.workspace_2level_bytes(R),), dtype=torch.uint8, device=dev))
         elif name.startswith("nvfp4"):
             self.out = (torch.empty((R, D // 2), dtype=torch.uint8, device=dev),
                         torch.empty((ap.swizzled_sf_size(R, D),), dtype=torch.uint8, device=dev))

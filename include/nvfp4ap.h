@@ -65,9 +65,15 @@ enum nvfp4ap_status {
 
 #define NVFP4AP_MAX_DIM 32768
 
-/* Bytes of the caller-owned device workspace of the two-level NVFP4
- * producers (one word; 4-byte aligned). */
-#define NVFP4AP_2LEVEL_WORKSPACE_BYTES 4
+/* Bytes of the caller-owned device workspace of the two-level LayerNorm
+ * NVFP4 producers for `rows` rows: the maximum word, padding to 16 bytes, then
+ * one 16-byte slot per row where the maximum pass keeps the row's statistics
+ * for the quantising pass (16-byte aligned).  The SwiGLU producer uses the
+ * word only (4 bytes, 4-byte aligned). */
+#define NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows) (16 + 16 * (int64_t)(rows))
+/* The same as a function (for callers that cannot use the macro); -1 for
+ * rows < 0 or a size past INT64_MAX. */
+int64_t nvfp4ap_2level_workspace_bytes(int64_t rows);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvfp4ap_status_string(int status);
@@ -257,10 +263,11 @@ int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* s
  * approximate reciprocal.  Outputs: packed and sf_swizzled as for the
  * single-level producers, and *tensor_scale = ts (device fp32, 4-byte
  * aligned) -- the dequantised value is e2m1 * decode(s) * ts.
- * workspace: caller-owned device memory of NVFP4AP_2LEVEL_WORKSPACE_BYTES,
- * 4-byte aligned, cleared and used by the call (two calls on concurrent
- * streams need two workspaces).  Three kernels on `stream`: a clear of the
- * workspace, the maximum pass, the quantising pass (graph-capturable). */
+ * workspace: caller-owned device memory of NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows)
+ * bytes, 16-byte aligned (NVFP4AP_ERR_ALIGN), cleared and used by the call
+ * (two calls on concurrent streams need two workspaces); a smaller buffer is
+ * written past its end.  Three kernels on `stream`: a clear of the word, the
+ * maximum pass, the quantising pass (graph-capturable). */
 int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed, void* sf_swizzled,
                                                  float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
                                                  nvfp4ap_stream_t stream);
@@ -277,14 +284,15 @@ int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, const int32_t* seg
 /* SwiGLU -> two-level NVFP4 (h3-blackwell-runtime compare page,
  * NVFP4_SWIGLU_FUSION_DESIGN.md: both bf16 boundaries kept):
  *   v = bf16(bf16(silu(gate)) * up),  silu(g) = g / (1 + exp(-g)),
- * the silu boundary taken on the binary32 value of silu (the library
- * recomputes in double the few elements its fast path cannot decide), then
- * the two-level contract above on v (no LayerNorm).  gate, up: device
+ * the silu boundary taken on the binary32 value of silu (the library takes
+ * bf16(binary32(silu(g))) from a table computed in float64 for all 65,536 bf16
+ * gate patterns), then the two-level contract above on v (no LayerNorm).  gate, up: device
  * (rows, dim) bf16 with the common row stride ld (elements): two tensors, or
  * the halves of one (rows, 2*dim) tensor (up = gate + dim, ld = 2*dim).  dim %
  * 16 == 0, ld >= dim, ld % 8 == 0 and rows * (dim / 8) < 2^32 (NVFP4AP_ERR_DIM /
  * _SHAPE), gate and up 16-byte aligned (32-byte aligned with ld % 16 == 0 takes
- * 256-bit loads).  Outputs and workspace as for the two-level producers. */
+ * 256-bit loads).  Outputs as for the two-level producers; workspace: the
+ * maximum word only, 4 bytes, 4-byte aligned. */
 int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* up, int64_t ld, void* packed, void* sf_swizzled,
                                    float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
                                    nvfp4ap_stream_t stream);

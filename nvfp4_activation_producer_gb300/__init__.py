@@ -33,7 +33,8 @@ __all__ = [
     "ada_layer_norm_quant_nvfp4_2level_seg_bf16",
     "swiglu_quant_nvfp4_2level_bf16",
     "swiglu_bf16",
-    "WORKSPACE_2LEVEL_BYTES",
+    "workspace_2level_bytes",
+    "SWIGLU_WORKSPACE_BYTES",
     "layer_norm_no_affine_quant_nvfp4_swizzled_bf16",
     "adaln_modulation6_bf16",
     "swizzled_sf_size",
@@ -46,7 +47,16 @@ LIB_PATH = _build.LIB
 
 OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT, ERR_SCRATCH = range(10)
 MAX_DIM = 32768
-WORKSPACE_2LEVEL_BYTES = 4
+SWIGLU_WORKSPACE_BYTES = 4  # the SwiGLU two-level producer keeps only the maximum word
+
+
+def workspace_2level_bytes(rows: int) -> int:
+    """Bytes of the workspace of the two-level LayerNorm producers for `rows`
+    rows: the maximum word (padded to 16 bytes) and a 16-byte statistics slot
+    per row (the C ABI's NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows))."""
+    if rows < 0:
+        raise ValueError("rows must be >= 0")
+    return 16 + 16 * rows
 
 
 class NvFp4ApError(RuntimeError):
@@ -111,6 +121,8 @@ def _load() -> ctypes.CDLL:
     L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16.argtypes = [p, f32, p, p, i64, i64, p]
     L.swizzled_sf_size.restype = i64
     L.swizzled_sf_size.argtypes = [i64, i64]
+    L.nvfp4ap_2level_workspace_bytes.restype = i64
+    L.nvfp4ap_2level_workspace_bytes.argtypes = [i64]
     L.adaln_modulation6_bf16.restype = i32
     L.adaln_modulation6_bf16.argtypes = [p, p, ctypes.POINTER(ctypes.c_void_p), i64, i64, i64, p]
     _lib = L
@@ -383,16 +395,18 @@ def ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(x, seg_idx, seg_scale, seg_shif
     return packed, sf_swizzled
 
 
-def _twolevel_extra(tensor_scale, workspace, dev):
+def _twolevel_extra(tensor_scale, workspace, dev, need: int):
+    """tensor_scale (1,) fp32 and a workspace of at least `need` bytes,
+    16-byte aligned; allocated when None."""
     if tensor_scale is None:
         tensor_scale = torch.empty((1,), dtype=torch.float32, device=dev)
     else:
         _scalar(tensor_scale, "tensor_scale", dev)
     if workspace is None:
-        workspace = torch.empty((WORKSPACE_2LEVEL_BYTES,), dtype=torch.uint8, device=dev)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     elif (not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or workspace.device != dev or
-          workspace.numel() * workspace.element_size() < WORKSPACE_2LEVEL_BYTES):
-        raise ValueError(f"workspace must be a CUDA tensor of at least {WORKSPACE_2LEVEL_BYTES} bytes on {dev}")
+          not workspace.is_contiguous() or workspace.numel() * workspace.element_size() < need):
+        raise ValueError(f"workspace must be a contiguous CUDA tensor of at least {need} bytes on {dev}")
     return tensor_scale, workspace
 
 
@@ -401,7 +415,7 @@ def layer_norm_no_affine_quant_nvfp4_2level_bf16(x, eps: float = 1e-5, packed=No
     """LayerNorm (no affine) -> two-level NVFP4: (packed, sf_swizzled, tensor_scale)."""
     rows, dim, dev = _x(x)
     packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
-    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev, workspace_2level_bytes(rows))
     rc = _load().layer_norm_no_affine_quant_nvfp4_2level_bf16(_ptr(x), eps, _ptr(packed), _ptr(sf_swizzled),
                                                               _ptr(tensor_scale), _ptr(workspace), rows, dim,
                                                               _stream(dev))
@@ -416,7 +430,7 @@ def ada_layer_norm_quant_nvfp4_2level_bf16(x, scale, shift, eps: float = 1e-5, p
     _need(scale, "scale", torch.bfloat16, (dim,), dev)
     _need(shift, "shift", torch.bfloat16, (dim,), dev)
     packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
-    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev, workspace_2level_bytes(rows))
     rc = _load().ada_layer_norm_quant_nvfp4_2level_bf16(_ptr(x), _ptr(scale), _ptr(shift), eps, _ptr(packed),
                                                         _ptr(sf_swizzled), _ptr(tensor_scale), _ptr(workspace),
                                                         rows, dim, _stream(dev))
@@ -430,7 +444,7 @@ def ada_layer_norm_quant_nvfp4_2level_seg_bf16(x, seg_idx, seg_scale, seg_shift,
     rows, dim, dev = _x(x)
     nseg = _seg(seg_idx, seg_scale, seg_shift, rows, dim, dev)
     packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
-    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev, workspace_2level_bytes(rows))
     rc = _load().ada_layer_norm_quant_nvfp4_2level_seg_bf16(_ptr(x), _ptr(seg_idx), _ptr(seg_scale),
                                                             _ptr(seg_shift), nseg, eps, _ptr(packed),
                                                             _ptr(sf_swizzled), _ptr(tensor_scale), _ptr(workspace),
@@ -471,7 +485,7 @@ def swiglu_quant_nvfp4_2level_bf16(gate, up, packed=None, sf_swizzled=None, tens
     contiguous (rows, 2*dim) tensor."""
     rows, dim, ld, dev = _gate_up(gate, up)
     packed, sf_swizzled = _nvfp4_outs(packed, sf_swizzled, rows, dim, dev)
-    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev)
+    tensor_scale, workspace = _twolevel_extra(tensor_scale, workspace, dev, SWIGLU_WORKSPACE_BYTES)
     rc = _load().swiglu_quant_nvfp4_2level_bf16(_ptr(gate), _ptr(up), ld, _ptr(packed), _ptr(sf_swizzled),
                                                 _ptr(tensor_scale), _ptr(workspace), rows, dim, _stream(dev))
     _raise("swiglu_quant_nvfp4_2level_bf16", rc)

@@ -285,8 +285,10 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   if (!a.x || !a.out || !a.sf || !a.tensor_scale || !a.amax_ws) return NVFP4AP_ERR_NULL;
   if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
   if (mod == MOD_SEG && (rc = check_seg(a)) != NVFP4AP_OK) return rc;
-  if (!aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.tensor_scale, 4) || !aligned(a.amax_ws, 4))
+  if (!aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.tensor_scale, 4) || !aligned(a.amax_ws, 16))
     return NVFP4AP_ERR_ALIGN;
+  // the workspace's statistics slots follow the word (16 bytes in)
+  a.row_stats = reinterpret_cast<float*>(reinterpret_cast<char*>(a.amax_ws) + 16);
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
   // default (and NVFP4AP_KERNEL=5): the block-per-lane kernels -- persistent,
   // one atomic per CTA in the maximum pass -- where they apply (measured on
@@ -647,6 +649,11 @@ NVFP4AP_EXPORT int swiglu_bf16(const void* gate, const void* up, int64_t ld, voi
   const int sms = sm_count();
   if (sms <= 0) return NVFP4AP_ERR_LAUNCH;
   return finish(launch_swiglu_values(gate, up, ld, rows, dim, out, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+NVFP4AP_EXPORT int64_t nvfp4ap_2level_workspace_bytes(int64_t rows) {
+  if (rows < 0 || rows > (INT64_MAX - 16) / 16) return -1;
+  return NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows);
 }
 
 NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {

@@ -59,6 +59,8 @@ struct LnArgs {
   int64_t nseg;
   unsigned int* amax_ws;      // two-level: one device word (the tensor's largest |v| as fp32 bits)
   float* tensor_scale;        // two-level: device fp32 output
+  float* row_stats;           // two-level: (rows,) float4 K, mean - K, rstd, 0 per row (written by the
+                              // block-per-lane maximum pass; nullptr: not kept)
   float eps;
   void* out;              // FP8: (rows, dim) e4m3; NVFP4: packed (rows, dim/2)
   void* sf;               // NVFP4: swizzled scales

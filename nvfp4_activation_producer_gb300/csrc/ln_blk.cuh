@@ -268,6 +268,11 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
     const float m1 = s.x * inv_d;  // mean - K
     const float var = fmaxf(fmaf(s.y, inv_d, -m1 * m1), 0.f);
     const float rstd = rsqrtf(var + a.eps);
+    if constexpr (KIND == BK_AMAX) {
+      // the row's statistics for a flat quantising pass (the same fp32 values)
+      if (a.row_stats != nullptr && t == 0)
+        reinterpret_cast<float4*>(a.row_stats)[row] = make_float4(K, m1, rstd, 0.f);
+    }
     // y = (x - K) * A + B (then * G + H): A = rstd, B = -(mean - K) * rstd
     // (FP8 without modulation: both times 1/act_scale)
     const float A = (KIND == BK_FP8 && MOD == MOD_NONE) ? rstd * inv_act : rstd;

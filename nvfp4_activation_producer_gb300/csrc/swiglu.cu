@@ -22,14 +22,14 @@
 // Work items are 16-element blocks (two-level passes) or 8-element chunks
 // (materialised values) in one flat grid-stride loop; an item's row comes
 // from a multiply-high division by the invariant items-per-row count
-// (Granlund and Montgomery's unsigned division by invariant integers), so the
-// loop carries no 64-bit division.  In the two-level passes a lane owns a
-// whole NVFP4 block: its gate and up are two 32-byte reads (one 256-bit load
-// each when both are 32-byte aligned), and its maximum, scale and 16 codes are
-// computed once, with no shuffle.  Two launches after a clear of the caller's
+// (divide.cuh), so the loop carries no 64-bit division.  In the two-level
+// passes a lane owns a whole NVFP4 block: its gate and up are two 32-byte
+// reads (one 256-bit load each when both are 32-byte aligned), and its
+// maximum, scale and 16 codes are computed once, with no shuffle.  Two launches after a clear of the caller's
 // word: the maximum pass (a running maximum per thread, one atomic per CTA)
 // and the quantising pass.
 #include "device.cuh"
+#include "divide.cuh"
 #include "kernels.h"
 
 namespace nvfp4ap {
@@ -56,32 +56,6 @@ __device__ __forceinline__ uint32_t swiglu_pair(uint32_t g, uint32_t u) {
   return f2_to_bf16x2(mul2(bf16x2_to_f2(silu_bf16x2(g)), bf16x2_to_f2(u)));
 }
 
-// Unsigned 32-bit division by an invariant d >= 1 (Granlund and Montgomery,
-// "Division by invariant integers using multiplication", 1994, the N = 32
-// unsigned case): with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
-// t = mulhi(m, n): n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) for
-// every n < 2^32.
-struct Div32 {
-  uint32_t d, m;
-  int sh1, sh2;
-};
-
-Div32 make_div(uint32_t d) {
-  int l = 0;
-  while (l < 32 && ((uint64_t)1 << l) < d) ++l;
-  Div32 v;
-  v.d = d;
-  v.m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << l) - d)) / d + 1);
-  v.sh1 = l < 1 ? l : 1;
-  v.sh2 = l - 1 > 0 ? l - 1 : 0;
-  return v;
-}
-
-__device__ __forceinline__ uint32_t div32(uint32_t n, const Div32& v) {
-  const uint32_t t = __umulhi(v.m, n);
-  return (t + ((n - t) >> v.sh1)) >> v.sh2;
-}
-
 // 32 contiguous bytes (16 bf16 values), read once
 template <bool V8>
 __device__ __forceinline__ void ld_block16(const uint16_t* p, uint32_t (&w)[8]) {
@@ -105,7 +79,7 @@ struct SwArgs {
   float* tensor_scale;
   unsigned int* amax_ws;
   uint32_t items;  // rows * items per row
-  Div32 per_row;   // items per row (16-element blocks or 8-element chunks)
+  InvDiv per_row;  // items per row (16-element blocks or 8-element chunks)
 };
 
 __global__ void sw_clear_kernel(unsigned int* w) {
@@ -126,7 +100,7 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_kernel(const SwArgs a) {
     if (blockIdx.x == 0 && threadIdx.x == 0) a.tensor_scale[0] = ts;
   }
   for (uint32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < a.items; n += stride) {
-    const uint32_t r = div32(n, a.per_row), b = n - r * (uint32_t)nblk;
+    const uint32_t r = inv_div(n, a.per_row), b = n - r * (uint32_t)nblk;
     const int64_t off = (int64_t)r * a.ld + (int64_t)b * 16;
     uint32_t gw[8], uw[8], vb[8];
     ld_block16<V8>(a.gate + off, gw);
@@ -209,7 +183,7 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_values_kernel(const SwArgs 
   const uint32_t nch = (uint32_t)(a.dim >> 3);
   const uint32_t stride = gridDim.x * blockDim.x;
   for (uint32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < a.items; n += stride) {
-    const uint32_t r = div32(n, a.per_row), j = n - r * nch;
+    const uint32_t r = inv_div(n, a.per_row), j = n - r * nch;
     const int64_t off = (int64_t)r * a.ld + (int64_t)j * 8;
     const uint4 g = ld_once_v4(a.gate + off), u = ld_once_v4(a.up + off);
     st_stream_v4(out + (int64_t)r * a.dim + (int64_t)j * 8,
@@ -239,7 +213,7 @@ cudaError_t launch_swiglu_2level(const void* gate, const void* up, int64_t ld, i
   const uint32_t nblk = (uint32_t)(dim / 16);
   SwArgs a{static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up), ld, rows, dim,
            static_cast<uint8_t*>(packed), static_cast<uint8_t*>(sf), tensor_scale, ws,
-           (uint32_t)(rows * nblk), make_div(nblk)};
+           (uint32_t)(rows * nblk), make_inv_div(nblk)};
   const bool v8 = (reinterpret_cast<uintptr_t>(gate) % 32 == 0) && (reinterpret_cast<uintptr_t>(up) % 32 == 0) &&
                   (ld % 16 == 0);
   cudaError_t e = launch_maybe_pdl(sw_clear_kernel, dim3(1), dim3(1), 0, st, ws);
@@ -256,7 +230,7 @@ cudaError_t launch_swiglu_values(const void* gate, const void* up, int64_t ld, i
   if (!swiglu_items_fit(rows, dim)) return cudaErrorInvalidValue;
   const uint32_t nch = (uint32_t)(dim / 8);
   SwArgs a{static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up), ld, rows, dim, nullptr, nullptr,
-           nullptr, nullptr, (uint32_t)(rows * nch), make_div(nch)};
+           nullptr, nullptr, (uint32_t)(rows * nch), make_inv_div(nch)};
   return launch_maybe_pdl(swiglu_values_kernel, dim3(sw_grid(swiglu_values_kernel, sms, a.items)), dim3(kSwThreads),
                           0, st, a, static_cast<uint16_t*>(out));
 }

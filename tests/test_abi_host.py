@@ -39,7 +39,7 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 22
+    assert len(declared) == 23
 
 
 def test_status_strings_and_version(lib):
@@ -155,6 +155,9 @@ def test_seg_and_two_level_argument_errors(lib):
     assert n(A, 1e-5, A, A, A, NULL, 4, 64, NULL) == 1             # null workspace
     assert n(A, 1e-5, A, A, A + 2, A, 4, 64, NULL) == 5            # tensor scale misaligned
     assert n(A, 1e-5, A, A, A, A + 1, 4, 64, NULL) == 5            # workspace misaligned
+    assert n(A, 1e-5, A, A, A, A + 8, 4, 64, NULL) == 5            # workspace not 16-byte aligned
+    ws = L.nvfp4ap_2level_workspace_bytes
+    assert ws(0) == 16 and ws(37810) == 16 + 16 * 37810 and ws(-1) == -1 and ws(1 << 62) == -1
     assert n(A, 1e-5, A, A, A, A, 4, 72, NULL) == 3
     assert n(NULL, 1e-5, NULL, NULL, NULL, NULL, 0, 64, NULL) == 0
     b = L.ada_layer_norm_quant_nvfp4_2level_bf16  # x, scale, shift, eps, packed, sf, ts, ws, rows, dim

@@ -155,11 +155,24 @@ def test_out_of_range_segment_index(ap, dev):
     check_fp8(got[keep], oracle.ln_quant_fp8(x[keep], 0.025, oracle.MOD_SEG, **src), 0.025, "valid rows")
 
 
+def test_two_level_workspace_too_small_is_rejected(ap, dev):
+    # the binding checks the statistics slots' size (the C ABI cannot)
+    w = synth.nvfp4_ln(64, 256, seed=2)
+    x = w.inputs["x"].to(dev)
+    small = torch.zeros(ap.workspace_2level_bytes(63), dtype=torch.uint8, device=dev)
+    with pytest.raises(ValueError):
+        ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x, workspace=small)
+    ok = torch.zeros(ap.workspace_2level_bytes(64), dtype=torch.uint8, device=dev)
+    a = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x, workspace=ok)
+    b = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x)
+    assert all(torch.equal(u, v) for u, v in zip(a, b))
+
+
 def test_two_level_workspace_reuse_and_graph(ap, dev):
     w = synth.segmented(515, 5376, seed=11)
     d = {k: v.to(dev) for k, v in w.inputs.items()}
     rows, dim = w.rows, w.dim
-    ws = torch.zeros(8, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ap.workspace_2level_bytes(rows), dtype=torch.uint8, device=dev)
     outs = []
     for _ in range(2):
         outs.append(ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"],
