@@ -13,7 +13,8 @@ modulation for that row plus the device fault word), workspace reuse, a CUDA
 graph capture of the three operations.  Every case runs on the default
 kernels (block-per-lane for the two-level forms, register row kernels for the
 single-level segmented forms), on the register row kernels
-(NVFP4AP_KERNEL=3) and on the block-per-lane kernels (NVFP4AP_KERNEL=5).
+(NVFP4AP_KERNEL=3), on the block-per-lane kernels (NVFP4AP_KERNEL=5) and with
+the warp-per-row maximum pass forced at every size (NVFP4AP_2L_AMAX=1).
 """
 import numpy as np
 import pytest
@@ -28,12 +29,16 @@ pytestmark = pytest.mark.gpu
 SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (130, 4096), (5, 32768), (257, 1536)]
 
 
-@pytest.fixture(autouse=True, params=["auto", "rows", "blk"])
+@pytest.fixture(autouse=True, params=["auto", "rows", "blk", "warp"])
 def family(request, monkeypatch):
     if request.param == "auto":
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
-        monkeypatch.setenv("NVFP4AP_KERNEL", "5" if request.param == "blk" else "3")
+        monkeypatch.setenv("NVFP4AP_KERNEL", "3" if request.param == "rows" else "5")
+    if request.param == "warp":
+        monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")  # the warp-per-row maximum pass at every size
+    else:
+        monkeypatch.delenv("NVFP4AP_2L_AMAX", raising=False)
     monkeypatch.delenv("NVFP4AP_BLK_GRID", raising=False)
     return request.param
 
@@ -202,8 +207,8 @@ def test_two_level_workspace_reuse_and_graph(ap, dev):
 def test_two_level_many_rows_per_group(ap, dev, family, kind, monkeypatch):
     # block-per-lane kernels on 1 and 3 CTAs: each row group walks many rows and
     # the maximum pass reduces them in one CTA
-    if family == "rows":
-        pytest.skip("grid limit of the block-per-lane kernels")
+    if family in ("rows", "warp"):
+        pytest.skip("grid limit of the block-per-lane row-group kernels")
     for ctas, dim in ((1, 272), (3, 3072)):
         monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
         rows = 3000
