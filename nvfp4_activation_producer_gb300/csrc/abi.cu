@@ -268,6 +268,14 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
       return finish(launch_ln_blk(a, nvfp4, MOD_SEG, bs, sms, st));
     }
   }
+  // FP8, many rows: the warp-per-row kernel (NVFP4AP_SEG_WARP=1 forces it,
+  // -1 turns it off)
+  if (!nvfp4 && env_int("NVFP4AP_KERNEL") != 5 && env_int("NVFP4AP_SEG_WARP") >= 0 &&
+      ln_blk_supported(BLK_FP8, MOD_SEG, a.dim, a.nseg) && aligned(a.x, 32) && aligned(a.out, 16)) {
+    const int sms = sm_count();
+    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || a.rows >= ln_warp_rows_min(sms)))
+      return finish(launch_ln_warp_rows_fp8(a, MOD_SEG, sms, st));
+  }
   RowShape s{};
   if (!pick_rows(MOD_SEG, a.dim, &s)) return NVFP4AP_ERR_DIM;
   const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;

@@ -119,6 +119,12 @@ cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int 
 // two-level NVFP4 on the block-per-lane kernels: clears a.amax_ws, maximum
 // pass, quantising pass; mod MOD_NONE, MOD_BCAST or MOD_SEG
 cudaError_t launch_ln_2level_blk(const LnArgs& a, int mod, BlkShape s, int sms, cudaStream_t st);
+// Warp-per-row FP8 producers (ln_blk.cuh): each warp sweeps its rows twice
+// (sums, then codes from the blocks read again through L1/L2); for at least
+// ln_warp_rows_min(sms) rows; mod MOD_NONE, MOD_BCAST or MOD_SEG (tables as
+// for the block-per-lane kernels).
+int64_t ln_warp_rows_min(int sms);
+cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStream_t st);
 // read and clear the segment-index fault words of the two translation units
 cudaError_t take_blk_seg_fault(unsigned int* fault);
 cudaError_t take_blk2l_seg_fault(unsigned int* fault);

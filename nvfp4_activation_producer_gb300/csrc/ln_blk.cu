@@ -1,7 +1,8 @@
 // ln_blk.cu -- instances of the block-per-lane kernel template (ln_blk.cuh)
 // for the single-level producers: FP8 (no modulation, broadcast bf16, modfp8,
 // AWQ, segmented) and NVFP4 (no modulation, broadcast bf16, modfp8,
-// segmented), and the shape choice.
+// segmented), and the shape choice; the warp-per-row FP8 kernels (no
+// modulation, broadcast bf16, segmented) for many rows.
 #include "ln_blk.cuh"
 
 namespace nvfp4ap {
@@ -58,6 +59,17 @@ cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int 
     case MOD_MODFP8: return launch_blk_bpt<BK_FP8, MOD_MODFP8>(a, s, sms, st);
     case MOD_AWQ: return launch_blk_bpt<BK_FP8, MOD_AWQ>(a, s, sms, st);
     case MOD_SEG: return launch_blk_bpt<BK_FP8, MOD_SEG>(a, s, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int64_t ln_warp_rows_min(int sms) { return warp_rows_min(sms); }
+
+cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStream_t st) {
+  switch (mod) {
+    case MOD_NONE: return launch_warp_rows<BK_FP8, MOD_NONE>(a, sms, st);
+    case MOD_BCAST: return launch_warp_rows<BK_FP8, MOD_BCAST>(a, sms, st);
+    case MOD_SEG: return launch_warp_rows<BK_FP8, MOD_SEG>(a, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

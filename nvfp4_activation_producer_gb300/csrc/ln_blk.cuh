@@ -62,6 +62,7 @@ namespace {
 enum { BK_FP8 = 0, BK_NVFP4 = 1, BK_AMAX = 2, BK_NV2L = 3 };
 
 constexpr int kBlkThreads = 512;  // threads per CTA (row groups x threads per row)
+constexpr int kWarpRowThreads = 1024;  // warp-per-row kernels: 32 warps per CTA
 // dynamic shared memory the modulation tables may take (the static slots and
 // the 227 KB per-CTA limit leave room above it)
 constexpr int kBlkMaxSmem = 200 * 1024;
@@ -153,21 +154,13 @@ __host__ __device__ constexpr int64_t blk_tab_float4s(int mod, int64_t nblk, int
   return mod == MOD_NONE ? 0 : (mod == MOD_SEG ? (nseg + 1) * 8 * nblk : 8 * nblk);
 }
 
-template <int KIND, int MOD, int BPT, bool FULL>
-__global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, const float inv_d, const int tpr) {
-  extern __shared__ float4 gh[];    // modulation tables, chunk-major (see the file comment)
-  __shared__ float2 red[2][16][8];  // [row parity][row group][warp of the row]
-  __shared__ float redm[kBlkThreads / 32];
-  constexpr bool kNv = (KIND != BK_FP8);
-  const int ngrp = blockDim.x / tpr;
-  const int g = threadIdx.x / tpr, t = threadIdx.x - g * tpr;
-  const int lane = threadIdx.x & 31, wig = t >> 5, wpr = tpr >> 5;
+// The CTA's modulation tables in shared memory (G = 1 + scale and H = shift as
+// fp32, FP8: both times 1/act_scale, AWQ also times inv_s; chunk-major; a
+// segmented source: one table per segment, then the identity table).  Ends
+// with a barrier when there are tables.
+template <int KIND, int MOD>
+__device__ __forceinline__ void blk_tables(const LnArgs& a, float4* gh, int nblk, float inv_act) {
   const int64_t D = a.dim;
-  const int nblk = (int)(D >> 4);
-  pdl_enter();
-
-  float inv_act = 1.0f;
-  if constexpr (KIND == BK_FP8) inv_act = 1.0f / __ldg(a.act_scale);
   if constexpr (MOD == MOD_SEG) {
     // one table per segment, then the identity table (G = 1, H = 0; FP8: 1/act_scale, 0)
     const int nseg = (int)a.nseg;
@@ -205,6 +198,25 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
     }
     __syncthreads();
   }
+
+}
+
+template <int KIND, int MOD, int BPT, bool FULL>
+__global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, const float inv_d, const int tpr) {
+  extern __shared__ float4 gh[];    // modulation tables, chunk-major (see the file comment)
+  __shared__ float2 red[2][16][8];  // [row parity][row group][warp of the row]
+  __shared__ float redm[kBlkThreads / 32];
+  constexpr bool kNv = (KIND != BK_FP8);
+  const int ngrp = blockDim.x / tpr;
+  const int g = threadIdx.x / tpr, t = threadIdx.x - g * tpr;
+  const int lane = threadIdx.x & 31, wig = t >> 5, wpr = tpr >> 5;
+  const int64_t D = a.dim;
+  const int nblk = (int)(D >> 4);
+  pdl_enter();
+
+  float inv_act = 1.0f;
+  if constexpr (KIND == BK_FP8) inv_act = 1.0f / __ldg(a.act_scale);
+  blk_tables<KIND, MOD>(a, gh, nblk, inv_act);
 
   // two-level: the tensor scale from the maximum pass's word (read through L2)
   float ts = 1.0f;
@@ -364,6 +376,161 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
       if (m > 0.f) atomicMax(a.amax_ws, __float_as_uint(m));
     }
   }
+}
+
+// 16 bf16 values (32 contiguous bytes), allocated in L1: the row is read twice
+__device__ __forceinline__ void ld_block_l1(const uint16_t* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+// Warp-per-row kernel for many rows per warp (KIND BK_FP8, or BK_AMAX: the
+// maximum pass of the two-level contract): each warp takes rows w, w + W, ...
+// and sweeps a row twice -- the shifted sums (three 256-bit loads per lane in
+// flight, allocated in L1), then the blocks read again (L1 or L2) to write the
+// FP8 codes, or to take the staged values' maximum and store the row's
+// statistics for the flat quantising pass.  No row stays in registers and
+// warps never wait on each other, so 32 warps per SM stream rows
+// independently.  The maximum pass issues one atomic per CTA.
+template <int KIND, int MOD>
+__global__ void __launch_bounds__(kWarpRowThreads, 1) warp_rows_kernel(const LnArgs a, const float inv_d) {
+  extern __shared__ float4 gh[];
+  __shared__ float redm[kWarpRowThreads / 32];
+  const int lane = threadIdx.x & 31;
+  const int64_t D = a.dim;
+  const int nblk = (int)(D >> 4);
+  pdl_enter();
+  float inv_act = 1.0f;
+  if constexpr (KIND == BK_FP8) inv_act = 1.0f / __ldg(a.act_scale);
+  blk_tables<KIND, MOD>(a, gh, nblk, inv_act);
+
+  float run = 0.0f;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < a.rows; row += nw) {
+    const uint16_t* xr = a.x + row * D;
+    const float K = __uint_as_float((uint32_t)__ldg(xr) << 16);
+    const float2 nk = splat2(-K);
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    for (int b0 = lane; b0 < nblk; b0 += 96) {
+      uint32_t w[3][8];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        if (b0 + 32 * k < nblk) {
+          ld_block_l1(xr + (int64_t)(b0 + 32 * k) * 16, w[k]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[k][i] = 0u;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        if (b0 + 32 * k < nblk) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 d = add2(bf16x2_to_f2(w[k][i]), nk);
+            s1 = add2(s1, d);
+            s2 = fma2(d, d, s2);
+          }
+        }
+      }
+    }
+    float2 s = make_float2(s1.x + s1.y, s2.x + s2.y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s.x += __shfl_xor_sync(0xFFFFFFFFu, s.x, o);
+      s.y += __shfl_xor_sync(0xFFFFFFFFu, s.y, o);
+    }
+    const float m1 = s.x * inv_d;  // mean - K
+    const float var = fmaxf(fmaf(s.y, inv_d, -m1 * m1), 0.f);
+    const float rstd = rsqrtf(var + a.eps);
+    if (KIND == BK_AMAX && lane == 0) reinterpret_cast<float4*>(a.row_stats)[row] = make_float4(K, m1, rstd, 0.f);
+    const float4* tab = gh;
+    if constexpr (MOD == MOD_SEG) {
+      const int sg = __ldg(a.seg_idx + row);
+      const bool ok = sg >= 0 && sg < a.nseg;
+      if (!ok && lane == 0) atomicOr(&g_blk_seg_fault, 1u);
+      tab = gh + (int64_t)(ok ? sg : a.nseg) * 8 * nblk;
+    }
+    // the maximum pass: the same fp32 operations as the quantising pass
+    const float A = (KIND == BK_FP8 && MOD == MOD_NONE) ? rstd * inv_act : rstd;
+    const float2 A2 = splat2(A), B2 = splat2(-m1 * A);
+    for (int b = lane; b < nblk; b += 32) {
+      uint32_t w[8];
+      ld_block_l1(xr + (int64_t)b * 16, w);
+      float2 y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        y[i] = fma2(add2(bf16x2_to_f2(w[i]), nk), A2, B2);
+        if constexpr (MOD != MOD_NONE) {
+          const float4 G4 = tab[(i >> 1) * nblk + b], H4 = tab[(4 + (i >> 1)) * nblk + b];
+          y[i] = (i & 1) ? fma2(y[i], make_float2(G4.z, G4.w), make_float2(H4.z, H4.w))
+                         : fma2(y[i], make_float2(G4.x, G4.y), make_float2(H4.x, H4.y));
+        }
+      }
+      if constexpr (KIND == BK_FP8) {
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = f2_to_e4m3x2(y[i]);
+        st_stream_v4(reinterpret_cast<uint8_t*>(a.out) + row * D + (int64_t)b * 16,
+                     make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16)));
+      } else {
+        uint32_t vb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vb[i] = f2_to_bf16x2(y[i]);
+        run = fmaxf(run, block_amax(vb));
+      }
+    }
+  }
+  if constexpr (KIND == BK_AMAX) {
+    // the CTA's largest |v| (non-negative fp32: its bits order like the values)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) run = fmaxf(run, __shfl_xor_sync(0xFFFFFFFFu, run, o));
+    if (lane == 0) redm[threadIdx.x >> 5] = run;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = redm[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, redm[w]);
+      if (m > 0.f) atomicMax(a.amax_ws, __float_as_uint(m));
+    }
+  }
+}
+
+// Dynamic-memory limit of a kernel raised once per device (keyed by the
+// kernel itself: instances share their function-pointer type).
+inline bool flat_smem_limit(const void* k) {
+  struct Entry { const void* k; int dev; };
+  static Entry done[64];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (done[i].k == k && done[i].dev == dev) return true;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBlkMaxSmem) != cudaSuccess) return false;
+  if (n < 64) done[n++] = Entry{k, dev};
+  return true;
+}
+
+// rows from which the warp-per-row kernels give every warp of the grid
+// several (one 1024-thread CTA per SM)
+inline int64_t warp_rows_min(int sms) { return (int64_t)sms * (kWarpRowThreads / 32) * 4; }
+
+template <int KIND, int MOD>
+cudaError_t launch_warp_rows(const LnArgs& a, int sms, cudaStream_t st) {
+  auto k = warp_rows_kernel<KIND, MOD>;
+  const int64_t smem64 = blk_tab_float4s(MOD, a.dim / 16, a.nseg) * (int64_t)sizeof(float4);
+  if (smem64 > kBlkMaxSmem || !flat_smem_limit((const void*)k)) return cudaErrorInvalidValue;
+  const int smem = (int)smem64;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kWarpRowThreads, smem) != cudaSuccess || occ < 1)
+    return cudaErrorInvalidConfiguration;
+  int64_t grid = (int64_t)sms * occ;
+  const int64_t need = (a.rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+  if (grid > need) grid = need;
+  const float inv_d = (float)(1.0 / (double)a.dim);
+  return launch_maybe_pdl(k, dim3((unsigned)grid), dim3(kWarpRowThreads), (size_t)smem, st, a, inv_d);
 }
 
 // Resident CTAs per SM of an instance with `smem` bytes of dynamic shared

@@ -14,7 +14,8 @@ graph capture of the three operations.  Every case runs on the default
 kernels (block-per-lane for the two-level forms, register row kernels for the
 single-level segmented forms), on the register row kernels
 (NVFP4AP_KERNEL=3), on the block-per-lane kernels (NVFP4AP_KERNEL=5) and with
-the warp-per-row maximum pass forced at every size (NVFP4AP_2L_AMAX=1).
+the warp-per-row kernels forced at every size (NVFP4AP_2L_AMAX=1 for the
+two-level maximum pass, NVFP4AP_SEG_WARP=1 for the FP8 segmented producer).
 """
 import numpy as np
 import pytest
@@ -36,9 +37,13 @@ def family(request, monkeypatch):
     else:
         monkeypatch.setenv("NVFP4AP_KERNEL", "3" if request.param == "rows" else "5")
     if request.param == "warp":
-        monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")  # the warp-per-row maximum pass at every size
+        # the warp-per-row kernels at every size: the two-level maximum pass and
+        # the FP8 segmented producer
+        monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")
+        monkeypatch.setenv("NVFP4AP_SEG_WARP", "1")
     else:
         monkeypatch.delenv("NVFP4AP_2L_AMAX", raising=False)
+        monkeypatch.delenv("NVFP4AP_SEG_WARP", raising=False)
     monkeypatch.delenv("NVFP4AP_BLK_GRID", raising=False)
     return request.param
 
