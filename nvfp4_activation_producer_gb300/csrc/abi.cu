@@ -184,15 +184,28 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
   const int vec = vec8 ? 8 : 2;
 
-  // NVFP4AP_KERNEL: 0 auto (default: the TMA pipeline for the table form,
-  // the register row kernels otherwise -- the faster family for each form on
-  // GB300 at 2,520-32,768 rows), 1 warp-per-row TMA ring, 2 first register
+  // NVFP4AP_KERNEL: 0 auto (below), 1 warp-per-row TMA ring, 2 first register
   // kernel, 3 register row kernels for every form, 4 TMA pipeline for every
-  // form.  The ring and TMA kernels have no modfp8 / AWQ source: those run
+  // form, 5 block-per-lane persistent kernel, 8 one-row-per-CTA block-per-lane
+  // kernel.  The ring and TMA kernels have no modfp8 / AWQ source: those run
   // on the register kernels.
   int kernel = env_int("NVFP4AP_KERNEL");
-  if (kernel == 0) kernel = (mod == MOD_TABLE) ? 4 : 3;
+  // default: the one-row-per-CTA block-per-lane kernel for the layer norm
+  // form where the row fits it exactly (measured on GB300: 4096x3072 7.9 ->
+  // 7.55 us; for the broadcast sources it measured slower than the persistent
+  // broadcast kernel in the bench: 9.3 -> 10.0 us, modfp8 and AWQ more), the
+  // TMA pipeline for the table form, the register kernels for the rest
+  if (kernel == 0) kernel = (mod == MOD_NONE) ? 8 : (mod == MOD_TABLE) ? 4 : 3;
   if (kernel == 1 && (mod == MOD_MODFP8 || mod == MOD_AWQ)) kernel = 3;
+  if (kernel == 8) {
+    // one-row-per-CTA block-per-lane kernel where the row fits it exactly
+    // (the default for the layer norm form, see above), else the other defaults
+    RbShape rb{};
+    if (vec8 && (mod == MOD_NONE || mod_is_bcast(mod)) && aligned(a.x, 32) && aligned(a.out, 16) &&
+        pick_rowblk(a.dim, env_int("NVFP4AP_RB_BPT"), &rb))
+      return finish(launch_ln_rowblk(a, false, mod, rb, st));
+    kernel = (mod == MOD_TABLE) ? 4 : 3;
+  }
   if (kernel == 5) {
     // block-per-lane persistent kernel where it applies, else the default
     if (vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) && aligned(a.out, 16)) {
@@ -344,7 +357,7 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
     RbShape rb{};
     if ((mod == MOD_NONE || mod == MOD_BCAST || mod == MOD_MODFP8) && aligned(a.x, 32) &&
         pick_rowblk(a.dim, env_int("NVFP4AP_RB_BPT"), &rb))
-      return finish(launch_ln_rowblk(a, mod, rb, st));
+      return finish(launch_ln_rowblk(a, true, mod, rb, st));
     kernel = 3;
   }
   if (kernel == 5) {

@@ -129,15 +129,16 @@ cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStrea
 cudaError_t take_blk_seg_fault(unsigned int* fault);
 cudaError_t take_blk2l_seg_fault(unsigned int* fault);
 
-// One-row-per-CTA block-per-lane NVFP4 kernels (ln_rowblk.cu): `tpr` threads
-// per row (32..128, a multiple of 32), `bpt` 16-element blocks per thread
-// (2..4), rows exactly tpr * bpt blocks; mod MOD_NONE, MOD_BCAST or
-// MOD_MODFP8; x 32-byte aligned.  pick_rowblk: the shape for `dim` (forced_bpt > 0: only that one).
+// One-row-per-CTA block-per-lane kernels (ln_rowblk.cu), NVFP4 and FP8: `tpr`
+// threads per row (64..128, a multiple of 32), `bpt` 16-element blocks per
+// thread (2..4), rows exactly tpr * bpt blocks; mod MOD_NONE, MOD_BCAST,
+// MOD_MODFP8 (and MOD_AWQ for FP8); x 32-byte aligned, FP8 out 16-byte
+// aligned.  pick_rowblk: the shape for `dim` (forced_bpt > 0: only that one).
 struct RbShape {
   int tpr, bpt;
 };
 bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s);
-cudaError_t launch_ln_rowblk(const LnArgs& a, int mod, RbShape s, cudaStream_t st);
+cudaError_t launch_ln_rowblk(const LnArgs& a, bool nvfp4, int mod, RbShape s, cudaStream_t st);
 
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);

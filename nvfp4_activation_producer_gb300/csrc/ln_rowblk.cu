@@ -1,11 +1,13 @@
-// ln_rowblk.cu -- one-row-per-CTA, block-per-lane NVFP4 producers for sm_103a.
+// ln_rowblk.cu -- one-row-per-CTA, block-per-lane LayerNorm producers (NVFP4
+// and FP8 e4m3fn) for sm_103a.
 //
 // Operations (adaptive-layernorm-producers README, "Available Functions",
 // "Tensor Contract"; NVFP4 encoding facts from the h3-blackwell-runtime
 // compare page):
 //   y = (x - mean) * rstd * (1 + scale) + shift, rstd = 1/sqrt(var + eps),
 //   scale/shift: none, bf16 broadcast vectors, or e4m3 vectors times fp32 deq
-//   scalars (modfp8)
+//   scalars (modfp8); AWQ (FP8) also multiplies y by inv_s
+//   FP8:   out = e4m3fn(y / act_scale), nearest-even, saturating
 //   NVFP4: v = bf16(y); per 16 elements s = e4m3fn(amax/6); e2m1 codes of
 //          v/s, two per byte (low nibble first); s in the 128x4 tiled layout
 //          with zero padding.
@@ -33,7 +35,7 @@ __device__ __forceinline__ void rb_load(const uint16_t* p, uint32_t (&w)[8]) {
                : "l"(p));
 }
 
-template <int MOD, int BPT, int TPR, int MINB>
+template <bool FP8, int MOD, int BPT, int TPR, int MINB>
 __global__ void __launch_bounds__(TPR, MINB) ln_rowblk_kernel(const LnArgs a, const float inv_d) {
   __shared__ float2 red[TPR / 32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -43,6 +45,7 @@ __global__ void __launch_bounds__(TPR, MINB) ln_rowblk_kernel(const LnArgs a, co
   pdl_enter();
 
   if (row >= a.rows) {
+    if constexpr (FP8) return;
     // rows past the end inside the last 128-row tile: zero scale bytes
     uint8_t* sfrow = reinterpret_cast<uint8_t*>(a.sf) + (row >> 7) * (int64_t)ct * 512 + (int)((row & 31) << 4) +
                      (int)(((row >> 5) & 3) << 2);
@@ -83,8 +86,40 @@ __global__ void __launch_bounds__(TPR, MINB) ln_rowblk_kernel(const LnArgs a, co
   const float m1 = s.x * inv_d;  // mean - K
   const float var = fmaxf(fmaf(s.y, inv_d, -m1 * m1), 0.f);
   const float rstd = rsqrtf(var + a.eps);
-  const float2 A2 = splat2(rstd), B2 = splat2(-m1 * rstd);
+  // y = (x - K) * A + B (then * G + H): A = rstd, B = -(mean - K) * rstd (FP8
+  // without modulation: both times 1/act_scale; with it: (..) * G + H, then
+  // times 1/act_scale, and inv_s for AWQ)
+  const float inv_act = FP8 ? 1.0f / __ldg(a.act_scale) : 1.0f;
+  const float A = (FP8 && MOD == MOD_NONE) ? rstd * inv_act : rstd;
+  const float2 A2 = splat2(A), B2 = splat2(-m1 * A), inv2 = splat2(inv_act);
   const float2 deq = source_deq<MOD>(a);
+  if constexpr (FP8) {
+    uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) + row * D;
+#pragma unroll
+    for (int k = 0; k < BPT; ++k) {
+      const int b = t + k * TPR;
+      uint32_t q[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        BcastCols<MOD, 8> bc;
+        AwqCols<8> aw;
+        if constexpr (MOD != MOD_NONE) bc.load(a, (int64_t)b * 16 + h * 8);
+        if constexpr (MOD == MOD_AWQ) aw.load(a, (int64_t)b * 16 + h * 8);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 y = fma2(add2(bf16x2_to_f2(w[k][h * 4 + i]), nk), A2, B2);
+          if constexpr (MOD != MOD_NONE) {
+            const float2 f = MOD == MOD_AWQ ? mul2(aw.mult(i), inv2) : inv2;
+            y = mul2(fma2(y, add2(bc.scale(i, deq), splat2(1.0f)), bc.shift(i, deq)), f);
+          }
+          q[h * 4 + i] = f2_to_e4m3x2(y);
+        }
+      }
+      st_stream_v4(orow + (int64_t)b * 16,
+                   make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16)));
+    }
+    return;
+  }
   uint8_t* prow = reinterpret_cast<uint8_t*>(a.out) + row * (D >> 1);
   uint8_t* sfrow = reinterpret_cast<uint8_t*>(a.sf) + (row >> 7) * (int64_t)ct * 512 + (int)((row & 31) << 4) +
                    (int)(((row >> 5) & 3) << 2);
@@ -126,18 +161,18 @@ __global__ void __launch_bounds__(TPR, MINB) ln_rowblk_kernel(const LnArgs a, co
   for (int c = nblk + t; c < padc; c += TPR) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
 }
 
-template <int MOD, int BPT, int TPR, int MINB>
+template <bool FP8, int MOD, int BPT, int TPR, int MINB>
 cudaError_t launch_rb(const LnArgs& a, cudaStream_t st) {
-  const int64_t rows_pad = (a.rows + 127) / 128 * 128;
+  const int64_t work = FP8 ? a.rows : (a.rows + 127) / 128 * 128;
   const float inv_d = (float)(1.0 / (double)a.dim);
-  return launch_maybe_pdl(ln_rowblk_kernel<MOD, BPT, TPR, MINB>, dim3((unsigned)rows_pad), dim3(TPR), 0, st, a,
+  return launch_maybe_pdl(ln_rowblk_kernel<FP8, MOD, BPT, TPR, MINB>, dim3((unsigned)work), dim3(TPR), 0, st, a,
                           inv_d);
 }
 
 // Resident CTAs per SM the registers are capped for (the fewest registers per
 // thread each shape compiles to without spills): 56 / 64 / 80 for two, three,
 // four blocks per lane; the broadcast source keeps its column words live and
-// takes 64 / 80 / 96.
+// takes 64 / 80 / 96 (AWQ: also inv_s).
 template <int MOD>
 constexpr int rb_minb(int bpt, int tpr) {
   const int regs = (MOD == MOD_NONE) ? (bpt == 2 ? 56 : bpt == 3 ? 64 : 80) : (bpt == 2 ? 64 : bpt == 3 ? 80 : 96);
@@ -146,9 +181,9 @@ constexpr int rb_minb(int bpt, int tpr) {
 }
 
 #define NVFP4AP_RB(B, T)                                                      \
-  if (s.bpt == B && s.tpr == T) return launch_rb<MOD, B, T, rb_minb<MOD>(B, T)>(a, st);
+  if (s.bpt == B && s.tpr == T) return launch_rb<FP8, MOD, B, T, rb_minb<MOD>(B, T)>(a, st);
 
-template <int MOD>
+template <bool FP8, int MOD>
 cudaError_t launch_rb_shape(const LnArgs& a, RbShape s, cudaStream_t st) {
   NVFP4AP_RB(2, 32) NVFP4AP_RB(2, 64) NVFP4AP_RB(2, 96) NVFP4AP_RB(2, 128)
   NVFP4AP_RB(3, 32) NVFP4AP_RB(3, 64) NVFP4AP_RB(3, 96) NVFP4AP_RB(3, 128)
@@ -167,7 +202,9 @@ bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s) {
     if (forced_bpt > 0 && bpt != forced_bpt) continue;
     if (nblk % bpt != 0) continue;
     const int64_t tpr = nblk / bpt;
-    if (tpr % 32 != 0 || tpr > 128) continue;
+    // two to four warps per row: a one-warp row measured slower than the
+    // register row kernels on GB300 (dim 1536)
+    if (tpr % 32 != 0 || tpr < 64 || tpr > 128) continue;
     s->bpt = bpt;
     s->tpr = (int)tpr;
     return true;
@@ -175,11 +212,20 @@ bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s) {
   return false;
 }
 
-cudaError_t launch_ln_rowblk(const LnArgs& a, int mod, RbShape s, cudaStream_t st) {
+cudaError_t launch_ln_rowblk(const LnArgs& a, bool nvfp4, int mod, RbShape s, cudaStream_t st) {
+  if (nvfp4) {
+    switch (mod) {
+      case MOD_NONE: return launch_rb_shape<false, MOD_NONE>(a, s, st);
+      case MOD_BCAST: return launch_rb_shape<false, MOD_BCAST>(a, s, st);
+      case MOD_MODFP8: return launch_rb_shape<false, MOD_MODFP8>(a, s, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (mod) {
-    case MOD_NONE: return launch_rb_shape<MOD_NONE>(a, s, st);
-    case MOD_BCAST: return launch_rb_shape<MOD_BCAST>(a, s, st);
-    case MOD_MODFP8: return launch_rb_shape<MOD_MODFP8>(a, s, st);
+    case MOD_NONE: return launch_rb_shape<true, MOD_NONE>(a, s, st);
+    case MOD_BCAST: return launch_rb_shape<true, MOD_BCAST>(a, s, st);
+    case MOD_MODFP8: return launch_rb_shape<true, MOD_MODFP8>(a, s, st);
+    case MOD_AWQ: return launch_rb_shape<true, MOD_AWQ>(a, s, st);
     default: return cudaErrorInvalidValue;
   }
 }
