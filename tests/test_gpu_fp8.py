@@ -213,6 +213,53 @@ def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
     ap.take_device_fault()  # no bounded wait ran out
 
 
+@pytest.mark.parametrize("rows,dim,bpt", [(131, 2048, 0), (3001, 4096, 0), (257, 6144, 0), (129, 4096, 4),
+                                          (77, 6144, 4), (1, 3072, 0)])
+def test_rowblk_layer_norm_shapes(ap, dev, rows, dim, bpt, monkeypatch):
+    # the FP8 layer norm on the one-row-per-CTA block-per-lane kernel (its
+    # default where a row is exactly 64-128 threads x 2-4 blocks)
+    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    if bpt:
+        monkeypatch.setenv("NVFP4AP_RB_BPT", str(bpt))
+    else:
+        monkeypatch.delenv("NVFP4AP_RB_BPT", raising=False)
+    w = synth.fp8_ln(rows, dim, seed=rows + dim + bpt)
+    d = _d(w, dev)
+    out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
+    ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
+    check_fp8(_codes(out), ref, _act(w))
+
+
+@pytest.mark.parametrize("op", ["bcast", "modfp8", "awq"])
+def test_rowblk_broadcast_sources_when_forced(ap, dev, op, monkeypatch):
+    # the FP8 broadcast sources on the same kernel (NVFP4AP_KERNEL=8)
+    monkeypatch.setenv("NVFP4AP_KERNEL", "8")
+    rows, dim = 517, 3072
+    if op == "bcast":
+        w = synth.fp8_broadcast(rows, dim, seed=5)
+        d = _d(w, dev)
+        out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+        u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+        ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+    elif op == "modfp8":
+        w = synth.fp8_modfp8(rows, dim, seed=6)
+        d = _d(w, dev)
+        out = ap.ada_layer_norm_quant_fp8_modfp8_bf16(d["x"], d["scale_fp8"], d["shift_fp8"], d["scale_deq"],
+                                                      d["shift_deq"], d["act_scale"])
+        src = dict(scale_fp8=w.inputs["scale_fp8"].view(torch.uint8).numpy(),
+                   shift_fp8=w.inputs["shift_fp8"].view(torch.uint8).numpy(),
+                   scale_deq=float(w.inputs["scale_deq"][0]), shift_deq=float(w.inputs["shift_deq"][0]))
+        ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_MODFP8, **src)
+    else:
+        w = synth.fp8_awq(rows, dim, seed=7)
+        d = _d(w, dev)
+        out = ap.awq_ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["inv_s"], d["act_scale"])
+        u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift", "inv_s")}
+        ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_AWQ, scale=u["scale"], shift=u["shift"],
+                                  inv_s=u["inv_s"])
+    check_fp8(_codes(out), ref, _act(w))
+
+
 @pytest.mark.parametrize("op", ["ln", "bcast"])
 def test_blk_many_rows_per_group(ap, dev, op, monkeypatch):
     # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows

@@ -158,6 +158,24 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
     ap.take_device_fault()
 
 
+@pytest.mark.parametrize("rows,dim,bpt", [(131, 2048, 0), (3001, 4096, 0), (257, 6144, 0), (129, 4096, 4),
+                                          (77, 6144, 4), (130, 3072, 0)])
+@pytest.mark.parametrize("kind", ["ln", "bcast"])
+def test_rowblk_shapes(ap, dev, kind, rows, dim, bpt, monkeypatch):
+    # the one-row-per-CTA block-per-lane kernel (the default where a row is
+    # exactly 64-128 threads x 2-4 blocks): 2, 3 and 4 blocks per lane, 64-128
+    # threads per row, ragged row counts (padding rows of the last scale tile)
+    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
+    if bpt:
+        monkeypatch.setenv("NVFP4AP_RB_BPT", str(bpt))
+    else:
+        monkeypatch.delenv("NVFP4AP_RB_BPT", raising=False)
+    w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=rows + dim + bpt)
+    gp, gs = _run(ap, kind, w, dev)
+    op, os_, v = _oracle(w, kind)
+    check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
+
+
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_blk_many_rows_per_group(ap, dev, kind, monkeypatch):
     # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows
