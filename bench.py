@@ -810,33 +810,61 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 def run_sweep(args, dev):
+    """FP8 broadcast row sweep (dims 1536 and 3072, rows 51...32768) plus the pages'
+    RTX 5090 shapes for the broadcast and layer-norm producers.  Per shape: device
+    time per call (a graph of 32 back-to-back calls over rotating buffers > 3x L2,
+    median of 3 replays) and single-launch time (CUDA events around one direct
+    call after a synchronize, median of 20: host launch latency included)."""
     import nvfp4_activation_producer_gb300 as ap
     l2 = 129 * 2 ** 20
+    shapes = [("fp8_broadcast", R, D) for D in synth.SWEEP_DIMS for R in synth.SWEEP_ROWS]
+    shapes += [(op, R, D) for op in ("fp8_broadcast", "fp8_layer_norm")
+               for R, D in ((16, 2048), (64, 3072), (256, 3072), (2520, 3072), (4096, 3072))]
     res = []
-    for D in synth.SWEEP_DIMS:
-        for R in synth.SWEEP_ROWS:
-            w = synth.fp8_broadcast(R, D, synth.SWEEP_SEED)
-            one = alg_bytes("fp8_broadcast", w)
-            nsets = max(2, int(np.ceil(3 * l2 / one)))
-            nsets = min(nsets, 512)
-            x = w.inputs["x"].to(dev)
-            xs = [x.clone() for _ in range(nsets)]
-            outs = [torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev) for _ in range(nsets)]
-            sc, sh, act = (w.inputs[k].to(dev) for k in ("scale", "shift", "act_scale"))
-            for i in range(nsets):
+    st = torch.cuda.Stream(dev)
+    for op, R, D in shapes:
+        w = synth.fp8_broadcast(R, D, synth.SWEEP_SEED)
+        one = alg_bytes(op, w)
+        nsets = min(max(2, int(np.ceil(3 * l2 / one))), 512)
+        xs = [w.inputs["x"].to(dev) for _ in range(nsets)]
+        outs = [torch.empty((R, D), dtype=torch.float8_e4m3fn, device=dev) for _ in range(nsets)]
+        sc, sh, act = (w.inputs[k].to(dev) for k in ("scale", "shift", "act_scale"))
+
+        def call(i):
+            if op == "fp8_broadcast":
                 ap.ada_layer_norm_quant_fp8_bf16(xs[i], sc, sh, act, out=outs[i])
-            reps = max(nsets, 200)
-            torch.cuda.synchronize()
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record()
-            for i in range(reps):
-                ap.ada_layer_norm_quant_fp8_bf16(xs[i % nsets], sc, sh, act, out=outs[i % nsets])
-            t1.record()
-            torch.cuda.synchronize()
-            us = t0.elapsed_time(t1) * 1e3 / reps
-            res.append({"rows": R, "dim": D, "us_per_call": round(us, 3), "gbs": round(one / us / 1e3, 1),
-                        "rows_per_s": round(R / us * 1e6), "buffer_sets": nsets})
-            del xs, outs
+            else:
+                ap.layer_norm_no_affine_quant_fp8_static_bf16(xs[i], act, out=outs[i])
+        with torch.cuda.stream(st):
+            for i in range(nsets):
+                call(i)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(32):
+                    call(i % nsets)
+            g.replay()
+            ts = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                g.replay()
+                e1.record(st)
+                st.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3 / 32)
+            single = []
+            for k in range(20):
+                st.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                call(k % nsets)
+                e1.record(st)
+                st.synchronize()
+                single.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(ts)
+        res.append({"op": op, "rows": R, "dim": D, "us_per_call": round(us, 3),
+                    "us_single_launch": round(statistics.median(single), 3), "gbs": round(one / us / 1e3, 1),
+                    "rows_per_s": round(R / us * 1e6), "buffer_sets": nsets})
+        del xs, outs, g
     return res
 
 
@@ -876,7 +904,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     result = run_ours(args, rank, world, local_rank)
     if args.sweep and rank == 0:
-        result["sweep_fp8_broadcast"] = run_sweep(args, torch.device("cuda", local_rank))
+        result["sweep"] = run_sweep(args, torch.device("cuda", local_rank))
     if rank == 0:
         line = json.dumps(result)
         print(line, flush=True)
