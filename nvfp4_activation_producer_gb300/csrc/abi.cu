@@ -21,6 +21,12 @@ namespace {
 
 inline bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+// Rows from which the block-per-lane persistent kernel is the default: the FP8
+// broadcast sources, and the single-level NVFP4 forms whose row does not fit
+// the one-row-per-CTA kernel (see run_fp8 and run_nvfp4 for the measurements).
+constexpr int64_t kBlkBcastRows = 4096;
+constexpr int64_t kBlkNvfp4Rows = 2048;
+
 int env_int(const char* name) {
   const char* v = std::getenv(name);
   return v ? std::atoi(v) : 0;
@@ -192,10 +198,23 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   int kernel = env_int("NVFP4AP_KERNEL");
   // default: the one-row-per-CTA block-per-lane kernel for the layer norm
   // form where the row fits it exactly (measured on GB300: 4096x3072 7.9 ->
-  // 7.55 us; for the broadcast sources it measured slower than the persistent
-  // broadcast kernel in the bench: 9.3 -> 10.0 us, modfp8 and AWQ more), the
-  // TMA pipeline for the table form, the register kernels for the rest
-  if (kernel == 0) kernel = (mod == MOD_NONE) ? 8 : (mod == MOD_TABLE) ? 4 : 3;
+  // 7.55 us), the TMA pipeline for the table form; for the three broadcast
+  // sources (bf16, modfp8, AWQ: one rule, so that they reduce to each other
+  // bit for bit) the block-per-lane persistent kernel from kBlkBcastRows rows
+  // where its shape has no idle lane and three or more rows per CTA, else the
+  // persistent broadcast kernel.  Measured on GB300 (graphs of 32 calls),
+  // sum over the three sources: 3072 x 4096 rows 28.2 -> 27.1 us, x 32768
+  // 177.7 -> 143.4 us; 1536 x 32768 100.1 -> 76.0 us; 6144 x 32768 351 ->
+  // 290 us; below 4096 rows the persistent kernel is as fast or faster
+  // (3072 x 2520: 20.3 against 21.1 us).
+  if (kernel == 0) {
+    BlkShape bs{};
+    if (mod_is_bcast(mod) && a.rows >= kBlkBcastRows && vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
+        aligned(a.x, 32) && aligned(a.out, 16) && blk_default_shape(a.dim, true, &bs))
+      kernel = 5;
+    else
+      kernel = (mod == MOD_NONE) ? 8 : (mod == MOD_TABLE) ? 4 : 3;
+  }
   if (kernel == 1 && (mod == MOD_MODFP8 || mod == MOD_AWQ)) kernel = 3;
   if (kernel == 8) {
     // one-row-per-CTA block-per-lane kernel where the row fits it exactly
@@ -211,11 +230,20 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     if (vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) && aligned(a.out, 16)) {
       BlkShape bs{};
       const int sms = sm_count();
-      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs, true)) {
         bs.ctas_per_sm = env_int("NVFP4AP_BLK_CTAS");
         bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
         return finish(launch_ln_blk(a, false, mod, bs, sms, st));
       }
+    }
+    kernel = (mod == MOD_TABLE) ? 4 : 3;
+  }
+  if (kernel == 6) {
+    // warp-per-row kernel (two sweeps of each row) where it applies, else the default
+    if (vec8 && (mod == MOD_NONE || mod == MOD_BCAST) && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
+        aligned(a.x, 32) && aligned(a.out, 16)) {
+      const int sms = sm_count();
+      if (sms > 0) return finish(launch_ln_warp_rows_fp8(a, mod, sms, st));
     }
     kernel = (mod == MOD_TABLE) ? 4 : 3;
   }
@@ -276,7 +304,7 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
       aligned(a.x, 32) && aligned(a.out, 16)) {
     BlkShape bs{};
     const int sms = sm_count();
-    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
+    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs, !nvfp4)) {
       bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
       return finish(launch_ln_blk(a, nvfp4, MOD_SEG, bs, sms, st));
     }
@@ -351,17 +379,24 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8, 8: one-row-per-CTA block-per-lane kernels
   // default: the one-row-per-CTA block-per-lane kernel where the row fits it
   // exactly (measured faster than the register row and persistent kernels on
-  // GB300 at dims 2048-4096, 2,520-16,384 rows: 5070x3072 layer norm 10.0 ->
-  // 8.5 us, broadcast 12.2 -> 10.6 us), the register row kernels otherwise
+  // GB300 at dims 2048-8192, 2,520-32,768 rows: 5070x3072 layer norm 10.0 ->
+  // 8.5 us, broadcast 12.2 -> 10.6 us); where it does not, the block-per-lane
+  // persistent kernel from kBlkNvfp4Rows rows when its shape has no idle lane
+  // and three or more rows per CTA (dims 1024, 1536, 5120; measured at
+  // 2,520-32,768 rows: faster at every size, 1536 x 32768 layer norm 33.4 ->
+  // 22.2 us, broadcast 36.8 -> 28.3 us, 5120 x 4096 broadcast 20.1 -> 16.0
+  // us), else the register row kernels
+  const bool blk_ok = ln_blk_supported(BLK_NVFP4, mod, a.dim, 0) && aligned(a.x, 32);
   if (kernel == 0 || kernel == 8) {
     RbShape rb{};
     if ((mod == MOD_NONE || mod == MOD_BCAST || mod == MOD_MODFP8) && aligned(a.x, 32) &&
         pick_rowblk(a.dim, env_int("NVFP4AP_RB_BPT"), &rb))
       return finish(launch_ln_rowblk(a, true, mod, rb, st));
-    kernel = 3;
+    BlkShape bs{};
+    kernel = (kernel == 0 && a.rows >= kBlkNvfp4Rows && blk_ok && blk_default_shape(a.dim, false, &bs)) ? 5 : 3;
   }
   if (kernel == 5) {
-    if (ln_blk_supported(BLK_NVFP4, mod, a.dim, 0) && aligned(a.x, 32)) {
+    if (blk_ok) {
       BlkShape bs{};
       const int sms = sm_count();
       if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {

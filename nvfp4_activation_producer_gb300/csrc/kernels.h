@@ -113,8 +113,12 @@ constexpr int64_t kBlkMaxDim = 8192;
 enum { BLK_FP8 = 0, BLK_NVFP4 = 1, BLK_2LEVEL = 2 };
 // `kind` BLK_*; nseg: segments of a MOD_SEG source (their tables must fit)
 bool ln_blk_supported(int kind, int mod, int64_t dim, int64_t nseg);
-// shape for `dim` (forced_bpt > 0: only that many blocks per lane)
-bool pick_blk(int64_t dim, int forced_bpt, BlkShape* s);
+// shape for `dim` (forced_bpt > 0: only that many blocks per lane); `fp8`:
+// the FP8 preference (3, 2, 4, 6 blocks per lane) instead of 3, 4, 2, 6
+bool pick_blk(int64_t dim, int forced_bpt, BlkShape* s, bool fp8 = false);
+// the block-per-lane kernel as a default: a shape with no idle lane and at
+// least three rows per CTA
+bool blk_default_shape(int64_t dim, bool fp8, BlkShape* s);
 cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int sms, cudaStream_t st);
 // two-level NVFP4 on the block-per-lane kernels: clears a.amax_ws, maximum
 // pass, quantising pass; mod MOD_NONE, MOD_BCAST or MOD_SEG
