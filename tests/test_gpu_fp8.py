@@ -318,3 +318,23 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
             ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
         check_fp8(_codes(out), ref, _act(w))
     ap.take_device_fault()
+
+
+@pytest.mark.parametrize("op", ["ln", "bcast"])
+def test_warp_rows_when_forced(ap, dev, op, monkeypatch):
+    # the warp-per-row kernel for the layer norm and broadcast forms
+    # (NVFP4AP_KERNEL=6): rows well above and below one per warp of the grid
+    monkeypatch.setenv("NVFP4AP_KERNEL", "6")
+    for rows, dim in ((3001, 3072), (517, 1536), (40000, 272)):
+        if op == "bcast":
+            w = synth.fp8_broadcast(rows, dim, seed=rows)
+            d = _d(w, dev)
+            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
+            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+        else:
+            w = synth.fp8_ln(rows, dim, seed=rows)
+            d = _d(w, dev)
+            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
+            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
+        check_fp8(_codes(out), ref, _act(w), f"{op} {rows}x{dim}")
