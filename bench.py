@@ -699,7 +699,8 @@ def run_e2e(ap, works, dev, stream, args, world, step_bytes, barrier):
     ms_step = ms / steps
     return {"value": round(job_gbs(step_bytes, world, ms_step), 1), "unit": "GB/s",
             "ms_per_step": round(ms_step, 4), "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "h2d / producers / d2h on three streams, two device buffer sets"}
+            "pipeline": "h2d / producers / d2h on three streams, two device buffer sets",
+            "binding": ap.marshalling()}
 
 
 # ---------------------------------------------------------------------------
