@@ -499,7 +499,7 @@ def run_ours(args, rank, world, local_rank):
         t_end.record(stream)
         for o, g, n, _, _ in per_op_graphs:
             evs = []
-            for _ in range(3):
+            for _ in range(args.op_replays):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 g.replay()
@@ -534,10 +534,13 @@ def run_ours(args, rank, world, local_rank):
     per_op = []
     for i, o in enumerate(ops + extra_ops):
         n = args.per_op_launches
-        us = statistics.median(e0.elapsed_time(e1) for e0, e1 in op_events[i]) * 1e3 / n
+        calls = [e0.elapsed_time(e1) * 1e3 / n for e0, e1 in op_events[i]]
+        us = statistics.median(calls)
         gbs = o.bytes / (us * 1e-6) / 1e9
         copy_us = statistics.median(e0.elapsed_time(e1) for e0, e1 in copy_events[i]) * 1e3 / n
         per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
+                       "us_p10": round(float(np.percentile(calls, 10)), 3),
+                       "us_p90": round(float(np.percentile(calls, 90)), 3),
                        "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4),
                        "copy_us": round(copy_us, 3), "frac_of_copy": round(copy_us / us, 4),
                        "in_step": i < len(ops)})
@@ -562,9 +565,10 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline, "per_op": per_op, "e2e": e2e, "chain": chain,
         "gpu_launches": launches, "clocks": clocks.summary(),
         "timing": ("step: CUDA graph of %d steps replayed %d times; per_op: graph of %d back-to-back calls per "
-                   "producer over rotating buffers > 3x L2, median of 3 replays; copy_us: the same for a streaming copy "
-                   "kernel (torch int32 add of 0) moving the producer's algorithmic bytes, frac_of_copy = copy_us / us_per_call"
-                   % (M, R, args.per_op_launches)),
+                   "producer over rotating buffers > 3x L2, median (us_per_call), p10 and p90 of the per-call time "
+                   "over %d replays; copy_us: the same for a streaming copy kernel (torch int32 add of 0) moving the "
+                   "producer's algorithmic bytes, median of 3 replays, frac_of_copy = copy_us / us_per_call"
+                   % (M, R, args.per_op_launches, args.op_replays)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
@@ -810,18 +814,69 @@ def run_reference(args):
 # row sweep of the FP8 broadcast producer (optional)
 # ---------------------------------------------------------------------------
 
+# the pages' RTX 5090 shapes of the FP8 broadcast and layer-norm producers
+PAGE_SHAPES = ((16, 2048), (64, 3072), (256, 3072), (2520, 3072), (4096, 3072))
+
+
+def eager_context(op, xs, sc, sh, act, nsets, st):
+    """Context only: the PyTorch eager chain the pages time beside their
+    producers (F.layer_norm, then *(1+scale)+shift for the broadcast form,
+    / act_scale, clamp to +-448, .to(float8_e4m3fn)), on this GPU, timed the
+    same two ways as the producer: device time per call from a CUDA graph of
+    32 calls over the rotating buffers, and one direct call.  It is not the
+    product path and no output of it is used."""
+    import torch.nn.functional as F
+    D = xs[0].shape[1]
+
+    def chain(i):
+        y = F.layer_norm(xs[i], (D,), eps=1e-5)
+        if op == "fp8_broadcast":
+            y = y * (1 + sc) + sh
+        return (y / act).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+
+    with torch.cuda.stream(st):
+        for i in range(nsets):
+            chain(i)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(32):
+                chain(i % nsets)
+        g.replay()
+        ts = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            g.replay()
+            e1.record(st)
+            st.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / 32)
+        single = []
+        for k in range(20):
+            st.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            chain(k % nsets)
+            e1.record(st)
+            st.synchronize()
+            single.append(e0.elapsed_time(e1) * 1e3)
+    del g
+    return {"eager_us_per_call": round(statistics.median(ts), 3),
+            "eager_us_single_launch": round(statistics.median(single), 3)}
+
+
 def run_sweep(args, dev):
     """FP8 broadcast row sweep (dims 1536 and 3072, rows 51...32768) plus the pages'
     RTX 5090 shapes for the broadcast and layer-norm producers.  Per shape: device
     time per call (a graph of 32 back-to-back calls over rotating buffers > 3x L2,
     median of 3 replays) and single-launch time (CUDA events around one direct
-    call after a synchronize, median of 20: host launch latency included)."""
+    call after a synchronize, median of 20: host launch latency included); at
+    the pages' shapes also the PyTorch eager chain, as context (eager_context)."""
     import nvfp4_activation_producer_gb300 as ap
     l2 = 129 * 2 ** 20
     shapes = [("fp8_broadcast", R, D) for D in synth.SWEEP_DIMS for R in synth.SWEEP_ROWS]
-    shapes += [(op, R, D) for op in ("fp8_broadcast", "fp8_layer_norm")
-               for R, D in ((16, 2048), (64, 3072), (256, 3072), (2520, 3072), (4096, 3072))]
+    shapes += [(op, R, D) for op in ("fp8_broadcast", "fp8_layer_norm") for R, D in PAGE_SHAPES]
     res = []
+    eager_done = set()
     st = torch.cuda.Stream(dev)
     for op, R, D in shapes:
         w = synth.fp8_broadcast(R, D, synth.SWEEP_SEED)
@@ -862,9 +917,13 @@ def run_sweep(args, dev):
                 st.synchronize()
                 single.append(e0.elapsed_time(e1) * 1e3)
         us = statistics.median(ts)
-        res.append({"op": op, "rows": R, "dim": D, "us_per_call": round(us, 3),
-                    "us_single_launch": round(statistics.median(single), 3), "gbs": round(one / us / 1e3, 1),
-                    "rows_per_s": round(R / us * 1e6), "buffer_sets": nsets})
+        rec = {"op": op, "rows": R, "dim": D, "us_per_call": round(us, 3),
+               "us_single_launch": round(statistics.median(single), 3), "gbs": round(one / us / 1e3, 1),
+               "rows_per_s": round(R / us * 1e6), "buffer_sets": nsets}
+        if (R, D) in PAGE_SHAPES and (op, R, D) not in eager_done:
+            rec.update(eager_context(op, xs, sc, sh, act, nsets, st))
+            eager_done.add((op, R, D))
+        res.append(rec)
         del xs, outs, g
     return res
 
@@ -878,6 +937,8 @@ def main():
     ap_.add_argument("--e2e-steps", type=int, default=20)
     ap_.add_argument("--graph-steps", type=int, default=25, help="steps captured per CUDA graph")
     ap_.add_argument("--per-op-launches", type=int, default=32, help="back-to-back calls per producer graph")
+    ap_.add_argument("--op-replays", type=int, default=11,
+                     help="replays of each producer graph (median, p10 and p90 of the per-call time)")
     ap_.add_argument("--only", default=None, help="comma list of producers to run (for profiling one kernel)")
     ap_.add_argument("--cpu-seconds", type=float, default=15.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
