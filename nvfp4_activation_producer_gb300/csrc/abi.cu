@@ -8,8 +8,10 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 
 #include <cuda_runtime.h>
+#include <unistd.h>
 
 #include "kernels.h"
 #include "nvfp4ap.h"
@@ -28,13 +30,13 @@ constexpr int64_t kBlkBcastRows = 4096;
 constexpr int64_t kBlkNvfp4Rows = 2048;
 
 int env_int(const char* name) {
-  const char* v = std::getenv(name);
+  const char* v = env_get(name);
   return v ? std::atoi(v) : 0;
 }
 
 // true when the variable is set to 0 (a default-on choice switched off)
 bool env_off(const char* name) {
-  const char* v = std::getenv(name);
+  const char* v = env_get(name);
   return v && v[0] == '0';
 }
 
@@ -462,8 +464,40 @@ LnArgs ln_args(const void* x, float eps, void* out, int64_t rows, int64_t dim) {
 }  // namespace
 
 bool pdl_enabled() {
-  const char* v = std::getenv("NVFP4AP_PDL");
+  const char* v = env_get("NVFP4AP_PDL");
   return !(v && v[0] == '0');
+}
+
+// The NVFP4AP_* settings of this thread's current call: one pass over the
+// environment per producer call (env_refresh, first thing in every producer
+// entry point) keeps the entries that start with NVFP4AP_; env_get then reads
+// those.  Each getenv is a scan of the whole environment (eight of them took
+// 1.9 us on an x86 host with 114 variables), the pass about a tenth of that,
+// and a setting changed between calls is still seen by the next call.
+namespace {
+struct EnvSnap {
+  int n;
+  const char* kv[64];
+};
+thread_local EnvSnap g_env = {0, {}};
+}  // namespace
+
+void env_refresh() {
+  int n = 0;
+  for (char** e = environ; e != nullptr && *e != nullptr; ++e) {
+    const char* kv = *e;
+    if (kv[0] == 'N' && std::strncmp(kv, "NVFP4AP_", 8) == 0 && n < 64) g_env.kv[n++] = kv;
+  }
+  g_env.n = n;
+}
+
+const char* env_get(const char* name) {
+  const size_t len = std::strlen(name);
+  for (int i = 0; i < g_env.n; ++i) {
+    const char* kv = g_env.kv[i];
+    if (std::strncmp(kv, name, len) == 0 && kv[len] == '=') return kv + len + 1;
+  }
+  return nullptr;
 }
 
 }  // namespace nvfp4ap
@@ -502,6 +536,7 @@ NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
                                                  const float* act_scale, float eps, void* out, int64_t rows,
                                                  int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
@@ -512,6 +547,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scal
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const void* scale, const void* shift,
                                                          const float* act_scale, float eps, void* out,
                                                          int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   int rc = check_common(rows, dim, eps);
   if (rc) return rc;
   if (dim % 8 != 0) return NVFP4AP_ERR_DIM;
@@ -533,6 +569,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const vo
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_bf16(const void* x, const void* scale, const void* shift,
                                                       const float* act_scale, float eps, void* out,
                                                       int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
@@ -544,6 +581,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_ptok_table_bf16(const void* x, const
                                                             int64_t chunks, int64_t shift_idx, int64_t scale_idx,
                                                             const float* act_scale, float eps, void* out,
                                                             int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.temb = static_cast<const uint16_t*>(temb);
   a.table = table;
@@ -558,6 +596,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_modfp8_bf16(const void* x, const voi
                                                         const float* scale_deq, const float* shift_deq,
                                                         const float* act_scale, float eps, void* out, int64_t rows,
                                                         int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.scale8 = static_cast<const uint8_t*>(scale_fp8);
   a.shift8 = static_cast<const uint8_t*>(shift_fp8);
@@ -570,6 +609,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_modfp8_bf16(const void* x, const voi
 NVFP4AP_EXPORT int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
                                                      const void* inv_s, const float* act_scale, float eps, void* out,
                                                      int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
@@ -581,6 +621,7 @@ NVFP4AP_EXPORT int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* 
 NVFP4AP_EXPORT int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_scale, float eps,
                                                               void* out, int64_t rows, int64_t dim,
                                                               nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.act_scale = act_scale;
   return run_fp8(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
@@ -589,6 +630,7 @@ NVFP4AP_EXPORT int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, con
 NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const void* scale, const void* shift,
                                                             float eps, void* packed, void* sf_swizzled,
                                                             int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
@@ -601,6 +643,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(const void* x
                                                                    const float* shift_deq, float eps, void* packed,
                                                                    void* sf_swizzled, int64_t rows, int64_t dim,
                                                                    nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.scale8 = static_cast<const uint8_t*>(scale_fp8);
   a.shift8 = static_cast<const uint8_t*>(shift_fp8);
@@ -613,6 +656,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(const void* x
 NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_swizzled_bf16(const void* x, float eps, void* packed,
                                                                   void* sf_swizzled, int64_t rows, int64_t dim,
                                                                   nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.sf = sf_swizzled;
   return run_nvfp4(a, MOD_NONE, reinterpret_cast<cudaStream_t>(stream));
@@ -622,6 +666,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_seg_bf16(const void* x, const int32_
                                                      const void* seg_shift, int64_t nseg, const float* act_scale,
                                                      float eps, void* out, int64_t rows, int64_t dim,
                                                      nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, out, rows, dim);
   a.seg_idx = seg_idx;
   a.seg_scale = static_cast<const uint16_t*>(seg_scale);
@@ -636,6 +681,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, c
                                                                 int64_t nseg, float eps, void* packed,
                                                                 void* sf_swizzled, int64_t rows, int64_t dim,
                                                                 nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.seg_idx = seg_idx;
   a.seg_scale = static_cast<const uint16_t*>(seg_scale);
@@ -649,6 +695,7 @@ NVFP4AP_EXPORT int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, f
                                                                 void* sf_swizzled, float* tensor_scale,
                                                                 void* workspace, int64_t rows, int64_t dim,
                                                                 nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.sf = sf_swizzled;
   a.tensor_scale = tensor_scale;
@@ -660,6 +707,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_bf16(const void* x, const v
                                                           float eps, void* packed, void* sf_swizzled,
                                                           float* tensor_scale, void* workspace, int64_t rows,
                                                           int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
@@ -675,6 +723,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, con
                                                               void* sf_swizzled, float* tensor_scale,
                                                               void* workspace, int64_t rows, int64_t dim,
                                                               nvfp4ap_stream_t stream) {
+  env_refresh();
   LnArgs a = ln_args(x, eps, packed, rows, dim);
   a.seg_idx = seg_idx;
   a.seg_scale = static_cast<const uint16_t*>(seg_scale);
@@ -689,6 +738,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_nvfp4_2level_seg_bf16(const void* x, con
 NVFP4AP_EXPORT int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* up, int64_t ld, void* packed,
                                                   void* sf_swizzled, float* tensor_scale, void* workspace,
                                                   int64_t rows, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (dim > NVFP4AP_MAX_DIM || dim % 16 != 0) return NVFP4AP_ERR_DIM;
   if (ld < dim || ld % 8 != 0 || !swiglu_items_fit(rows, dim)) return NVFP4AP_ERR_SHAPE;
@@ -706,6 +756,7 @@ NVFP4AP_EXPORT int swiglu_quant_nvfp4_2level_bf16(const void* gate, const void* 
 
 NVFP4AP_EXPORT int swiglu_bf16(const void* gate, const void* up, int64_t ld, void* out, int64_t rows, int64_t dim,
                                nvfp4ap_stream_t stream) {
+  env_refresh();
   if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (dim > NVFP4AP_MAX_DIM || dim % 8 != 0) return NVFP4AP_ERR_DIM;
   if (ld < dim || ld % 8 != 0 || !swiglu_items_fit(rows, dim)) return NVFP4AP_ERR_SHAPE;
@@ -731,6 +782,7 @@ NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {
 
 NVFP4AP_EXPORT int adaln_modulation6_bf16(const float* params, const float* modulation, void* const out[6],
                                           int64_t batch, int64_t seq, int64_t dim, nvfp4ap_stream_t stream) {
+  env_refresh();
   if (batch < 0 || seq < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (seq != 0 && batch > INT64_MAX / seq) return NVFP4AP_ERR_SHAPE;
   const int64_t tokens = batch * seq;

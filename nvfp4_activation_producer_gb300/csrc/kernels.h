@@ -11,6 +11,10 @@ namespace nvfp4ap {
 // NVFP4AP_PDL=0: the kernel may then be dispatched while the previous kernel
 // on the stream drains (the kernel itself waits for it, see pdl_enter()).
 bool pdl_enabled();
+// NVFP4AP_* settings of the current producer call (abi.cu): env_refresh takes
+// one pass over the environment, env_get reads that snapshot (nullptr if unset)
+void env_refresh();
+const char* env_get(const char* name);
 template <typename... KArgs, typename... Args>
 cudaError_t launch_maybe_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                              Args&&... args) {

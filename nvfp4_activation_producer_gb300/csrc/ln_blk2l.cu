@@ -135,7 +135,7 @@ cudaError_t run_blk_2level(const LnArgs& a, BlkShape s, int sms, cudaStream_t st
   if (e != cudaSuccess) return e;
   // maximum pass: warp per row when the rows give every warp of the grid
   // several (NVFP4AP_2L_AMAX=1 forces it, 2 the row-group kernel)
-  const char* v = std::getenv("NVFP4AP_2L_AMAX");
+  const char* v = env_get("NVFP4AP_2L_AMAX");
   const int force = v ? std::atoi(v) : 0;
   const bool warp_rows = a.row_stats != nullptr &&
                          (force == 1 || (force == 0 && a.rows >= (int64_t)sms * (kFlatThreads / 32) * 4));

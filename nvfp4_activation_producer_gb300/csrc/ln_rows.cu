@@ -247,7 +247,7 @@ cudaError_t launch_persist(const LnArgs& a, RowShape s, int sms, int ctas_per_sm
   const int64_t work_rows = KIND == KIND_NVFP4 ? (a.rows + 127) / 128 * 128 : a.rows;
   // rows that exactly fill the threads' chunks take the FULL instance
   // (NVFP4AP_FULL=0 turns it off)
-  const char* full_env = std::getenv("NVFP4AP_FULL");
+  const char* full_env = env_get("NVFP4AP_FULL");
   const bool full = !(full_env && full_env[0] == '0') && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
 #define NVFP4AP_CASE(N)                                                                        \
   case N: {                                                                                    \

@@ -376,7 +376,7 @@ TmaPlan tma_plan(TmaKernel k, int mod, int64_t dim, int tpr, int forced_stages) 
     if (bytes >= 96 * 1024) break;
   }
   if (n < 128) cache[n++] = Entry{k, dim, tpr, forced_stages, dev, best};
-  if (const char* dbg = std::getenv("NVFP4AP_DEBUG"))
+  if (const char* dbg = env_get("NVFP4AP_DEBUG"))
     if (dbg[0] == '1')
       std::fprintf(stderr, "nvfp4ap: tma plan dim=%lld tpr=%d: stages=%d ctas/SM=%d\n", (long long)dim, tpr,
                    best.stages, best.occ);
@@ -393,7 +393,7 @@ cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int 
                           int ctas_per_sm, cudaStream_t st) {
   // rows that exactly fill the threads' chunks take the FULL instance
   // (NVFP4AP_FULL=0 turns it off)
-  const char* full_env = std::getenv("NVFP4AP_FULL");
+  const char* full_env = env_get("NVFP4AP_FULL");
   const bool full = !(full_env && full_env[0] == '0') && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
   TmaKernel k = pick(nvfp4, mod, s.per_thread, full);
   if (!k || s.tpr > 256 || s.rpc != 1) return cudaErrorInvalidValue;
