@@ -125,8 +125,9 @@ def alg_bytes(name: str, w) -> int:
 
 
 def launches_per_call(name: str) -> int:
-    """Kernels one call of the producer launches: the two-level producers clear
-    their word, then run the maximum and the quantising pass."""
+    """Kernels one call of the producer launches: the two-level producers (the
+    LayerNorm forms and SwiGLU) clear their word, then run the maximum and the
+    quantising pass."""
     return 3 if name.startswith("nvfp4_2level") else 1
 
 
@@ -524,7 +525,7 @@ def run_ours(args, rank, world, local_rank):
     value = job_gbs(step_bytes, world, ms_per_step)
     args.steps = steps
     launches = sum(launches_per_call(o.name) for o in ops) * steps + \
-        sum(launches_per_call(o.name) * n * 3 for o, _, n, _, _ in per_op_graphs)
+        sum(launches_per_call(o.name) * n * args.op_replays for o, _, n, _, _ in per_op_graphs)
     del per_op_graphs, copy_graphs
 
     peaks = measured_peaks()

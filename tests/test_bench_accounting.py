@@ -1,0 +1,51 @@
+"""bench.py's accounting, on the CPU: the algorithmic bytes every GB/s and
+roofline figure divides by (the per-op formulas: each input element the
+producer uses read once, each output byte written once), and the kernel
+launches per call that the JSON line's gpu_launches counts."""
+import sys
+import types
+
+import pytest
+
+sys.argv = sys.argv[:1]
+import bench  # noqa: E402
+
+
+def _w(R, D):
+    # the shape is all the formulas read for these producers
+    return types.SimpleNamespace(rows=R, dim=D, inputs={})
+
+
+def _sf(R, D):
+    return ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
+
+
+@pytest.mark.parametrize("name,make,expect", [
+    # x read, codes written, plus the broadcast vectors and the act_scale word
+    ("fp8_broadcast", lambda: _w(4096, 3072), 4096 * 3072 * 3 + 4 * 3072 + 4),
+    ("fp8_layer_norm", lambda: _w(4096, 3072), 4096 * 3072 * 3 + 4),
+    # per-token: x and the two (R, D) bf16 tensors read
+    ("fp8_per_token", lambda: _w(2520, 3072), 2520 * 3072 * 7 + 4),
+    # table: x, two of the six temb chunks, two fp32 table rows
+    ("fp8_table", lambda: _w(4096, 3072), 4096 * 3072 * 7 + 8 * 3072 + 4),
+    # NVFP4: x read, half a byte per element, the padded swizzled scale buffer
+    ("nvfp4_layer_norm", lambda: _w(5070, 3072), 5070 * 3072 * 2 + 5070 * 1536 + _sf(5070, 3072)),
+    ("nvfp4_broadcast", lambda: _w(5070, 3072),
+     5070 * 3072 * 2 + 4 * 3072 + 5070 * 1536 + _sf(5070, 3072)),
+    # six-way: fp32 params and modulation read, six bf16 outputs written
+    ("modulation6", lambda: _w(5070, 3072), 5070 * 3072 * 36 + 24 * 3072),
+])
+def test_alg_bytes(name, make, expect):
+    assert bench.alg_bytes(name, make()) == expect
+
+
+def test_swizzled_buffer_size_matches_the_library_formula():
+    # the 128x4 layout: rows padded to 128, 16-element blocks padded to 4 columns
+    assert _sf(5070, 3072) == 5120 * 192 == 983040
+
+
+@pytest.mark.parametrize("name,n", [("nvfp4_2level_layer_norm", 3), ("nvfp4_2level_seg_h3", 3),
+                                    ("nvfp4_2level_swiglu_h3", 3), ("swiglu_values_h3", 1), ("fp8_broadcast", 1),
+                                    ("modulation6", 1), ("fp8_seg_h3", 1)])
+def test_launches_per_call(name, n):
+    assert bench.launches_per_call(name) == n
