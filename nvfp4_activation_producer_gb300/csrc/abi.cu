@@ -245,6 +245,8 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     if (vec8 && (mod == MOD_NONE || mod == MOD_BCAST) && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
         aligned(a.x, 32) && aligned(a.out, 16)) {
       const int sms = sm_count();
+      if (sms > 0 && !env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0)
+        return finish(launch_warp_regs(a, false, mod, sms, st));
       if (sms > 0) return finish(launch_ln_warp_rows_fp8(a, mod, sms, st));
     }
     kernel = (mod == MOD_TABLE) ? 4 : 3;
@@ -316,8 +318,13 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   if (!nvfp4 && env_int("NVFP4AP_KERNEL") != 5 && env_int("NVFP4AP_SEG_WARP") >= 0 &&
       ln_blk_supported(BLK_FP8, MOD_SEG, a.dim, a.nseg) && aligned(a.x, 32) && aligned(a.out, 16)) {
     const int sms = sm_count();
-    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || a.rows >= ln_warp_rows_min(sms)))
+    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || a.rows >= ln_warp_rows_min(sms))) {
+      // the row held in registers where a lane's share fits (NVFP4AP_WARPREG=0:
+      // the two-sweep kernel; measured on GB300 at 37810x5376: 119.7 -> 101.1 us)
+      if (!env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0)
+        return finish(launch_warp_regs(a, false, MOD_SEG, sms, st));
       return finish(launch_ln_warp_rows_fp8(a, MOD_SEG, sms, st));
+    }
   }
   RowShape s{};
   if (!pick_rows(MOD_SEG, a.dim, &s)) return NVFP4AP_ERR_DIM;
@@ -524,13 +531,14 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
-  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u;
+  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u, k = 0u;
   if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess ||
-      take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess) {
+      take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess ||
+      take_warpreg_seg_fault(&k) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  return (f | g | h | i | j) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  return (f | g | h | i | j | k) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,

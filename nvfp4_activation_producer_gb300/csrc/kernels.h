@@ -133,9 +133,17 @@ cudaError_t launch_ln_2level_blk(const LnArgs& a, int mod, BlkShape s, int sms, 
 // for the block-per-lane kernels).
 int64_t ln_warp_rows_min(int sms);
 cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStream_t st);
+// Register-resident warp-per-row producers (ln_warpreg.cu): the same
+// operations as the warp-per-row kernels with the row read once.  Lanes hold
+// warp_regs_bpl(dim) blocks (0 when dim is not a multiple of 16 or above
+// 6144); amax: the two-level maximum pass (else FP8); mod MOD_NONE,
+// MOD_BCAST or MOD_SEG.
+int warp_regs_bpl(int64_t dim);
+cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, cudaStream_t st);
 // read and clear the segment-index fault words of the two translation units
 cudaError_t take_blk_seg_fault(unsigned int* fault);
 cudaError_t take_blk2l_seg_fault(unsigned int* fault);
+cudaError_t take_warpreg_seg_fault(unsigned int* fault);
 
 // One-row-per-CTA block-per-lane kernels (ln_rowblk.cu), NVFP4 and FP8: `tpr`
 // threads per row (64..128, a multiple of 32), `bpt` 16-element blocks per

@@ -139,7 +139,13 @@ cudaError_t run_blk_2level(const LnArgs& a, BlkShape s, int sms, cudaStream_t st
   const int force = v ? std::atoi(v) : 0;
   const bool warp_rows = a.row_stats != nullptr &&
                          (force == 1 || (force == 0 && a.rows >= (int64_t)sms * (kFlatThreads / 32) * 4));
-  e = warp_rows ? launch_warp_rows<BK_AMAX, MOD>(a, sms, st) : launch_blk_bpt<BK_AMAX, MOD>(a, s, sms, st);
+  // the warp-per-row pass with the row held in registers where a lane's share
+  // fits (NVFP4AP_WARPREG=0: the two-sweep kernel)
+  const char* wr = env_get("NVFP4AP_WARPREG");
+  const bool regs = warp_rows && !(wr != nullptr && wr[0] == '0') && warp_regs_bpl(a.dim) > 0;
+  e = regs        ? launch_warp_regs(a, true, MOD, sms, st)
+      : warp_rows ? launch_warp_rows<BK_AMAX, MOD>(a, sms, st)
+                  : launch_blk_bpt<BK_AMAX, MOD>(a, s, sms, st);
   if (e != cudaSuccess) return e;
   // flat quantising pass when the statistics were kept and the block index
   // fits 32 bits; otherwise the row-group pass

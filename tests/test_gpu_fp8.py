@@ -320,11 +320,14 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
     ap.take_device_fault()
 
 
+@pytest.mark.parametrize("regs", ["1", "0"])
 @pytest.mark.parametrize("op", ["ln", "bcast"])
-def test_warp_rows_when_forced(ap, dev, op, monkeypatch):
-    # the warp-per-row kernel for the layer norm and broadcast forms
-    # (NVFP4AP_KERNEL=6): rows well above and below one per warp of the grid
+def test_warp_rows_when_forced(ap, dev, op, regs, monkeypatch):
+    # the warp-per-row kernels for the layer norm and broadcast forms
+    # (NVFP4AP_KERNEL=6): rows well above and below one per warp of the grid;
+    # the row held in registers (default) or read twice (NVFP4AP_WARPREG=0)
     monkeypatch.setenv("NVFP4AP_KERNEL", "6")
+    monkeypatch.setenv("NVFP4AP_WARPREG", regs)
     for rows, dim in ((3001, 3072), (517, 1536), (40000, 272)):
         if op == "bcast":
             w = synth.fp8_broadcast(rows, dim, seed=rows)
