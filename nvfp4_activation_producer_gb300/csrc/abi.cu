@@ -318,11 +318,11 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   if (!nvfp4 && env_int("NVFP4AP_KERNEL") != 5 && env_int("NVFP4AP_SEG_WARP") >= 0 &&
       ln_blk_supported(BLK_FP8, MOD_SEG, a.dim, a.nseg) && aligned(a.x, 32) && aligned(a.out, 16)) {
     const int sms = sm_count();
-    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || a.rows >= ln_warp_rows_min(sms))) {
-      // the row held in registers where a lane's share fits (NVFP4AP_WARPREG=0:
-      // the two-sweep kernel; measured on GB300 at 37810x5376: 119.7 -> 101.1 us)
-      if (!env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0)
-        return finish(launch_warp_regs(a, false, MOD_SEG, sms, st));
+    // the row held in registers where a lane's share fits (NVFP4AP_WARPREG=0:
+    // the two-sweep kernel; measured on GB300 at 37810x5376: 119.7 -> 101.1 us)
+    const bool regs = !env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0;
+    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || warp_path_rows(a.rows, a.dim, sms, regs))) {
+      if (regs) return finish(launch_warp_regs(a, false, MOD_SEG, sms, st));
       return finish(launch_ln_warp_rows_fp8(a, MOD_SEG, sms, st));
     }
   }

@@ -139,6 +139,12 @@ cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStrea
 // 6144); amax: the two-level maximum pass (else FP8); mod MOD_NONE,
 // MOD_BCAST or MOD_SEG.
 int warp_regs_bpl(int64_t dim);
+// whether the warp-per-row path takes `rows` x `dim` on `sms` SMs: the two-sweep
+// kernel from 4 rows per warp of its grid (sms * 128 rows); the
+// register-resident one (regs) from the same number of elements, rows * dim >=
+// sms * 128 * 3072 (measured on GB300: at 12000x5376 the two-level maximum pass
+// 70.4 -> 60.9 us against the row-group kernel, at 12000x3072 a tie)
+bool warp_path_rows(int64_t rows, int64_t dim, int sms, bool regs);
 cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, cudaStream_t st);
 // read and clear the segment-index fault words of the two translation units
 cudaError_t take_blk_seg_fault(unsigned int* fault);

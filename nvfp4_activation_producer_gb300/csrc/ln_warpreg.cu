@@ -160,6 +160,11 @@ int warp_regs_bpl(int64_t dim) {
   return 0;
 }
 
+bool warp_path_rows(int64_t rows, int64_t dim, int sms, bool regs) {
+  const int64_t min_rows = (int64_t)sms * 32 * 4;
+  return regs ? rows * dim >= min_rows * 3072 : rows >= min_rows;
+}
+
 // this translation unit's copy of the segment fault word (ln_blk.cuh), read and cleared
 cudaError_t take_warpreg_seg_fault(unsigned int* fault) { return take_blk_word(fault); }
 

@@ -266,3 +266,29 @@ def test_register_rows_equal_two_sweeps(ap, dev, family, rows, dim, monkeypatch)
     for a, b in zip(*res):
         assert torch.equal(a, b)
     ap.take_device_fault()
+
+
+def test_register_warp_path_from_the_element_threshold(ap, dev, family, monkeypatch):
+    # the register-resident warp kernels take a tensor from sms * 128 * 3072
+    # elements (fewer rows than the two-sweep kernel's sms * 128 at wide dims):
+    # just above it, the default gives the forced warp path's bytes, within the
+    # oracle's tolerance
+    if family != "auto":
+        pytest.skip("runs once")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    dim = 6144
+    rows = -(-sms * 128 * 3072 // dim) + 8
+    assert rows < sms * 128
+    w = synth.segmented(rows, dim, seed=77)
+    d = {k: v.to(dev) for k, v in w.inputs.items() if isinstance(v, torch.Tensor)}
+    q = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"], d["act_scale"])
+    pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"])
+    default = (q.view(torch.uint8).clone(), pk.clone(), sf.clone(), ts.clone())
+    monkeypatch.setenv("NVFP4AP_SEG_WARP", "1")
+    monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")
+    q = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"], d["act_scale"])
+    pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"])
+    for a, b in zip(default, (q.view(torch.uint8), pk, sf, ts)):
+        assert torch.equal(a, b)
+    ref = oracle.ln_quant_fp8(_u(w.inputs["x"]), 0.025, oracle.MOD_SEG, **_seg_src(w))
+    check_fp8(default[0].cpu().numpy(), ref, 0.025, "fp8 segmented above the element threshold")
