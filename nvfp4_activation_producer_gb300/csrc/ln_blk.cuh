@@ -1,8 +1,7 @@
 // ln_blk.cuh -- block-per-lane LayerNorm producer kernel template (FP8
 // e4m3fn, NVFP4 single-level, and the two passes of the two-level NVFP4
 // contract) and its launch helper, shared by the translation units that
-// instantiate it (ln_blk.cu, ln_blk2l.cu; ln_warpreg.cu uses its helpers and
-// tables).
+// instantiate it (ln_blk.cu, ln_blk2l.cu).
 //
 // Operations (adaptive-layernorm-producers README, "Available Functions",
 // "Tensor Contract"; NVFP4 encoding facts, the two-level contract and the
