@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -765,7 +766,28 @@ def oracle_sample_step(works, frac_rows: int, nthreads: int):
     return total
 
 
-def cpu_baseline(works, budget_s: float = 15.0, frac_rows: int = 8):
+def host_cpu() -> str:
+    """The host CPU's model as the OS reports it (lscpu's model name, else
+    /proc/cpuinfo), for the oracle timings."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(works, budget_s: float = 15.0, frac_rows: int = 8, single_s: float = 3.0):
+    """The oracle timed on the host cores: row-parallel over every core for
+    ~budget_s, then single-threaded for ~single_s (smaller samples)."""
     import oracle
     oracle.build()
     nthreads = oracle.default_threads()
@@ -778,9 +800,20 @@ def cpu_baseline(works, budget_s: float = 15.0, frac_rows: int = 8):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    reps1, total1 = 0, 0
+    while True:
+        total1 += oracle_sample_step(works, frac_rows * 16, 1)
+        reps1 += 1
+        if time.perf_counter() - t1 >= single_s:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(total / dt / 1e9, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"first 1/{frac_rows} of the rows of every producer of the step, repeated {reps}x "
-                      f"({dt:.1f} s, {total / 1e9:.2f} GB algorithmic)"}
+                      f"({dt:.1f} s, {total / 1e9:.2f} GB algorithmic)",
+            "single_thread": {"value": round(total1 / dt1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"first 1/{frac_rows * 16} of the rows, repeated {reps1}x ({dt1:.1f} s)"},
+            "host_cpu": host_cpu(), "nproc": os.cpu_count()}
 
 
 def run_reference(args):
