@@ -35,6 +35,11 @@
  *    A pointer that violates its op's rule gives NVFP4AP_ERR_ALIGN.
  *  - dim must be at most NVFP4AP_MAX_DIM for the LayerNorm ops (a whole row
  *    is held in registers); the six-way op has no such limit.
+ *  - Environment: each producer call reads the variables whose names start
+ *    with NVFP4AP_ (one pass over the environment per call).  They select
+ *    kernel families and launch shapes for experiments (e.g. NVFP4AP_KERNEL,
+ *    NVFP4AP_PDL=0, NVFP4AP_WARPREG=0); none is needed, and every kernel
+ *    family meets the same output contract.
  */
 #ifndef NVFP4AP_H
 #define NVFP4AP_H
