@@ -11,9 +11,12 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers to contiguous row-major memory
- *    owned by the caller.  The library never allocates, never frees, never
- *    synchronises and never reads device memory on the host, so every call
- *    can be captured in a CUDA graph with static buffers.
+ *    owned by the caller.  The producers never allocate, never free, never
+ *    synchronise and never read device memory on the host, so every producer
+ *    call can be captured in a CUDA graph with static buffers.  The only
+ *    entry points that read device memory on the host (and so synchronise)
+ *    are the diagnostics nvfp4ap_take_device_fault and
+ *    nvfp4ap_noalloc_progress.
  *  - bf16 tensors are IEEE bfloat16 bit patterns (2 bytes), e4m3 tensors are
  *    OCP float8_e4m3fn bytes, fp32 tensors are IEEE binary32.
  *  - `stream` is the CUDA stream the kernel is launched on (NULL = legacy
@@ -61,11 +64,15 @@ enum nvfp4ap_status {
   NVFP4AP_ERR_INDEX = 4,   /* chunks < 1 or shift_idx/scale_idx out of range */
   NVFP4AP_ERR_ALIGN = 5,   /* a pointer misses its alignment rule            */
   NVFP4AP_ERR_LAUNCH = 6,  /* the CUDA launch failed (cudaGetLastError)      */
-  NVFP4AP_ERR_VALUE = 7,   /* eps negative or not finite                      */
-  NVFP4AP_ERR_FAULT = 8,   /* a kernel's bounded wait ran out (see
+  NVFP4AP_ERR_TIMEOUT = 7, /* a kernel's bounded wait ran out; that kernel's
+                              output is incomplete (reported by
                               nvfp4ap_take_device_fault)                      */
-  NVFP4AP_ERR_SCRATCH = 9  /* the call needs more than the static scratch of
+  NVFP4AP_ERR_VALUE = 8,   /* eps negative or not finite                      */
+  NVFP4AP_ERR_SCRATCH = 9, /* the call needs more than the static scratch of
                               ada_layer_norm_quant_fp8_bf16_noalloc holds     */
+  NVFP4AP_ERR_FAULT = 10   /* a segmented producer met a segment index
+                              outside [0, nseg) (reported by
+                              nvfp4ap_take_device_fault)                      */
 };
 
 #define NVFP4AP_MAX_DIM 32768
@@ -86,16 +93,30 @@ const char* nvfp4ap_status_string(int status);
 /* Version of this ABI (major*10000 + minor*100 + patch). */
 int nvfp4ap_version(void);
 
-/* The LayerNorm producers stage rows through shared memory with
+/* Some LayerNorm producer kernels (the table form's default kernel and the
+ * allocation-free producer) stage rows through shared memory with
  * asynchronous bulk copies and wait on them with a bounded wait (about one
- * second).  If a wait ever runs out, the kernel stops early, leaves its
- * output incomplete and sets a fault word on the current device instead of
- * hanging.  The segmented producers set it too when a row's segment index is
- * out of range.  This call reads and clears that word: NVFP4AP_ERR_FAULT if any
- * kernel on the current device has set it since the last call, NVFP4AP_OK if
- * not, NVFP4AP_ERR_LAUNCH if the device could not be read.  Unlike every
- * other entry point it synchronises with the device (a blocking copy). */
+ * second by default).  If a wait runs out, the kernel waits (with that same
+ * default bound) for every copy it still has in flight, stops early, leaves
+ * its output incomplete and sets a device word instead of hanging.  The
+ * segmented producers set a second word when a row's segment index is out
+ * of range.  This call reads and clears both words on the current device:
+ * NVFP4AP_ERR_TIMEOUT if a wait ran out since the last call (it takes
+ * precedence), else NVFP4AP_ERR_FAULT if a segment index was out of range,
+ * else NVFP4AP_OK; NVFP4AP_ERR_LAUNCH if the device could not be read.
+ * Unlike the producers it synchronises with the device (a blocking copy). */
 int nvfp4ap_take_device_fault(void);
+
+/* The bound of those waits, for testing the failure path: `cycles` SM clock
+ * cycles after a first non-blocking test of the copy; cycles <= 0 restores the
+ * default (2e9 cycles, about one second).  A very small bound makes the first
+ * wait of each CTA give up before its copy lands, so a test can check the
+ * report above; the copies in flight are still waited for with the default
+ * bound before the kernel returns.  Process-wide, read when a producer is
+ * launched (a captured graph keeps the bound it was captured with).  Returns
+ * NVFP4AP_OK.  nvfp4ap_wait_limit returns the bound in effect. */
+int nvfp4ap_set_wait_limit(int64_t cycles);
+int64_t nvfp4ap_wait_limit(void);
 
 /* ------------------------------------------------------------------------
  * FP8 producers.  For each row r of x (rows, dim) bf16:
@@ -116,15 +137,19 @@ int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* 
 
 /* No counterpart in the paper: an addition of this library.
  *
- * ada_layer_norm_quant_fp8_bf16_noalloc computes exactly what
- * ada_layer_norm_quant_fp8_bf16 computes, with the same arguments, for callers
- * that cannot allocate device memory at all -- for example code that runs
- * under a device-memory budget fixed at start-up, or inside a framework region
- * whose caching allocator must not grow.  It runs the TMA ring kernel, which
- * keeps one progress word per CTA (rows finished; bit 31 set if one of the
- * CTA's bounded waits ran out) in device scratch; here that scratch is a fixed
- * array inside the library, 1024 words (4 KB), 256-byte aligned, which every
- * GPU that loads the library holds until the process exits.  The call
+ * ada_layer_norm_quant_fp8_bf16_noalloc computes the same operation as
+ * ada_layer_norm_quant_fp8_bf16, with the same arguments and within the same
+ * bounds against the library's reference (its kernel takes the row statistics
+ * in two passes, so a byte can differ by one code step from the default
+ * kernel's), for callers that cannot allocate device memory at all -- for
+ * example code that runs under a device-memory budget fixed at start-up, or
+ * inside a framework region whose caching allocator must not grow.  It runs
+ * the TMA ring kernel, which keeps one progress word per CTA (rows finished;
+ * bit 31 set if one of the CTA's bounded waits ran out) in device scratch;
+ * here that scratch is a fixed array inside the library, 1024 words (4 KB),
+ * 256-byte aligned, which every GPU that loads the library holds until the
+ * process exits.  The words of the last call can be read back with
+ * nvfp4ap_noalloc_progress (diagnostics).  The call
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine):
  * it clears the words it will use with cudaMemsetAsync on `stream`, then
  * launches.
@@ -143,6 +168,17 @@ int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* 
 int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const void* scale, const void* shift,
                                           const float* act_scale, float eps, void* out,
                                           int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
+
+/* No counterpart in the paper: diagnostics of the allocation-free producer.
+ * *used (if not NULL) receives the CTA count of the last
+ * ada_layer_norm_quant_fp8_bf16_noalloc launch on the current device (0 before
+ * the first); the first min(n, *used) progress words of that launch are
+ * copied into the host array `words` (if not NULL and n > 0): each holds the
+ * rows its CTA finished in bits 0-30 and bit 31 if one of its waits ran out,
+ * so after a complete call the words sum to rows.  A blocking read of device
+ * memory (synchronises with the device); a later call overwrites the words.
+ * Returns NVFP4AP_OK, or NVFP4AP_ERR_LAUNCH if the device could not be read. */
+int nvfp4ap_noalloc_progress(uint32_t* words, int64_t n, int64_t* used);
 
 /* README "Available Functions": ada_layer_norm_quant_fp8_ptok_bf16.
  * scale, shift: (rows, dim) bf16, one row of modulation per token. */

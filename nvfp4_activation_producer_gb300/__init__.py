@@ -41,12 +41,19 @@ __all__ = [
     "library_path",
     "marshalling",
     "take_device_fault",
+    "set_wait_limit",
+    "wait_limit",
+    "noalloc_progress",
     "NvFp4ApError",
+    "NvFp4ApArgumentError",
 ]
 
 LIB_PATH = _build.LIB
 
-OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_VALUE, ERR_FAULT, ERR_SCRATCH = range(10)
+(OK, ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_LAUNCH, ERR_TIMEOUT, ERR_VALUE, ERR_SCRATCH,
+ ERR_FAULT) = range(11)
+# statuses that report a bad argument (the binding raises them as ValueError too)
+_ARG_ERRORS = (ERR_NULL, ERR_SHAPE, ERR_DIM, ERR_INDEX, ERR_ALIGN, ERR_VALUE, ERR_SCRATCH)
 MAX_DIM = 32768
 SWIGLU_WORKSPACE_BYTES = 4  # the SwiGLU two-level producer keeps only the maximum word
 
@@ -61,11 +68,17 @@ def workspace_2level_bytes(rows: int) -> int:
 
 
 class NvFp4ApError(RuntimeError):
-    """A non-zero status from the C ABI."""
+    """A non-zero status from the C ABI (launch, timeout and device-fault
+    statuses are raised as this class)."""
 
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__(f"{fn}: status {status}: {msg}")
         self.status = status
+
+
+class NvFp4ApArgumentError(NvFp4ApError, ValueError):
+    """A status that reports a bad argument (null pointer, shape, dim, index,
+    alignment, eps, scratch size): both a NvFp4ApError and a ValueError."""
 
 
 _lib = None
@@ -152,6 +165,12 @@ def _declare(L: ctypes.CDLL) -> None:
     L.nvfp4ap_version.argtypes = []
     L.nvfp4ap_take_device_fault.restype = i32
     L.nvfp4ap_take_device_fault.argtypes = []
+    L.nvfp4ap_set_wait_limit.restype = i32
+    L.nvfp4ap_set_wait_limit.argtypes = [i64]
+    L.nvfp4ap_wait_limit.restype = i64
+    L.nvfp4ap_wait_limit.argtypes = []
+    L.nvfp4ap_noalloc_progress.restype = i32
+    L.nvfp4ap_noalloc_progress.argtypes = [p, i64, ctypes.POINTER(ctypes.c_int64)]
     for name in ("ada_layer_norm_quant_fp8_bf16", "ada_layer_norm_quant_fp8_ptok_bf16"):
         fn = getattr(L, name)
         fn.restype = i32
@@ -196,8 +215,33 @@ def _declare(L: ctypes.CDLL) -> None:
 
 def take_device_fault() -> None:
     """Raise NvFp4ApError if a producer kernel on the current device ran out of
-    its bounded wait since the last check (synchronises with the device)."""
+    its bounded wait (status ERR_TIMEOUT) or met an out-of-range segment index
+    (ERR_FAULT) since the last check (synchronises with the device)."""
     _raise("nvfp4ap_take_device_fault", _load().nvfp4ap_take_device_fault())
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Bound of the TMA kernels' waits in SM clock cycles (<= 0: the default,
+    about one second); for tests of the failure path."""
+    _raise("nvfp4ap_set_wait_limit", _load().nvfp4ap_set_wait_limit(int(cycles)))
+
+
+def wait_limit() -> int:
+    """The bound of the TMA kernels' waits in effect, in SM clock cycles."""
+    return int(_load().nvfp4ap_wait_limit())
+
+
+def noalloc_progress():
+    """Per-CTA progress words of the last allocation-free launch on the current
+    device, as a list of ints (rows finished in bits 0-30, bit 31 if a wait
+    ran out); a blocking read."""
+    L = _load()
+    used = ctypes.c_int64(0)
+    _raise("nvfp4ap_noalloc_progress", L.nvfp4ap_noalloc_progress(None, 0, ctypes.byref(used)))
+    n = used.value
+    words = (ctypes.c_uint32 * max(n, 1))()
+    _raise("nvfp4ap_noalloc_progress", L.nvfp4ap_noalloc_progress(words, n, ctypes.byref(used)))
+    return [int(w) for w in words[:n]]
 
 
 def library_path() -> str:
@@ -208,7 +252,7 @@ def library_path() -> str:
 def _raise(fn: str, rc: int):
     if rc != OK:
         msg = _load().nvfp4ap_status_string(rc).decode()
-        raise NvFp4ApError(fn, rc, msg)
+        raise (NvFp4ApArgumentError if rc in _ARG_ERRORS else NvFp4ApError)(fn, rc, msg)
 
 
 # ---------------------------------------------------------------------------

@@ -4,6 +4,7 @@
 // indices, pointer alignment, eps), picks the kernel variant and launch shape
 // from dim, launches on the caller's stream and returns a status.  Nothing
 // here allocates, synchronises or touches device memory.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -254,7 +255,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   RingShape rs{};
   if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
-    if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, st));
+    if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, wait_limit_cycles(), st));
   }
   RowShape rows_shape{};
   if (vec8 && (kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
@@ -262,7 +263,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     const int sms = sm_count();
     if (kernel == 4 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
       return finish(launch_ln_tma(a, false, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
-                                  env_int("NVFP4AP_TMA_CTAS"), st));
+                                  env_int("NVFP4AP_TMA_CTAS"), wait_limit_cycles(), st));
     if (mod_is_bcast(mod) && persist_ok(rows_shape) && sms > 0)
       return finish(
           launch_ln_bcast_persistent(a, false, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
@@ -421,7 +422,7 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   RingShape rs{};
   if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
     const int sms = sm_count();
-    if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, st));
+    if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, wait_limit_cycles(), st));
   }
   RowShape rows_shape{};
   if ((kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
@@ -430,7 +431,7 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
     const int sms = sm_count();
     if (kernel == 4 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
       return finish(launch_ln_tma(a, true, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
-                                  env_int("NVFP4AP_TMA_CTAS"), st));
+                                  env_int("NVFP4AP_TMA_CTAS"), wait_limit_cycles(), st));
     // four rows of a scale tile per CTA (whole 16-byte scale chunks): opt-in
     // with NVFP4AP_TILE4=1 -- measured slower on GB300 than one row per CTA
     const bool tile4 = env_int("NVFP4AP_TILE4") > 0 && rows_shape.tpr <= 128 && rows_shape.per_thread <= 4 &&
@@ -469,6 +470,18 @@ LnArgs ln_args(const void* x, float eps, void* out, int64_t rows, int64_t dim) {
 }
 
 }  // namespace
+
+// Bound of the TMA kernels' mbarrier waits (SM clock cycles); 0 = the
+// default, about one second at 2 GHz.
+namespace {
+constexpr long long kDefaultWaitCycles = 2000000000LL;
+std::atomic<long long> g_wait_limit{0};
+}  // namespace
+
+long long wait_limit_cycles() {
+  const long long v = g_wait_limit.load(std::memory_order_relaxed);
+  return v > 0 ? v : kDefaultWaitCycles;
+}
 
 bool pdl_enabled() {
   const char* v = env_get("NVFP4AP_PDL");
@@ -521,8 +534,10 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
     case NVFP4AP_ERR_ALIGN: return "a pointer misses its alignment rule";
     case NVFP4AP_ERR_LAUNCH: return "CUDA launch failed";
     case NVFP4AP_ERR_VALUE: return "eps is negative or not finite";
+    case NVFP4AP_ERR_TIMEOUT:
+      return "a kernel's bounded wait ran out: its output is incomplete (read by nvfp4ap_take_device_fault)";
     case NVFP4AP_ERR_FAULT:
-      return "a producer kernel's bounded wait ran out, or a segment index was out of range (see the output)";
+      return "a segment index was outside [0, nseg): that row was produced with zero modulation";
     case NVFP4AP_ERR_SCRATCH: return "the call needs more per-CTA words than the library's static scratch array holds";
     default: return "unknown status";
   }
@@ -531,6 +546,7 @@ NVFP4AP_EXPORT const char* nvfp4ap_status_string(int status) {
 NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
+  // wait words (ring and TMA kernels), then the segment-index words
   unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u, k = 0u;
   if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess ||
       take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess ||
@@ -538,7 +554,19 @@ NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  return (f | g | h | i | j | k) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  if (f | g) return NVFP4AP_ERR_TIMEOUT;
+  return (h | i | j | k) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+}
+
+NVFP4AP_EXPORT int nvfp4ap_set_wait_limit(int64_t cycles) {
+  g_wait_limit.store(cycles > 0 ? (long long)cycles : 0LL, std::memory_order_relaxed);
+  return NVFP4AP_OK;
+}
+
+NVFP4AP_EXPORT int64_t nvfp4ap_wait_limit(void) { return (int64_t)wait_limit_cycles(); }
+
+NVFP4AP_EXPORT int nvfp4ap_noalloc_progress(uint32_t* words, int64_t n, int64_t* used) {
+  return noalloc_progress(words, n, used);
 }
 
 NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const void* shift,
@@ -569,7 +597,7 @@ NVFP4AP_EXPORT int ada_layer_norm_quant_fp8_bf16_noalloc(const void* x, const vo
   a.scale = static_cast<const uint16_t*>(scale);
   a.shift = static_cast<const uint16_t*>(shift);
   a.act_scale = act_scale;
-  rc = noalloc_fp8_bcast(a, sms, reinterpret_cast<cudaStream_t>(stream));
+  rc = noalloc_fp8_bcast(a, sms, wait_limit_cycles(), reinterpret_cast<cudaStream_t>(stream));
   if (rc == NVFP4AP_ERR_LAUNCH) (void)cudaGetLastError();
   return rc;
 }

@@ -7,6 +7,10 @@
 
 namespace nvfp4ap {
 
+// Bound of every mbarrier wait of the TMA kernels in SM clock cycles (about
+// one second unless nvfp4ap_set_wait_limit changed it).
+long long wait_limit_cycles();
+
 // Launch `k` on `st` with programmatic stream serialisation (PDL) unless
 // NVFP4AP_PDL=0: the kernel may then be dispatched while the previous kernel
 // on the stream drains (the kernel itself waits for it, see pdl_enter()).
@@ -174,11 +178,16 @@ struct RingShape {
   int warps, stages, ctas_per_sm;
 };
 int64_t ring_smem_bytes(int mod, int64_t dim, int warps, int stages);
-cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, cudaStream_t st);
+cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, long long wait_limit,
+                           cudaStream_t st);
 // FP8 broadcast producer on the ring kernel with its per-CTA words in the
 // library's static scratch array; returns an NVFP4AP_* status (arguments
 // already validated, dim % 8 == 0, 16-byte aligned inputs).
-int noalloc_fp8_bcast(const LnArgs& a, int sms, cudaStream_t st);
+int noalloc_fp8_bcast(const LnArgs& a, int sms, long long wait_limit, cudaStream_t st);
+// Copies the first min(n, used) per-CTA words of the last allocation-free
+// launch on the current device into `words` (a synchronising read); *used =
+// that launch's CTA count (0 if none yet).
+int noalloc_progress(unsigned int* words, int64_t n, int64_t* used);
 // Reads and clears the fault word the ring kernels set when a bounded wait
 // runs out (synchronising copy).
 cudaError_t take_ring_fault(unsigned int* fault);
@@ -188,7 +197,7 @@ cudaError_t take_ring_fault(unsigned int* fault);
 // shared-memory stages by bulk copies.  forced_stages / ctas_per_sm: 0 = auto.
 bool ln_tma_supported(bool nvfp4, int mod, RowShape s);
 cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
-                          int ctas_per_sm, cudaStream_t st);
+                          int ctas_per_sm, long long wait_limit, cudaStream_t st);
 cudaError_t take_tma_fault(unsigned int* fault);
 
 // Segmented modulation (MOD_SEG) on the register row kernels: FP8 (dim % 8

@@ -17,11 +17,16 @@
 //  * a warp reduces its row with shuffles only (no CTA barrier in the loop),
 //    reading the staged row from shared memory three times (sum, centred sum
 //    of squares, output), and writes the codes straight to global memory;
-//  * every mbarrier wait is bounded (kWaitCycles); on expiry the warp sets
-//    the library's fault word and stops instead of spinning forever.
+//  * every mbarrier wait is bounded by the `wait_limit` argument (SM clock
+//    cycles; the library passes about one second); on expiry lane 0 waits,
+//    with the library's normal bound, for every copy the warp has in flight
+//    (the one whose wait ran out included), then sets the library's fault
+//    word and the warp stops, so no copy is left writing into the shared
+//    memory of a warp -- or a CTA -- that has exited.
 #include <mutex>
 
 #include "device.cuh"
+#include "nvfp4ap.h"
 #include "kernels.h"
 #include "tma.cuh"
 
@@ -183,7 +188,8 @@ __device__ __forceinline__ void nvfp4_row(const LnArgs& a, int64_t row, const ui
 // `cta_state` (may be null): one word per CTA; each warp adds the number of
 // rows it finished, and bit 31 marks a CTA one of whose waits ran out.
 template <int KIND, int MOD>
-__global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int S, unsigned int* cta_state) {
+__global__ void __launch_bounds__(512)
+    ln_ring_kernel(const LnArgs a, const int S, unsigned int* cta_state, const long long wait_limit) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int W = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t D = a.dim;
@@ -219,8 +225,11 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
   uint64_t* wb = bars + w * S;
   const float inv_act = KIND == KIND_FP8 ? 1.0f / __ldg(a.act_scale) : 0.f;
 
+  uint32_t pending = 0u;  // lane 0: stages with a copy in flight
+  uint32_t phase = 0u;    // lane 0: parity of each stage's next completion
   auto issue = [&](int64_t row, int s) {
     uint8_t* dst = ring + (size_t)s * stage_bytes;
+    pending |= 1u << s;
     mbar_expect_tx(&wb[s], stage_bytes);
     bulk_g2s(dst, a.x + row * D, xbytes, &wb[s]);
     if constexpr (MOD == MOD_PTOK) {
@@ -244,9 +253,12 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
   uint32_t parity = 0u;
   unsigned int done = 0u;
   for (int64_t row = gw; row < a.rows; row += G) {
-    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&wb[s], parity));
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&wb[s], parity, wait_limit));
     if (!ok) {
       if (lane == 0) {
+        // drain: every issued copy of this warp, the expired one included
+        for (int q = 0; q < S; ++q)
+          if (pending & (1u << q)) (void)mbar_wait(&wb[q], (phase >> q) & 1u);
         atomicOr(&g_ring_fault, 1u);
         if (cta_state) atomicOr(&cta_state[blockIdx.x], 0x80000000u);
       }
@@ -258,6 +270,8 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
     else nvfp4_row<MOD>(a, row, stage, cst, lane);
     __syncwarp();
     if (lane == 0) {
+      pending &= ~(1u << s);
+      phase ^= 1u << s;
       const int64_t nr = row + (int64_t)S * G;
       if (nr < a.rows) issue(nr, s);
     }
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(512) ln_ring_kernel(const LnArgs a, const int 
   }
 }
 
-using RingKernel = void (*)(const LnArgs, const int, unsigned int*);
+using RingKernel = void (*)(const LnArgs, const int, unsigned int*, const long long);
 
 RingKernel pick(int kind, int mod) {
   if (kind == KIND_FP8) {
@@ -325,7 +339,8 @@ int ring_occupancy(RingKernel k, int threads, int64_t smem) {
   return occ;
 }
 
-cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, cudaStream_t st) {
+cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, long long wait_limit,
+                           cudaStream_t st) {
   RingKernel k = pick(nvfp4 ? KIND_NVFP4 : KIND_FP8, mod);
   if (!k) return cudaErrorInvalidValue;
   const int64_t smem = ring_smem_bytes(mod, a.dim, rs.warps, rs.stages);
@@ -336,7 +351,7 @@ cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, i
   const int64_t work_rows = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
   int64_t grid = (work_rows + rs.warps - 1) / rs.warps;
   if (grid > (int64_t)sms * occ) grid = (int64_t)sms * occ;
-  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, nullptr);
+  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, nullptr, wait_limit);
   return cudaGetLastError();
 }
 
@@ -364,26 +379,48 @@ static unsigned int* noalloc_scratch(int dev) {
   return addr[dev];
 }
 
-int noalloc_fp8_bcast(const LnArgs& a, int sms, cudaStream_t st) {
+// CTAs of the last allocation-free launch per device (host-side record for
+// noalloc_progress)
+static int64_t g_noalloc_ctas[64] = {0};
+
+int noalloc_fp8_bcast(const LnArgs& a, int sms, long long wait_limit, cudaStream_t st) {
   // ring shape as for the allocating path: 8 warps, up to 4 stages in ~110 KB
   RingShape rs{8, 4, 0};
   while (rs.stages > 1 && ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages) > 110 * 1024) --rs.stages;
   while (rs.warps > 1 && ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages) > 110 * 1024) --rs.warps;
   const int64_t smem = ring_smem_bytes(MOD_BCAST, a.dim, rs.warps, rs.stages);
-  if (smem > 227 * 1024) return 3;  // NVFP4AP_ERR_DIM
+  if (smem > 227 * 1024) return NVFP4AP_ERR_DIM;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 6;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4AP_ERR_LAUNCH;
   unsigned int* state = noalloc_scratch(dev);
-  if (!state) return 6;  // NVFP4AP_ERR_LAUNCH
+  if (!state) return NVFP4AP_ERR_LAUNCH;
   RingKernel k = ln_ring_kernel<KIND_FP8, MOD_BCAST>;
   const int occ = ring_occupancy(k, rs.warps * 32, smem);
-  if (occ < 1) return 6;
+  if (occ < 1) return NVFP4AP_ERR_LAUNCH;
   int64_t grid = (a.rows + rs.warps - 1) / rs.warps;
   if (grid > (int64_t)sms * occ) grid = (int64_t)sms * occ;
-  if (grid > kNoAllocMaxCtas) return 9;  // NVFP4AP_ERR_SCRATCH
-  if (cudaMemsetAsync(state, 0, (size_t)grid * sizeof(unsigned int), st) != cudaSuccess) return 6;
-  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, state);
-  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+  if (grid > kNoAllocMaxCtas) return NVFP4AP_ERR_SCRATCH;
+  if (cudaMemsetAsync(state, 0, (size_t)grid * sizeof(unsigned int), st) != cudaSuccess) return NVFP4AP_ERR_LAUNCH;
+  k<<<(unsigned)grid, rs.warps * 32, (size_t)smem, st>>>(a, rs.stages, state, wait_limit);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4AP_ERR_LAUNCH;
+  g_noalloc_ctas[dev] = grid;
+  return NVFP4AP_OK;
+}
+
+int noalloc_progress(unsigned int* words, int64_t n, int64_t* used) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4AP_ERR_LAUNCH;
+  const int64_t m = g_noalloc_ctas[dev];
+  if (used) *used = m;
+  if (!words || n <= 0 || m == 0) return NVFP4AP_OK;
+  unsigned int* state = noalloc_scratch(dev);
+  if (!state) return NVFP4AP_ERR_LAUNCH;
+  const int64_t k = n < m ? n : m;
+  if (cudaMemcpy(words, state, (size_t)k * sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NVFP4AP_ERR_LAUNCH;
+  }
+  return NVFP4AP_OK;
 }
 
 cudaError_t take_ring_fault(unsigned int* fault) {

@@ -20,9 +20,12 @@
 //    registers and written with streaming stores;
 //  * broadcast scale/shift and the fp32 table rows are the same for every row
 //    of a CTA: they are converted once into fp32 registers;
-//  * every mbarrier wait is bounded (about one second); a CTA whose wait runs
-//    out (decided CTA-wide at the reduction barrier) waits, again bounded, for
-//    its copies still in flight, sets the fault word and returns.
+//  * every mbarrier wait is bounded by the `wait_limit` argument (SM clock
+//    cycles; the library passes about one second); a CTA whose wait runs out
+//    (decided CTA-wide at the reduction barrier) waits, with the library's
+//    normal bound, for every copy it has in flight -- the one whose wait ran
+//    out included -- then sets the fault word and returns, so no copy is
+//    left writing into the shared memory of a CTA that has exited.
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -47,7 +50,8 @@ __device__ __forceinline__ void unpack4(uint4 v, uint32_t (&w)[4]) {
 
 // FULL: the row is exactly NV * tpr chunks (no chunk-validity checks).
 template <int KIND, int MOD, int NV, bool FULL = false>
-__global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float inv_d, const int S) {
+__global__ void __launch_bounds__(256)
+    ln_tma_kernel(const LnArgs a, const float inv_d, const int S, const long long wait_limit) {
   constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
   constexpr bool kConst = (MOD == MOD_BCAST || MOD == MOD_TABLE);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
   int s = 0, par = 0;
   uint32_t parity = 0u;
   for (int64_t row = blockIdx.x; row < a.rows; row += Gr) {
-    const bool ok = mbar_wait(&bars[s], parity);
+    const bool ok = mbar_wait_bounded(&bars[s], parity, wait_limit);
     const uint8_t* st = stages + (size_t)s * stage_bytes;
     const uint4* xs = reinterpret_cast<const uint4*>(st);
     const float K = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(st)) << 16);
@@ -190,7 +194,6 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
     if (bad) {
       // the CTA stops: wait (bounded) for its copies still in flight, then report
       if (t == 0) {
-        pending &= ~(1u << s);  // the copy whose wait ran out
         for (int q = 0; q < S; ++q)
           if (pending & (1u << q)) (void)mbar_wait(&bars[q], (phase >> q) & 1u);
         atomicOr(&g_tma_fault, 1u);
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(256) ln_tma_kernel(const LnArgs a, const float
   }
 }
 
-using TmaKernel = void (*)(const LnArgs, const float, const int);
+using TmaKernel = void (*)(const LnArgs, const float, const int, const long long);
 
 template <int KIND, int MOD>
 TmaKernel pick_nv(int nv, bool full) {
@@ -390,7 +393,7 @@ bool ln_tma_supported(bool nvfp4, int mod, RowShape s) {
 }
 
 cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
-                          int ctas_per_sm, cudaStream_t st) {
+                          int ctas_per_sm, long long wait_limit, cudaStream_t st) {
   // rows that exactly fill the threads' chunks take the FULL instance
   // (NVFP4AP_FULL=0 turns it off)
   const char* full_env = env_get("NVFP4AP_FULL");
@@ -405,7 +408,7 @@ cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int 
   if (grid > a.rows) grid = a.rows;
   const float inv_d = (float)(1.0 / (double)a.dim);
   return launch_maybe_pdl(k, dim3((unsigned)grid), dim3(s.tpr), (size_t)tma_smem(mod, a.dim, p.stages), st, a,
-                          inv_d, p.stages);
+                          inv_d, p.stages, wait_limit);
 }
 
 cudaError_t take_tma_fault(unsigned int* fault) {

@@ -32,13 +32,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0u;
 }
-// Bounded wait for the phase with the given parity; false when it ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p;\n"
+      "  mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Wait for the phase with the given parity: a first non-blocking test, then
+// (potentially blocking) tries while fewer than `limit` SM clock cycles have
+// passed; false when it ran out.  A limit of a few cycles gives up right
+// after the first test.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
-  return true;
+  while (clock64() - t0 <= limit)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// The same with the library's normal bound (~1 s).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_bounded(bar, parity, kWaitCycles);
 }
 // 1-D bulk copy global -> shared (this CTA), completing `bytes` on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

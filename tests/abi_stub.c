@@ -155,4 +155,11 @@ int64_t nvfp4ap_2level_workspace_bytes(int64_t rows) { return 16 + 16 * rows; }
 const char* nvfp4ap_status_string(int status) { return status ? "stub status" : "ok"; }
 int nvfp4ap_version(void) { return 0; }
 int nvfp4ap_take_device_fault(void) { return 0; }
+int nvfp4ap_set_wait_limit(int64_t cycles) { (void)cycles; return 0; }
+int64_t nvfp4ap_wait_limit(void) { return 0; }
+int nvfp4ap_noalloc_progress(uint32_t* words, int64_t n, int64_t* used) {
+  (void)words; (void)n;
+  if (used) *used = 0;
+  return 0;
+}
 int64_t swizzled_sf_size(int64_t rows, int64_t dim) { return (rows + 127) / 128 * 128 * ((dim / 16 + 3) / 4 * 4); }

@@ -39,15 +39,43 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 23
+    assert len(declared) == 26
 
 
 def test_status_strings_and_version(lib):
     L, _ = lib
-    for s in range(10):
-        assert L.nvfp4ap_status_string(s)
+    for s in range(11):
+        assert L.nvfp4ap_status_string(s) != b"unknown status"
     assert L.nvfp4ap_status_string(99) == b"unknown status"
+    # the status values of the boundary's contract
+    import nvfp4_activation_producer_gb300 as ap
+    assert (ap.ERR_NULL, ap.ERR_SHAPE, ap.ERR_DIM, ap.ERR_INDEX, ap.ERR_ALIGN, ap.ERR_LAUNCH, ap.ERR_TIMEOUT) == tuple(
+        range(1, 8))
+    assert b"wait ran out" in L.nvfp4ap_status_string(ap.ERR_TIMEOUT)
+    assert b"segment index" in L.nvfp4ap_status_string(ap.ERR_FAULT)
     assert L.nvfp4ap_version() >= 100
+
+
+def test_wait_limit_setting(lib):
+    # the bound of the TMA kernels' waits: set, read back, default restored
+    L, _ = lib
+    assert L.nvfp4ap_set_wait_limit(1000) == 0
+    assert L.nvfp4ap_wait_limit() == 1000
+    assert L.nvfp4ap_set_wait_limit(0) == 0
+    assert L.nvfp4ap_wait_limit() == 2000000000
+    assert L.nvfp4ap_set_wait_limit(-5) == 0
+    assert L.nvfp4ap_wait_limit() == 2000000000
+
+
+def test_argument_statuses_raise_value_errors():
+    import nvfp4_activation_producer_gb300 as ap
+    for rc in (ap.ERR_NULL, ap.ERR_SHAPE, ap.ERR_DIM, ap.ERR_INDEX, ap.ERR_ALIGN, ap.ERR_VALUE, ap.ERR_SCRATCH):
+        with pytest.raises(ValueError):
+            ap._raise("f", rc)
+    for rc in (ap.ERR_LAUNCH, ap.ERR_TIMEOUT, ap.ERR_FAULT):
+        with pytest.raises(RuntimeError) as e:
+            ap._raise("f", rc)
+        assert not isinstance(e.value, ValueError)
 
 
 def test_swizzled_sf_size_matches_oracle_and_pages(lib, orc, golden_dir):
@@ -72,8 +100,8 @@ def test_fp8_argument_errors(lib):
     assert f(A, A, A, A, 1e-5, A, 4, 0, NULL) == 2            # dim 0
     assert f(A, A, A, A, 1e-5, A, 4, 63, NULL) == 3           # odd dim
     assert f(A, A, A, A, 1e-5, A, 4, 32770, NULL) == 3        # above the maximum dim
-    assert f(A, A, A, A, -1.0, A, 4, 64, NULL) == 7           # negative eps
-    assert f(A, A, A, A, float("nan"), A, 4, 64, NULL) == 7   # NaN eps
+    assert f(A, A, A, A, -1.0, A, 4, 64, NULL) == 8           # negative eps
+    assert f(A, A, A, A, float("nan"), A, 4, 64, NULL) == 8   # NaN eps
     assert f(NULL, A, A, A, 1e-5, A, 4, 64, NULL) == 1        # null x
     assert f(A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1        # null scale
     assert f(A, A, A, NULL, 1e-5, A, 4, 64, NULL) == 1        # null act_scale
@@ -111,7 +139,7 @@ def test_nvfp4_argument_errors(lib):
     assert f(A, A, A, 1e-5, A, A, 0, 64, NULL) == 0
     g = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16
     assert g(A, 1e-5, A, A, -3, 64, NULL) == 2
-    assert g(A, float("inf"), A, A, 3, 64, NULL) == 7
+    assert g(A, float("inf"), A, A, 3, 64, NULL) == 8
 
 
 def test_modfp8_and_awq_argument_errors(lib):
@@ -122,13 +150,13 @@ def test_modfp8_and_awq_argument_errors(lib):
     assert m(A, A, A, A + 2, A, A, 1e-5, A, 4, 64, NULL) == 5     # scale_deq misaligned
     assert m(A, A + 1, A, A, A, A, 1e-5, A, 4, 64, NULL) == 5     # e4m3 vector at an odd address
     assert m(A, A, A, A, A, A, 1e-5, A, 4, 63, NULL) == 3         # odd dim
-    assert m(A, A, A, A, A, A, -2.0, A, 4, 64, NULL) == 7
+    assert m(A, A, A, A, A, A, -2.0, A, 4, 64, NULL) == 8
     assert m(NULL, NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0
     w = L.awq_ada_layer_norm_quant_fp8_bf16  # x, scale, shift, inv_s, act, eps, out, rows, dim
     assert w(A, A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1         # null inv_s
     assert w(A, A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1         # null shift
     assert w(A, A, A, A + 2, A, 1e-5, A, 4, 64, NULL) == 5        # inv_s not 4-byte aligned
-    assert w(A, A, A, A, A, float("nan"), A, 4, 64, NULL) == 7
+    assert w(A, A, A, A, A, float("nan"), A, 4, 64, NULL) == 8
     assert w(A, A, A, A, A, 1e-5, A, 4, 32770, NULL) == 3
     n = L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16  # x, s8, h8, sdeq, hdeq, eps, packed, sf, rows, dim
     assert n(A, A, A, A, A, 1e-5, A, A, 4, 40, NULL) == 3         # dim % 16
@@ -178,7 +206,7 @@ def test_seg_and_two_level_argument_errors(lib):
     assert v(A, A, 64, NULL, 4, 64, NULL) == 1
     c = L.ada_layer_norm_quant_nvfp4_2level_seg_bf16  # x, idx, s, h, nseg, eps, packed, sf, ts, ws, rows, dim
     assert c(A, A, A, A, -1, 1e-5, A, A, A, A, 4, 64, NULL) == 4
-    assert c(A, A, A, A, 2, float("nan"), A, A, A, A, 4, 64, NULL) == 7
+    assert c(A, A, A, A, 2, float("nan"), A, A, A, A, 4, 64, NULL) == 8
 
 
 def test_modulation6_argument_errors(lib):
