@@ -26,16 +26,18 @@
  *    been launched and no memory has been touched, except NVFP4AP_ERR_LAUNCH,
  *    which reports the CUDA error of the launch itself.
  *  - rows == 0 (or batch*seq == 0) is a valid no-op; pointers may then be NULL.
- *  - Alignment: x, scale, shift, temb, table and the outputs take a 16-byte
- *    vector path when every pointer is 16-byte aligned and dim is a multiple
- *    of 8; the FP8 ops otherwise fall back to a 4-byte (bf16 pair) path that
- *    needs 4-byte aligned bf16 inputs and 2-byte aligned outputs.  The NVFP4
- *    ops need 16-byte aligned x/scale/shift and an 8-byte aligned `packed`.
- *    e4m3 (dim,) inputs (scale_fp8, shift_fp8) count as aligned for the
- *    vector path at 8 bytes and for the pair path at 2 bytes (NVFP4: 8 bytes,
- *    else NVFP4AP_ERR_ALIGN); inv_s follows the bf16 rules; fp32 scalars
- *    (act_scale, scale_deq, shift_deq) must be 4-byte aligned.
- *    A pointer that violates its op's rule gives NVFP4AP_ERR_ALIGN.
+ *  - Alignment (the tensor contract asks for contiguity only): the
+ *    LayerNorm producers, single-level, accept any element-aligned pointers
+ *    -- bf16 tensors at 2 bytes, fp32 tables, scalars and segment indices at
+ *    4, e4m3 vectors and the outputs at 1.  They run vectorised kernels when
+ *    x, scale, shift, temb, inv_s and the segment tables are 16-byte aligned,
+ *    the table 16 (FP8) or 8 bytes, the outputs 8 bytes and the e4m3 vectors
+ *    8 bytes (FP8 also has a bf16-pair path at 4/2 bytes), and otherwise an
+ *    element-wise kernel (one load per element, byte stores) with the same
+ *    results within the same bounds.  A pointer that is not even
+ *    element-aligned gives NVFP4AP_ERR_ALIGN.  The two-level, SwiGLU,
+ *    six-way and allocation-free entry points keep the alignment rules
+ *    stated beside them (NVFP4AP_ERR_ALIGN otherwise).
  *  - dim must be at most NVFP4AP_MAX_DIM for the LayerNorm ops (a whole row
  *    is held in registers); the six-way op has no such limit.
  *  - Environment: each producer call reads the variables whose names start
@@ -228,9 +230,9 @@ int awq_ada_layer_norm_quant_fp8_bf16(const void* x, const void* scale, const vo
 /* Segmented modulation (h3-blackwell-runtime compare page: segment-specific
  * shift and scale selection with a per-row segment index).
  * seg_idx: device (rows,) int32, 4-byte aligned; row r takes row seg_idx[r] of
- * seg_scale, seg_shift: device (nseg, dim) bf16, 16-byte aligned.
+ * seg_scale, seg_shift: device (nseg, dim) bf16.
  *   y[d] = (x[r,d] - mean) * rstd * (1 + seg_scale[g,d]) + seg_shift[g,d]
- * dim % 8 == 0 and x 16-byte aligned (NVFP4AP_ERR_DIM / _ALIGN otherwise).
+ * dim even (FP8) or a multiple of 16 (NVFP4), else NVFP4AP_ERR_DIM.
  * nseg < 1 gives NVFP4AP_ERR_INDEX.  An index outside [0, nseg) cannot be
  * checked on the host: that row is produced with zero modulation and the
  * device fault word is set (nvfp4ap_take_device_fault). */
@@ -258,7 +260,7 @@ int layer_norm_no_affine_quant_fp8_static_bf16(const void* x, const float* act_s
  *   and every padding byte of the swizzled buffer (rows up to a multiple of
  *   128, block columns up to a multiple of 4) is written as 0.
  * dim % 16 == 0.  packed: rows*dim/2 bytes; sf_swizzled:
- * swizzled_sf_size(rows, dim) bytes.
+ * swizzled_sf_size(rows, dim) bytes (any alignment, see the conventions).
  * ---------------------------------------------------------------------- */
 
 /* README "Available Functions": ada_layer_norm_quant_nvfp4_swizzled_bf16.
@@ -268,7 +270,7 @@ int ada_layer_norm_quant_nvfp4_swizzled_bf16(const void* x, const void* scale, c
                                              int64_t rows, int64_t dim, nvfp4ap_stream_t stream);
 
 /* README "Available Functions": ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16.
- * scale_fp8, shift_fp8: device (dim,) e4m3fn bytes (8-byte aligned);
+ * scale_fp8, shift_fp8: device (dim,) e4m3fn bytes;
  * scale_deq, shift_deq: device pointers to ONE fp32 each; the modulation is
  * decode(code) * deq as for ada_layer_norm_quant_fp8_modfp8_bf16, the output
  * as ada_layer_norm_quant_nvfp4_swizzled_bf16. */

@@ -141,6 +141,22 @@ int finish(cudaError_t e) {
   return NVFP4AP_ERR_LAUNCH;
 }
 
+// The element-wise kernel (ln_scalar.cu) for pointers that are only
+// element-aligned: bf16 tensors at 2 bytes, fp32 tables and scalars at 4,
+// e4m3 and output bytes at 1 (the tensor contract asks for contiguity only).
+// NVFP4AP_ERR_ALIGN when even that does not hold.
+int run_scalar(const LnArgs& a, bool nvfp4, int mod, cudaStream_t st) {
+  const void* bf[] = {a.x, a.scale, a.shift, a.temb, a.inv_s, a.seg_scale, a.seg_shift};
+  for (const void* p : bf)
+    if (p && !aligned(p, 2)) return NVFP4AP_ERR_ALIGN;
+  const void* f32[] = {a.table, a.act_scale, a.scale_deq, a.shift_deq, a.seg_idx};
+  for (const void* p : f32)
+    if (p && !aligned(p, 4)) return NVFP4AP_ERR_ALIGN;
+  const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
+  if (!grid_ok(work, 1)) return NVFP4AP_ERR_SHAPE;
+  return finish(launch_ln_scalar(a, nvfp4, mod, st));
+}
+
 int check_common(int64_t rows, int64_t dim, float eps) {
   if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
   if (dim > NVFP4AP_MAX_DIM) return NVFP4AP_ERR_DIM;
@@ -190,7 +206,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     vec8 = vec8 && aligned(p, 16);
     pair_ok = pair_ok && aligned(p, 4);
   }
-  if (!vec8 && !pair_ok) return NVFP4AP_ERR_ALIGN;
+  if (!vec8 && !pair_ok) return run_scalar(a, false, mod, st);
   const int vec = vec8 ? 8 : 2;
 
   // NVFP4AP_KERNEL: 0 auto (below), 1 warp-per-row TMA ring, 2 first register
@@ -291,7 +307,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
 int check_seg(const LnArgs& a) {
   if (!a.seg_idx || !a.seg_scale || !a.seg_shift) return NVFP4AP_ERR_NULL;
   if (a.nseg < 1) return NVFP4AP_ERR_INDEX;
-  if (!aligned(a.seg_idx, 4) || !aligned(a.seg_scale, 16) || !aligned(a.seg_shift, 16)) return NVFP4AP_ERR_ALIGN;
+  if (!aligned(a.seg_idx, 4)) return NVFP4AP_ERR_ALIGN;
   return NVFP4AP_OK;
 }
 
@@ -300,11 +316,16 @@ int check_seg(const LnArgs& a) {
 int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
-  if (a.dim % (nvfp4 ? 16 : 8) != 0) return NVFP4AP_ERR_DIM;
+  if (a.dim % (nvfp4 ? 16 : 2) != 0) return NVFP4AP_ERR_DIM;
   if (a.rows == 0) return NVFP4AP_OK;
   if (!a.x || !a.out || (nvfp4 ? !a.sf : !a.act_scale)) return NVFP4AP_ERR_NULL;
   if ((rc = check_seg(a)) != NVFP4AP_OK) return rc;
-  if (!aligned(a.x, 16) || !aligned(a.out, 8) || (!nvfp4 && !aligned(a.act_scale, 4))) return NVFP4AP_ERR_ALIGN;
+  if (!nvfp4 && !aligned(a.act_scale, 4)) return NVFP4AP_ERR_ALIGN;
+  // vector kernels: dim % 8, 16-byte aligned x and tables, 8-byte aligned
+  // output; anything else takes the element-wise kernel
+  if (a.dim % 8 != 0 || !aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.seg_scale, 16) ||
+      !aligned(a.seg_shift, 16))
+    return run_scalar(a, nvfp4, MOD_SEG, st);
   if (env_int("NVFP4AP_KERNEL") == 5 && ln_blk_supported(nvfp4 ? BLK_NVFP4 : BLK_FP8, MOD_SEG, a.dim, a.nseg) &&
       aligned(a.x, 32) && aligned(a.out, 16)) {
     BlkShape bs{};
@@ -344,6 +365,7 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   if (!a.x || !a.out || !a.sf || !a.tensor_scale || !a.amax_ws) return NVFP4AP_ERR_NULL;
   if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
   if (mod == MOD_SEG && (rc = check_seg(a)) != NVFP4AP_OK) return rc;
+  if (mod == MOD_SEG && (!aligned(a.seg_scale, 16) || !aligned(a.seg_shift, 16))) return NVFP4AP_ERR_ALIGN;
   if (!aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.tensor_scale, 4) || !aligned(a.amax_ws, 16))
     return NVFP4AP_ERR_ALIGN;
   // the workspace's statistics slots follow the word (16 bytes in)
@@ -382,9 +404,12 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   if (!a.x || !a.out || !a.sf) return NVFP4AP_ERR_NULL;
   if (mod == MOD_BCAST && (!a.scale || !a.shift)) return NVFP4AP_ERR_NULL;
   if (mod == MOD_MODFP8 && (rc = check_modfp8(a)) != NVFP4AP_OK) return rc;
-  if (!aligned(a.x, 16) || !aligned(a.out, 8)) return NVFP4AP_ERR_ALIGN;
-  if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
-  if (mod == MOD_MODFP8 && (!aligned(a.scale8, 8) || !aligned(a.shift8, 8))) return NVFP4AP_ERR_ALIGN;
+  // vector kernels: 16-byte aligned x and bf16 vectors, 8-byte aligned packed
+  // output and e4m3 vectors; anything else takes the element-wise kernel
+  if (!aligned(a.x, 16) || !aligned(a.out, 8) ||
+      (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) ||
+      (mod == MOD_MODFP8 && (!aligned(a.scale8, 8) || !aligned(a.shift8, 8))))
+    return run_scalar(a, true, mod, st);
 
   int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8, 8: one-row-per-CTA block-per-lane kernels
   // default: the one-row-per-CTA block-per-lane kernel where the row fits it
@@ -547,15 +572,15 @@ NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
   // wait words (ring and TMA kernels), then the segment-index words
-  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u, k = 0u;
+  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u, k = 0u, l = 0u;
   if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess ||
       take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess ||
-      take_warpreg_seg_fault(&k) != cudaSuccess) {
+      take_warpreg_seg_fault(&k) != cudaSuccess || take_scalar_seg_fault(&l) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
   if (f | g) return NVFP4AP_ERR_TIMEOUT;
-  return (h | i | j | k) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  return (h | i | j | k | l) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int nvfp4ap_set_wait_limit(int64_t cycles) {

@@ -166,6 +166,12 @@ struct RbShape {
 bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s);
 cudaError_t launch_ln_rowblk(const LnArgs& a, bool nvfp4, int mod, RbShape s, cudaStream_t st);
 
+// Element-wise LayerNorm producers (ln_scalar.cu) for pointers that are only
+// element-aligned: one CTA of 256 threads per row, FP8 (any modulation
+// source) or NVFP4 (MOD_NONE, MOD_BCAST, MOD_MODFP8, MOD_SEG).
+cudaError_t launch_ln_scalar(const LnArgs& a, bool nvfp4, int mod, cudaStream_t st);
+cudaError_t take_scalar_seg_fault(unsigned int* fault);
+
 // NVFP4 producers (K5-K6).
 cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 int ln_nvfp4_max_tpr(int per_thread);

@@ -5,11 +5,18 @@ parity test):
   - FP8 / NVFP4 codes: at least CODE_MATCH_MIN of the elements equal, and every
     mismatch exactly one step in the ordered code index (magnitude +-1 with the
     same sign, or +0 <-> -0 / +-0 <-> the smallest magnitude).
+  - per row: at most ROW_MISMATCH_FRAC of the row's codes (and never fewer
+    than ROW_MISMATCH_MIN) differ, so one row whose every code is one step off
+    fails even where it is a small part of a large tensor.
   - dequantised output: ||deq_gpu - deq_orc||_2 / ||deq_orc||_2 over the whole
     output tensor below DEQ_REL_MAX ("max relative error" is read as the largest
-    of these over every compared output; a row-wise ratio cannot be the bound,
-    since on short rows one permitted one-step mismatch alone exceeds 1e-2).
-    The largest row-wise ratio is reported alongside, not asserted.
+    of these over every compared output; a row-wise ratio cannot be the bound
+    everywhere, since on short rows one permitted one-step mismatch alone
+    exceeds 1e-2).  Row-wise the same bound is asserted where it is
+    meaningful: FP8 rows of at least ROW_REL_MIN_DIM elements with at most one
+    mismatch (one e4m3 step of a value within four standard deviations of the
+    row is below 1e-2 of such a row's norm).  The largest row-wise ratio is
+    reported for every output.
   - NVFP4 block-scale bytes: equal, except for blocks whose oracle amax lies
     within one bf16 ulp of an e4m3 rounding boundary of amax/6 (there the fp32
     and fp64 routes to the staged bf16 value may differ by one ulp); the
@@ -28,6 +35,9 @@ import oracle
 CODE_MATCH_MIN = 0.999
 MAX_STEP = 1
 DEQ_REL_MAX = 1e-2
+ROW_MISMATCH_FRAC = 0.01
+ROW_MISMATCH_MIN = 2
+ROW_REL_MIN_DIM = 2048
 
 _E4M3 = None
 _E2M1 = None
@@ -80,7 +90,18 @@ def check_codes(gpu: np.ndarray, orc: np.ndarray, sign_bit: int, what: str) -> d
     bad = (~eq) & (step > MAX_STEP)
     assert not bad.any(), f"{what}: {int(bad.sum())} codes more than {MAX_STEP} step off, first at {np.argwhere(bad)[:5].tolist()}"
     assert frac >= CODE_MATCH_MIN, f"{what}: only {frac:.6f} of codes equal"
+    if gpu.ndim == 2 and gpu.size:
+        per_row = (~eq).sum(axis=1)
+        cap = max(ROW_MISMATCH_MIN, int(np.ceil(ROW_MISMATCH_FRAC * gpu.shape[1])))
+        worst = int(per_row.max())
+        assert worst <= cap, f"{what}: row {int(per_row.argmax())} has {worst} mismatched codes (cap {cap})"
     return {"equal_frac": frac, "mismatches": int((~eq).sum())}
+
+
+def _row_rel_all(deq_g: np.ndarray, deq_o: np.ndarray) -> np.ndarray:
+    num = np.sqrt(((deq_g - deq_o) ** 2).sum(axis=1))
+    den = np.sqrt((deq_o ** 2).sum(axis=1))
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), 0.0)
 
 
 def check_fp8(gpu_codes: np.ndarray, orc_codes: np.ndarray, act_scale: float, what: str = "fp8") -> dict:
@@ -91,6 +112,10 @@ def check_fp8(gpu_codes: np.ndarray, orc_codes: np.ndarray, act_scale: float, wh
     assert rel < DEQ_REL_MAX, f"{what}: relative error {rel}"
     st["rel_err"] = rel
     st["row_rel_err_max"] = _row_rel(dg, do)
+    if gpu_codes.ndim == 2 and gpu_codes.shape[1] >= ROW_REL_MIN_DIM:
+        rows_ok = (gpu_codes != orc_codes).sum(axis=1) <= 1
+        rr = _row_rel_all(dg, do)[rows_ok]
+        assert rr.size == 0 or rr.max() < DEQ_REL_MAX, f"{what}: row-wise relative error {rr.max()}"
     return st
 
 

@@ -105,9 +105,9 @@ def test_fp8_argument_errors(lib):
     assert f(NULL, A, A, A, 1e-5, A, 4, 64, NULL) == 1        # null x
     assert f(A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1        # null scale
     assert f(A, A, A, NULL, 1e-5, A, 4, 64, NULL) == 1        # null act_scale
-    assert f(A + 1, A, A, A, 1e-5, A, 4, 64, NULL) == 5       # x not even 4-byte aligned
+    assert f(A + 1, A, A, A, 1e-5, A, 4, 64, NULL) == 5       # bf16 x at an odd address (not element-aligned)
     assert f(A, A, A, A + 2, 1e-5, A, 4, 64, NULL) == 5       # act_scale misaligned
-    assert f(A, A, A, A, 1e-5, A + 1, 4, 64, NULL) == 5       # odd output address
+    assert f(A, A + 1, A, A, 1e-5, A, 4, 64, NULL) == 5       # bf16 scale at an odd address
     assert f(NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0  # rows == 0: no-op
     g = L.ada_layer_norm_quant_fp8_ptok_bf16
     assert g(A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1
@@ -123,7 +123,7 @@ def test_table_index_errors(lib):
     assert t(A, A, A, 6, 0, -1, A, 1e-5, A, 4, 64, NULL) == 4  # negative scale_idx
     assert t(A, A, A, 0, 0, 0, A, 1e-5, A, 4, 64, NULL) == 4   # no chunks
     assert t(A, NULL, A, 6, 0, 1, A, 1e-5, A, 4, 64, NULL) == 1
-    assert t(A, A, A + 4, 6, 0, 1, A, 1e-5, A, 4, 64, NULL) == 5  # table not 8-byte aligned
+    assert t(A, A, A + 2, 6, 0, 1, A, 1e-5, A, 4, 64, NULL) == 5  # fp32 table not 4-byte aligned
 
 
 def test_nvfp4_argument_errors(lib):
@@ -133,9 +133,8 @@ def test_nvfp4_argument_errors(lib):
     assert f(A, A, A, 1e-5, A, A, 4, 32784, NULL) == 3         # above the maximum dim
     assert f(A, A, A, 1e-5, NULL, A, 4, 64, NULL) == 1         # null packed
     assert f(A, A, A, 1e-5, A, NULL, 4, 64, NULL) == 1         # null scales
-    assert f(A + 4, A, A, 1e-5, A, A, 4, 64, NULL) == 5        # x not 16-byte aligned
-    assert f(A, A, A + 8, 1e-5, A, A, 4, 64, NULL) == 5        # shift not 16-byte aligned
-    assert f(A, A, A, 1e-5, A + 4, A, 4, 64, NULL) == 5        # packed not 8-byte aligned
+    assert f(A + 1, A, A, 1e-5, A, A, 4, 64, NULL) == 5        # x at an odd address
+    assert f(A, A, A + 1, 1e-5, A, A, 4, 64, NULL) == 5        # shift at an odd address
     assert f(A, A, A, 1e-5, A, A, 0, 64, NULL) == 0
     g = L.layer_norm_no_affine_quant_nvfp4_swizzled_bf16
     assert g(A, 1e-5, A, A, -3, 64, NULL) == 2
@@ -148,20 +147,20 @@ def test_modfp8_and_awq_argument_errors(lib):
     assert m(A, NULL, A, A, A, A, 1e-5, A, 4, 64, NULL) == 1      # null scale_fp8
     assert m(A, A, A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1      # null shift_deq
     assert m(A, A, A, A + 2, A, A, 1e-5, A, 4, 64, NULL) == 5     # scale_deq misaligned
-    assert m(A, A + 1, A, A, A, A, 1e-5, A, 4, 64, NULL) == 5     # e4m3 vector at an odd address
+    assert m(A + 1, A, A, A, A, A, 1e-5, A, 4, 64, NULL) == 5     # x at an odd address
     assert m(A, A, A, A, A, A, 1e-5, A, 4, 63, NULL) == 3         # odd dim
     assert m(A, A, A, A, A, A, -2.0, A, 4, 64, NULL) == 8
     assert m(NULL, NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0
     w = L.awq_ada_layer_norm_quant_fp8_bf16  # x, scale, shift, inv_s, act, eps, out, rows, dim
     assert w(A, A, A, NULL, A, 1e-5, A, 4, 64, NULL) == 1         # null inv_s
     assert w(A, A, NULL, A, A, 1e-5, A, 4, 64, NULL) == 1         # null shift
-    assert w(A, A, A, A + 2, A, 1e-5, A, 4, 64, NULL) == 5        # inv_s not 4-byte aligned
+    assert w(A, A, A, A + 1, A, 1e-5, A, 4, 64, NULL) == 5        # inv_s at an odd address
     assert w(A, A, A, A, A, float("nan"), A, 4, 64, NULL) == 8
     assert w(A, A, A, A, A, 1e-5, A, 4, 32770, NULL) == 3
     n = L.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16  # x, s8, h8, sdeq, hdeq, eps, packed, sf, rows, dim
     assert n(A, A, A, A, A, 1e-5, A, A, 4, 40, NULL) == 3         # dim % 16
     assert n(A, A, A, A, NULL, 1e-5, A, A, 4, 64, NULL) == 1      # null shift_deq
-    assert n(A, A + 4, A, A, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_fp8 not 8-byte aligned
+    assert n(A + 1, A, A, A, A, 1e-5, A, A, 4, 64, NULL) == 5     # x at an odd address
     assert n(A, A, A, A + 1, A, 1e-5, A, A, 4, 64, NULL) == 5     # scale_deq misaligned
     assert n(NULL, NULL, NULL, NULL, NULL, 1e-5, NULL, NULL, 0, 64, NULL) == 0
 
@@ -171,9 +170,9 @@ def test_seg_and_two_level_argument_errors(lib):
     f = L.ada_layer_norm_quant_fp8_seg_bf16  # x, seg_idx, seg_scale, seg_shift, nseg, act, eps, out, rows, dim
     assert f(A, A, A, A, 0, A, 1e-5, A, 4, 64, NULL) == 4          # no segments
     assert f(A, NULL, A, A, 3, A, 1e-5, A, 4, 64, NULL) == 1       # null index
-    assert f(A, A, A, A + 8, 3, A, 1e-5, A, 4, 64, NULL) == 5      # shift table not 16-byte aligned
+    assert f(A, A, A, A + 1, 3, A, 1e-5, A, 4, 64, NULL) == 5      # shift table at an odd address
     assert f(A, A + 2, A, A, 3, A, 1e-5, A, 4, 64, NULL) == 5      # index not 4-byte aligned
-    assert f(A, A, A, A, 3, A, 1e-5, A, 4, 60, NULL) == 3          # dim % 8
+    assert f(A, A, A, A, 3, A, 1e-5, A, 4, 63, NULL) == 3          # odd dim
     assert f(NULL, NULL, NULL, NULL, 0, NULL, 1e-5, NULL, 0, 64, NULL) == 0
     g = L.ada_layer_norm_quant_nvfp4_swizzled_seg_bf16  # x, idx, s, h, nseg, eps, packed, sf, rows, dim
     assert g(A, A, A, A, 3, 1e-5, A, A, 4, 40, NULL) == 3          # dim % 16

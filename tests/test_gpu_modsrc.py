@@ -178,13 +178,16 @@ def test_awq_pair_path_when_off_16_byte_alignment(ap, dev):
     check_fp8(_codes(out), ref, act, "awq pair path")
 
 
-def test_modfp8_nvfp4_rejects_misaligned_vectors(ap, dev):
+def test_modfp8_nvfp4_misaligned_vectors_take_the_element_wise_kernel(ap, dev):
     w = synth.nvfp4_modfp8(16, 64, seed=79)
     d = _d(w, dev)
     s8 = _offset_view(d["scale_fp8"], 4)
-    with pytest.raises(RuntimeError, match="status 5"):
-        ap.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(d["x"], s8, d["shift_fp8"], d["scale_deq"],
-                                                           d["shift_deq"])
+    pk, sf = ap.ada_layer_norm_quant_nvfp4_swizzled_modfp8_bf16(d["x"], s8, d["shift_fp8"], d["scale_deq"],
+                                                                d["shift_deq"])
+    src = _modfp8_src(w)
+    xu = synth.u16(w.inputs["x"])
+    op, os_ = oracle.ln_quant_nvfp4(xu, oracle.MOD_MODFP8, **src)
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), op, os_, 16, 64, what="modfp8 vectors off 8-byte alignment")
 
 
 def test_modfp8_extreme_codes_and_saturation(ap, dev):

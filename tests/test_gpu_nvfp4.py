@@ -120,13 +120,15 @@ def test_batch_invariance(ap, dev, path):
         assert np.array_equal(unswizzle(s2.cpu().numpy(), n, 3072), full_s[start:start + n])
 
 
-def test_misaligned_input_rejected(ap, dev):
-    x = torch.zeros(16 * 64 + 8, dtype=torch.bfloat16, device=dev)[8:].view(16, 64)  # 16-byte aligned: ok
-    ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(x)
-    y = torch.zeros(16 * 64 + 4, dtype=torch.bfloat16, device=dev)[4:].view(16, 64)  # 8-byte aligned only
-    with pytest.raises(ap.NvFp4ApError) as e:
-        ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(y)
-    assert e.value.status == ap.ERR_ALIGN
+def test_misaligned_input_takes_the_element_wise_kernel(ap, dev):
+    w = synth.nvfp4_ln(16, 64, seed=8)
+    x = w.inputs["x"]
+    ref_p, ref_s = oracle.ln_quant_nvfp4(synth.u16(x))
+    for off in (8, 4, 1):  # 16-byte aligned (vector kernels), 8-byte, 2-byte (element-wise kernel)
+        y = torch.zeros(16 * 64 + off, dtype=torch.bfloat16, device=dev)[off:].view(16, 64)
+        y.copy_(x.to(dev))
+        pk, sf = ap.layer_norm_no_affine_quant_nvfp4_swizzled_bf16(y)
+        check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), ref_p, ref_s, 16, 64, what=f"x offset {off}")
 
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
