@@ -17,8 +17,8 @@
 //   Two-level NVFP4, two launches:
 //     BK_AMAX: the largest |v| of the whole tensor into one device word;
 //     BK_NV2L: ts = bf16(amax / 2688) from that word; per 16 elements
-//              s = e4m3fn(min((amax_b / 6) / ts, 448)) with both divisions
-//              IEEE fp32; e2m1 codes of v / (s * ts).
+//              s = e4m3fn(min((amax_b / 6) / ts, 448)) with both
+//              quotients correctly rounded in fp32; e2m1 codes of v / (s * ts).
 //
 // Design.  A lane owns whole 16-element blocks of a row: blocks t, t + tpr,
 // ... (tpr = threads per row, a warp or a few), each read with one 256-bit
@@ -219,9 +219,10 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
   blk_tables<KIND, MOD>(a, gh, nblk, inv_act);
 
   // two-level: the tensor scale from the maximum pass's word (read through L2)
-  float ts = 1.0f;
+  float ts = 1.0f, rts = 1.0f;
   if constexpr (KIND == BK_NV2L) {
     ts = blk_round_bf16(__fdiv_rn(__uint_as_float(__ldcg(a.amax_ws)), 2688.0f));
+    rts = __frcp_rn(ts);
     if (blockIdx.x == 0 && threadIdx.x == 0) a.tensor_scale[0] = ts;
   }
   float run = 0.0f;  // maximum pass: this thread's largest |v|
@@ -325,11 +326,12 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
           uint32_t sbyte, c0, c1;
           float scl, pre = 1.0f;
           if constexpr (KIND == BK_NV2L) {
-            // (amax_b / 6) / ts with IEEE divisions, clamped at 448 (fminf takes
+            // (amax_b / 6) / ts, both quotients correctly rounded (two_level_quot),
+            // clamped at 448 (fminf takes
             // 448 for the 0/0 of an all-zero tensor); the divisor of the codes
             // is s * ts, exact in fp32 (4 + 8 significant bits); a divisor
             // below 2^-64 and the block's values are both scaled by 2^64
-            sbyte = f2_to_e4m3x2(make_float2(fminf(__fdiv_rn(__fdiv_rn(amax, 6.0f), ts), 448.0f), 0.f)) & 0xFFu;
+            sbyte = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax, ts, rts), 448.0f), 0.f)) & 0xFFu;
             scl = e4m3_to_f32(sbyte) * ts;
             if (scl != 0.f && scl < 0x1p-64f) {
               scl *= 0x1p64f;

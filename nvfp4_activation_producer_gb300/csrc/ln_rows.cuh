@@ -17,8 +17,8 @@
 //     KIND_AMAX: v as above; the largest |v| of the whole tensor into one
 //                device word (atomic max of the non-negative fp32 bits);
 //     KIND_NV2L: ts = bf16(amax / 2688) from that word; per 16 elements
-//                s = e4m3fn(min((amax_b / 6) / ts, 448)) with both divisions
-//                IEEE fp32; e2m1 codes of v / (s * ts).
+//                s = e4m3fn(min((amax_b / 6) / ts, 448)) with both
+//                quotients correctly rounded in fp32; e2m1 codes of v / (s * ts).
 //
 // Design.  A row is owned by `tpr` threads (a warp or a few warps); thread t
 // owns the 8-element chunks t, t+tpr, ... of the row (a warp reads 512
@@ -326,9 +326,10 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
     for (int k = 0; k < NV; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xFFFFFFFFu, amax[k], 1));
     // two-level: the tensor scale from the first pass's maximum (read through
     // L2: it was written by atomics of the previous launch)
-    float ts = 1.0f;
+    float ts = 1.0f, rts = 1.0f;
     if constexpr (KIND == KIND_NV2L) {
       ts = round_bf16(__fdiv_rn(__uint_as_float(__ldcg(a.amax_ws)), 2688.0f));
+      rts = __frcp_rn(ts);
       if (blockIdx.x == 0 && t == 0 && ry == 0) a.tensor_scale[0] = ts;
     }
     uint32_t sbyte[NV], codes[NV];
@@ -336,10 +337,11 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
     for (int k = 0; k < NV; ++k) {
       float scl;
       if constexpr (KIND == KIND_NV2L) {
-        // (amax_b / 6) / ts with IEEE divisions, clamped at 448 (fminf takes
+        // (amax_b / 6) / ts, both quotients correctly rounded (two_level_quot),
+        // clamped at 448 (fminf takes
         // 448 for the 0/0 of an all-zero tensor); the divisor of the codes is
         // s * ts, exact in fp32 (4 + 8 significant bits)
-        sbyte[k] = f2_to_e4m3x2(make_float2(fminf(__fdiv_rn(__fdiv_rn(amax[k], 6.0f), ts), 448.0f), 0.f)) & 0xFFu;
+        sbyte[k] = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax[k], ts, rts), 448.0f), 0.f)) & 0xFFu;
         scl = e4m3_to_f32(sbyte[k]) * ts;
       } else {
         // e4m3(amax/6) via the fp32 constant 1/6 gives the byte of the exact

@@ -94,9 +94,10 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_kernel(const SwArgs a) {
   const int nblk = (int)(a.dim >> 4), padc = (nblk + 3) & ~3, ct = padc >> 2;
   const uint32_t stride = gridDim.x * blockDim.x;
 
-  float ts = 1.0f, run = 0.0f;
+  float ts = 1.0f, rts = 1.0f, run = 0.0f;
   if constexpr (QUANT) {
     ts = round_bf16(__fdiv_rn(__uint_as_float(__ldcg(a.amax_ws)), 2688.0f));
+    rts = __frcp_rn(ts);
     if (blockIdx.x == 0 && threadIdx.x == 0) a.tensor_scale[0] = ts;
   }
   for (uint32_t n = blockIdx.x * blockDim.x + threadIdx.x; n < a.items; n += stride) {
@@ -113,11 +114,11 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_kernel(const SwArgs a) {
     if constexpr (!QUANT) {
       run = fmaxf(run, amax);
     } else {
-      // (amax_b / 6) / ts with IEEE divisions, clamped at 448 (fminf takes 448
-      // for the 0/0 of an all-zero tensor); the divisor of the codes is s * ts,
-      // exact in fp32; a divisor below 2^-64 and the values are scaled by 2^64
-      const uint32_t sbyte =
-          f2_to_e4m3x2(make_float2(fminf(__fdiv_rn(__fdiv_rn(amax, 6.0f), ts), 448.0f), 0.f)) & 0xFFu;
+      // (amax_b / 6) / ts, each quotient correctly rounded (two_level_quot),
+      // clamped at 448 (fminf takes 448 for the 0/0 of an all-zero tensor); the
+      // divisor of the codes is s * ts, exact in fp32; a divisor below 2^-64
+      // and the values are scaled by 2^64
+      const uint32_t sbyte = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax, ts, rts), 448.0f), 0.f)) & 0xFFu;
       float scl = e4m3_to_f32(sbyte) * ts, pre = 1.0f;
       if (scl != 0.f && scl < 0x1p-64f) {
         scl *= 0x1p64f;

@@ -149,3 +149,87 @@ def test_two_level_quotient_is_exact_for_every_divisor_mantissa():
         assert np.array_equal(v32.astype(np.float64), v)
         q = _fma32(v32, r_h, (v32 * r_l).astype(np.float32))
         assert np.array_equal(_code_rne32(q), exact_code(v, d)), ulps
+
+
+# ---------------------------------------------------------------------------
+# two-level block scale: (amax / 6) / ts without IEEE divisions
+# ---------------------------------------------------------------------------
+
+def _rn32(x: Fraction) -> np.float32:
+    """Round an exact rational to the nearest float32, ties to even (normal and
+    subnormal range; no overflow in the cases below)."""
+    f = np.float32(float(x))  # within one float32 ulp of x
+    best = None
+    for c in (np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))):
+        d = abs(Fraction(float(c)) - x)
+        if best is None or d < best[0] or (d == best[0] and (int(np.float32(c).view(np.uint32)) & 1) == 0):
+            best = (d, c)
+    return np.float32(best[1])
+
+
+def _fma_exact(a, b, c) -> np.float32:
+    return _rn32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+
+
+INV6 = _rn32(Fraction(1, 6))
+
+
+def _two_level_q_fast(amax: np.float32, ts: np.float32) -> np.float32:
+    # the kernel's form: RN(amax / 6) and RN(q1 / ts) each from a product by the
+    # correctly rounded reciprocal and one fused residual correction
+    q = np.float32(amax * INV6)
+    e = _fma_exact(np.float32(-6.0), q, amax)
+    q1 = _fma_exact(e, INV6, q)
+    rt = _rn32(Fraction(1) / Fraction(float(ts)))
+    q = np.float32(q1 * rt)
+    e = _fma_exact(-ts, q, q1)
+    return _fma_exact(e, rt, q)
+
+
+def _two_level_q_exact(amax: np.float32, ts: np.float32) -> np.float32:
+    q1 = _rn32(Fraction(float(amax)) / 6)
+    return _rn32(Fraction(float(q1)) / Fraction(float(ts)))
+
+
+def test_two_level_scale_quotient_exact_for_every_significand_pair():
+    # both operands are bf16 values: 8-bit significands; scaling by powers of
+    # two commutes with the roundings in the normal range, so every pair of
+    # significands at one exponent covers the kernel's fast path
+    sig = [np.float32(m / 128.0) for m in range(128, 256)]
+    for a in sig:
+        for t in sig:
+            assert _two_level_q_fast(a, t) == _two_level_q_exact(a, t), (a, t)
+
+
+def test_two_level_scale_byte_on_random_bf16_pairs_across_the_range():
+    # the e4m3 byte of fminf(q, 448) over bf16 pairs of every magnitude the fast
+    # path takes (amax, ts >= 2^-100), overflow to the clamp included
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0x0D80, 0x7F80, size=(6000, 2), dtype=np.uint32)  # from 2^-100 to the largest bf16
+    for ab, tb in bits:
+        a, t = (np.uint32(ab) << 16).view(np.float32), (np.uint32(tb) << 16).view(np.float32)
+        with np.errstate(over="ignore", invalid="ignore"):
+            qf = _two_level_q_fast_safe(a, t)
+        qe = _two_level_q_exact_big(a, t)
+        assert _e4m3(np.fmin(np.float32(qf), np.float32(448.0))) == _e4m3(np.minimum(qe, 448.0)), (a, t)
+
+
+def _two_level_q_fast_safe(amax, ts):
+    # as _two_level_q_fast, with float32 overflow to inf as the hardware gives it
+    # (the exact helpers above assume finite values)
+    q = np.float32(amax * INV6)
+    e = _fma_exact(np.float32(-6.0), q, amax)
+    q1 = _fma_exact(e, INV6, q)
+    rt = _rn32(Fraction(1) / Fraction(float(ts)))
+    q = np.float32(q1 * rt)
+    if not np.isfinite(q):
+        return np.float32(np.nan)  # -ts * inf + q1 = -inf; -inf * rt + inf = NaN
+    e = _fma_exact(-ts, q, q1)
+    r = Fraction(float(e)) * Fraction(float(rt)) + Fraction(float(q))
+    return np.float32(np.inf) if abs(r) > Fraction(float(np.finfo(np.float32).max)) else _rn32(r)
+
+
+def _two_level_q_exact_big(amax, ts) -> float:
+    q1 = _rn32(Fraction(float(amax)) / 6)
+    r = Fraction(float(q1)) / Fraction(float(ts))
+    return float("inf") if r > Fraction(float(np.finfo(np.float32).max)) else float(_rn32(r))
