@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import platform
 import statistics
 import subprocess
@@ -68,10 +69,59 @@ def step_workloads():
     ]
 
 
+# The FP8 producers at the shapes of the pages' RTX 5090 table (benchmarks/
+# RESULTS.md, "AdaLN->FP8 / LN->FP8"; 4096x3072 is in the step) and at 32768
+# rows: (rows, dim, the page's AdaLN->FP8 us, the page's LN->FP8 us) -- the
+# page's figures are another GPU's, context only.
+PAGE_FP8_SHAPES = ((16, 2048, 4.117, 3.962), (64, 3072, 4.133, 4.117), (256, 3072, 4.140, 4.108),
+                   (2520, 3072, 12.330, 10.267), (4096, 3072, 18.465, 16.412))
+SWEEP_EXTRA = ((32768, 3072),)
+# below this many rows a producer is bound by launch latency and ramp, not by
+# HBM: its per_op line carries no bandwidth fraction
+LAUNCH_BOUND_ROWS = 2500
+
+
+def op_kind(name: str) -> str:
+    """The producer of a per_op line: names with a trailing _<rows>x<dim> are
+    the same producer at another shape."""
+    m = re.match(r"^(.*)_(\d+)x(\d+)$", name)
+    return m.group(1) if m else name
+
+
+def page_context(name: str, rows: int, dim: int):
+    """The pages' own figure for this producer and shape, if they print one
+    (another GPU's: context only)."""
+    kind = op_kind(name)
+    for R, D, ada, ln in PAGE_FP8_SHAPES:
+        if (R, D) == (rows, dim) and kind in ("fp8_broadcast", "fp8_layer_norm"):
+            us = ada if kind == "fp8_broadcast" else ln
+            return {"us": us, "hw": "RTX 5090, --iters 100 on identical buffers (benchmarks/RESULTS.md)"}
+    if kind == "modulation6" and (rows, dim) == (5070, 3072):
+        return {"us": 347.251, "hw": "RTX 5090 (benchmarks/RESULTS.md, adaln_modulation6 B1 S5070 D3072)"}
+    return None
+
+
+def page_shape_workloads():
+    """The FP8 broadcast and layer-norm producers at the pages' shapes (but the
+    step's 4096x3072) and at SWEEP_EXTRA."""
+    shapes = []
+    for R, D, _, _ in PAGE_FP8_SHAPES:
+        if (R, D) == (4096, 3072):
+            continue
+        seed = 1001 if (R, D) == (16, 2048) else 1006
+        shapes.append((f"fp8_broadcast_{R}x{D}", synth.fp8_broadcast(R, D, seed)))
+        shapes.append((f"fp8_layer_norm_{R}x{D}", synth.fp8_ln(R, D, seed)))
+    for R, D in SWEEP_EXTRA:
+        shapes.append((f"fp8_broadcast_{R}x{D}", synth.fp8_broadcast(R, D, 1006)))
+        shapes.append((f"fp8_layer_norm_{R}x{D}", synth.fp8_ln(R, D, 1006)))
+    return shapes
+
+
 def extra_workloads():
     """Producers measured beside the step (same shapes as their broadcast
-    counterparts), reported in `per_op` with "in_step": false."""
-    return [
+    counterparts, the pages' FP8 shapes, a large row count), reported in
+    `per_op` with "in_step": false."""
+    return page_shape_workloads() + [
         ("fp8_modfp8", synth.fp8_modfp8(4096, 3072, 2006)),
         ("fp8_awq", synth.fp8_awq(4096, 3072, 2007)),
         ("nvfp4_modfp8", synth.nvfp4_modfp8(5070, 3072, 2008)),
@@ -87,6 +137,7 @@ def alg_bytes(name: str, w) -> int:
     """Bytes the producer must move: every input element it uses read once,
     every output byte written once (per-op formulas of the design notes)."""
     R, D = w.rows, w.dim
+    name = op_kind(name)
     if name == "fp8_broadcast":
         return 2 * R * D + 4 * D + R * D + 4
     if name == "fp8_modfp8":
@@ -129,7 +180,7 @@ def launches_per_call(name: str) -> int:
     """Kernels one call of the producer launches: the two-level producers (the
     LayerNorm forms and SwiGLU) clear their word, then run the maximum and the
     quantising pass."""
-    return 3 if name.startswith("nvfp4_2level") else 1
+    return 3 if op_kind(name).startswith("nvfp4_2level") else 1
 
 
 class DeviceOp:
@@ -158,7 +209,7 @@ class DeviceOp:
     def api_call(self):
         """The producer through the Python API (tensor checks, then the C ABI)."""
         ap, d, o, p = self.ap, self.d, self.out, self.w.params
-        n = self.name
+        n = op_kind(self.name)
         if n == "fp8_broadcast":
             ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"], p["eps"], out=o[0])
         elif n == "fp8_layer_norm":
@@ -208,7 +259,7 @@ class DeviceOp:
         L = self.ap._load()
         d, o, p, R, D = self.d, self.out, self.w.params, self.w.rows, self.w.dim
         P = lambda t: t.data_ptr()
-        n = self.name
+        n = op_kind(self.name)
         if n == "fp8_broadcast":
             fn, a = L.ada_layer_norm_quant_fp8_bf16, (P(d["x"]), P(d["scale"]), P(d["shift"]), P(d["act_scale"]),
                                                       p["eps"], P(o[0]), R, D, stream)
@@ -446,7 +497,10 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.get_device_properties(dev), "L2_cache_size") else 129 * 2 ** 20
     per_op_graphs = []
     for o in ops + extra_ops:
-        nsets = max(2, -(-3 * l2 // o.bytes))
+        # rotating buffer sets > 3x L2 (at most one per call of the graph: the
+        # launch-bound shapes then run from L2, which bounds them no more than
+        # their launches do)
+        nsets = min(args.per_op_launches, max(2, -(-3 * l2 // o.bytes)))
         copies = [o] + [DeviceOp(ap, o.name, o.w, dev) for _ in range(nsets - 1)]
         ccalls = [c.bind_raw(stream.cuda_stream) for c in copies]
         with torch.cuda.stream(stream):
@@ -470,7 +524,7 @@ def run_ours(args, rank, world, local_rank):
     copy_graphs = []
     for o in ops + extra_ops:
         words = max(4, (o.bytes // 8) // 4 * 4)
-        nsets = max(2, -(-3 * l2 // (8 * words)))
+        nsets = min(args.per_op_launches, max(2, -(-3 * l2 // (8 * words))))
         bufs = [(torch.zeros(words, dtype=torch.int32, device=dev), torch.empty(words, dtype=torch.int32, device=dev))
                 for _ in range(nsets)]
         g = torch.cuda.CUDAGraph()
@@ -519,8 +573,21 @@ def run_ours(args, rank, world, local_rank):
                 evs.append((e0, e1))
             copy_events.append(evs)
     barrier()
+    # the same step graph replayed enough times for ~400 steps, after the timed
+    # K steps: a longer look at the step time (context beside `value`)
+    rep_n = max(1, -(-400 // M))
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        r0.record(stream)
+        for _ in range(rep_n):
+            graph.replay()
+        r1.record(stream)
+    barrier()
     clocks.mark("t1")
     clocks.stop()
+    rep_ms = max_over_ranks(r0.elapsed_time(r1), world, dev)
+    step_repeat = {"steps": rep_n * M, "ms_per_step": round(rep_ms / (rep_n * M), 5),
+                   "value": round(job_gbs(step_bytes, world, rep_ms / (rep_n * M)), 1), "unit": "GB/s"}
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_per_step = elapsed_ms / steps
     value = job_gbs(step_bytes, world, ms_per_step)
@@ -540,12 +607,20 @@ def run_ours(args, rank, world, local_rank):
         us = statistics.median(calls)
         gbs = o.bytes / (us * 1e-6) / 1e9
         copy_us = statistics.median(e0.elapsed_time(e1) for e0, e1 in copy_events[i]) * 1e3 / n
-        per_op.append({"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
-                       "us_p10": round(float(np.percentile(calls, 10)), 3),
-                       "us_p90": round(float(np.percentile(calls, 90)), 3),
-                       "alg_bytes": o.bytes, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4),
-                       "copy_us": round(copy_us, 3), "frac_of_copy": round(copy_us / us, 4),
-                       "in_step": i < len(ops)})
+        launch_bound = o.w.rows < LAUNCH_BOUND_ROWS
+        rec = {"op": o.name, "rows": o.w.rows, "dim": o.w.dim, "us_per_call": round(us, 3),
+               "us_p10": round(float(np.percentile(calls, 10)), 3),
+               "us_p90": round(float(np.percentile(calls, 90)), 3),
+               "alg_bytes": o.bytes, "gbs": round(gbs, 1),
+               "frac_of_hbm_peak": None if launch_bound else round(gbs / hbm, 4),
+               "copy_us": round(copy_us, 3), "frac_of_copy": None if launch_bound else round(copy_us / us, 4),
+               "in_step": i < len(ops)}
+        if launch_bound:
+            rec["launch_bound"] = True
+        page = page_context(o.name, o.w.rows, o.w.dim)
+        if page:
+            rec["page"] = page
+        per_op.append(rec)
     dom = max(range(len(ops)), key=lambda i: per_op[i]["us_per_call"])  # largest share of the step
     d = per_op[dom]
     roofline = {"bound": "hbm", "kernel": d["op"], "achieved": d["gbs"], "peak": hbm, "peak_source": peak_src,
@@ -565,12 +640,18 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "no flush: each step streams ~0.9 GB of distinct buffers (> 129 MB L2) between repeats "
                          "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": roofline, "per_op": per_op, "e2e": e2e, "chain": chain,
-        "gpu_launches": launches, "clocks": clocks.summary(),
-        "timing": ("step: CUDA graph of %d steps replayed %d times; per_op: graph of %d back-to-back calls per "
-                   "producer over rotating buffers > 3x L2, median (us_per_call), p10 and p90 of the per-call time "
-                   "over %d replays; copy_us: the same for a streaming copy kernel (torch int32 add of 0) moving the "
-                   "producer's algorithmic bytes, median of 3 replays, frac_of_copy = copy_us / us_per_call"
-                   % (M, R, args.per_op_launches, args.op_replays)),
+        "step_repeat": step_repeat,
+        "gpu_launches": launches + rep_n * M * sum(launches_per_call(o.name) for o in ops),
+        "clocks": clocks.summary(),
+        "timing": ("step: exactly %d steps timed, %d replay(s) of a CUDA graph of %d steps (%.2f ms of GPU time); "
+                   "step_repeat: the same graph replayed %d times (%d steps) right after, a longer look at the same "
+                   "step; per_op: graph of %d back-to-back calls per producer over rotating buffers > 3x L2 (at most "
+                   "one set per call: shapes below %d rows are launch-bound, run from L2 and carry no bandwidth "
+                   "fraction), median (us_per_call), p10 and p90 of the per-call time over %d replays; copy_us: the "
+                   "same for a streaming copy kernel (torch int32 add of 0) moving the producer's algorithmic bytes, "
+                   "median of 3 replays, frac_of_copy = copy_us / us_per_call"
+                   % (steps, R, M, elapsed_ms, rep_n, rep_n * M, args.per_op_launches, LAUNCH_BOUND_ROWS,
+                      args.op_replays)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(works, budget_s=args.cpu_seconds)
@@ -836,9 +917,14 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_full, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "sampled": True,
+            "sample_wall_s": round(dt, 3), "ms_per_step_sampled": round(dt / len(times) * 1e3, 3),
             "config": {"workload": WORKLOAD, "step_alg_bytes": step_bytes,
-                       "sample": f"each step runs the CPU oracle on the first 1/{frac} of the rows of every "
-                                 f"producer; ms_per_step is scaled to the full step"},
+                       "sample": f"sampled: each step runs the CPU oracle on the first 1/{frac} of the rows of every "
+                                 f"producer ({sample_bytes} algorithmic bytes, {dt / len(times) * 1e3:.1f} ms per "
+                                 f"step, {dt:.2f} s for all steps); value is those bytes over that time, and "
+                                 f"ms_per_step ({ms_full:.1f} ms) the full step's bytes at that rate -- an "
+                                 f"extrapolation, not a timed full step"},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                              "sample": f"first 1/{frac} of the rows of every producer, {args.steps} steps"},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -49,3 +49,19 @@ def test_swizzled_buffer_size_matches_the_library_formula():
                                     ("modulation6", 1), ("fp8_seg_h3", 1)])
 def test_launches_per_call(name, n):
     assert bench.launches_per_call(name) == n
+
+
+def test_shape_suffixed_lines_count_as_their_producer():
+    # per_op lines of a producer at another shape (the pages' FP8 shapes)
+    assert bench.op_kind("fp8_broadcast_16x2048") == "fp8_broadcast"
+    assert bench.op_kind("fp8_layer_norm_32768x3072") == "fp8_layer_norm"
+    assert bench.op_kind("nvfp4_2level_seg_h3") == "nvfp4_2level_seg_h3"
+    assert bench.alg_bytes("fp8_broadcast_16x2048", _w(16, 2048)) == 16 * 2048 * 3 + 4 * 2048 + 4
+    assert bench.alg_bytes("fp8_layer_norm_2520x3072", _w(2520, 3072)) == 2520 * 3072 * 3 + 4
+    names = [n for n, _ in bench.page_shape_workloads()]
+    for R, D, _, _ in bench.PAGE_FP8_SHAPES:
+        if (R, D) != (4096, 3072):
+            assert f"fp8_broadcast_{R}x{D}" in names and f"fp8_layer_norm_{R}x{D}" in names
+    assert bench.page_context("fp8_broadcast_16x2048", 16, 2048)["us"] == 4.117
+    assert bench.page_context("fp8_layer_norm", 4096, 3072)["us"] == 16.412
+    assert bench.page_context("nvfp4_broadcast", 5070, 3072) is None
