@@ -40,11 +40,17 @@
  *    stated beside them (NVFP4AP_ERR_ALIGN otherwise).
  *  - dim must be at most NVFP4AP_MAX_DIM for the LayerNorm ops (a whole row
  *    is held in registers); the six-way op has no such limit.
- *  - Environment: each producer call reads the variables whose names start
- *    with NVFP4AP_ (one pass over the environment per call).  They select
- *    kernel families and launch shapes for experiments (e.g. NVFP4AP_KERNEL,
- *    NVFP4AP_PDL=0, NVFP4AP_WARPREG=0); none is needed, and every kernel
+ *  - Environment: each producer call reads three variables (one pass over
+ *    the environment per call); none is needed.  NVFP4AP_KERNEL=F[:C] forces
+ *    a kernel family for tests -- F = 3 register row kernels, 4 TMA
+ *    pipeline, 5 block-per-lane persistent kernels, 6 warp-per-row kernels
+ *    (FP8 segmented form and the two-level maximum pass), 8 one-row-per-CTA
+ *    block-per-lane kernels; a family that does not take a form or shape
+ *    falls back to the register row kernels (the table form: the TMA
+ *    pipeline) -- and C caps the persistent kernels at C CTAs per SM; every
  *    family meets the same output contract.
+ *    NVFP4AP_PDL=0 launches without programmatic dependent launch;
+ *    NVFP4AP_DEBUG=1 prints launch errors and the staged kernels' plans.
  */
 #ifndef NVFP4AP_H
 #define NVFP4AP_H

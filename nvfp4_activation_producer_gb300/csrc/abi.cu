@@ -30,28 +30,42 @@ inline bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintp
 constexpr int64_t kBlkBcastRows = 4096;
 constexpr int64_t kBlkNvfp4Rows = 2048;
 
-int env_int(const char* name) {
-  const char* v = env_get(name);
-  return v ? std::atoi(v) : 0;
+// Kernel families a call may be forced onto (NVFP4AP_KERNEL=F[:C]), for tests
+// that cover each family's instances; every family meets the same output
+// contract.  C caps the resident CTAs per SM of the persistent kernels, so a
+// small problem still walks many rows through each CTA.
+enum Family { FAM_AUTO = 0, FAM_ROWS = 3, FAM_TMA = 4, FAM_BLK = 5, FAM_WARP = 6, FAM_ROWBLK = 8 };
+struct Force {
+  int family, ctas;
+};
+Force forced() {
+  Force f{FAM_AUTO, 0};
+  const char* v = env_get("NVFP4AP_KERNEL");
+  if (!v) return f;
+  char* end = nullptr;
+  const long fam = std::strtol(v, &end, 10);
+  if (fam == FAM_ROWS || fam == FAM_TMA || fam == FAM_BLK || fam == FAM_WARP || fam == FAM_ROWBLK) f.family = (int)fam;
+  if (end && *end == ':') {
+    const long c = std::strtol(end + 1, nullptr, 10);
+    if (c > 0 && c < 64) f.ctas = (int)c;
+  }
+  return f;
 }
 
-// true when the variable is set to 0 (a default-on choice switched off)
-bool env_off(const char* name) {
-  const char* v = env_get(name);
-  return v && v[0] == '0';
+bool debug_on() {
+  const char* v = env_get("NVFP4AP_DEBUG");
+  return v && v[0] == '1';
 }
 
 // Launch shape for a row of `nvec` units (vectors or blocks): the candidate
 // per-thread counts are tried in order of preference and the one that wastes
 // the fewest thread slots (tpr * per_thread - nvec, tpr a multiple of 32 not
 // above the instance's limit) wins; ties keep the earlier candidate.
-// `forced` (> 0) restricts the choice to that per-thread count when it fits.
 template <typename MaxTpr>
-bool pick_shape(int64_t nvec, const int* cands, int ncand, MaxTpr max_tpr, int forced, RowShape* out) {
+bool pick_shape(int64_t nvec, const int* cands, int ncand, MaxTpr max_tpr, RowShape* out) {
   int64_t best_waste = -1;
   for (int i = 0; i < ncand; ++i) {
     const int nv = cands[i];
-    if (forced > 0 && nv != forced) continue;
     const int lim = max_tpr(nv);
     if (lim <= 0) continue;
     int64_t tpr = (nvec + nv - 1) / nv;
@@ -83,52 +97,23 @@ int sm_count() {
   return n;
 }
 
-// Shape of the TMA ring kernel for a row of `dim`: 8 warps per CTA and as
-// many stages (up to 4) as fit a budget of ~110 KB of shared memory per CTA,
-// so that two CTAs share an SM; fewer warps with one stage when a stage is
-// large.  Returns false when not even one warp with one stage fits (227 KB).
-bool pick_ring(int mod, int64_t dim, RingShape* rs) {
-  const int64_t budget = (env_int("NVFP4AP_RING_SMEM_KB") > 0 ? env_int("NVFP4AP_RING_SMEM_KB") : 110) * 1024;
-  int warps = env_int("NVFP4AP_RING_WARPS") > 0 ? env_int("NVFP4AP_RING_WARPS") : 8;
-  if (warps > 16) warps = 16;
-  int stages = env_int("NVFP4AP_RING_STAGES");
-  rs->ctas_per_sm = env_int("NVFP4AP_RING_CTAS");
-  if (stages <= 0) {
-    stages = 4;
-    while (stages > 1 && ring_smem_bytes(mod, dim, warps, stages) > budget) --stages;
-    while (warps > 1 && ring_smem_bytes(mod, dim, warps, stages) > budget) --warps;
-  }
-  if (stages > 8) stages = 8;
-  if (ring_smem_bytes(mod, dim, warps, stages) > 227 * 1024) return false;
-  rs->warps = warps;
-  rs->stages = stages;
-  return true;
-}
-
 // Shape of the register row kernel: 8-element chunks per thread from a
 // preference list (3 first: 24 elements per thread measured fastest on
 // GB300 at dim 1536-3072), the first that wastes the fewest thread slots;
 // up to 96 elements per thread for one input row, 48 for the per-token forms
-// (three input rows in registers).  Rows per CTA fill 128 threads
-// (NVFP4AP_ROWS_PER_CTA overrides).
+// (three input rows in registers).  Rows per CTA fill 128 threads.
 bool pick_rows(int mod, int64_t dim, RowShape* s) {
   static const int kWide[] = {3, 4, 6, 2, 8, 12, 1};
   static const int kToken[] = {3, 4, 2, 6, 1};
   const bool per_token = (mod == MOD_PTOK || mod == MOD_TABLE);
   const int* c = per_token ? kToken : kWide;
   const int n = per_token ? 5 : 7;
-  auto lim = [mod](int nv) { return ln_rows_max_tpr(mod, nv); };
-  if (!pick_shape(dim / 8, c, n, lim, env_int("NVFP4AP_PER_THREAD"), s) && !pick_shape(dim / 8, c, n, lim, 0, s))
-    return false;
-  const int want = env_int("NVFP4AP_ROWS_PER_CTA");
-  if (want > 0 && want <= 16 && want * s->tpr <= 512) s->rpc = want;  // the kernels are bounded to 512 threads
-  return true;
+  return pick_shape(dim / 8, c, n, [mod](int nv) { return ln_rows_max_tpr(mod, nv); }, s);
 }
 
 // The persistent broadcast kernel takes one row per CTA of at most 256
-// threads and up to 6 chunks per thread (NVFP4AP_PERSIST=0 turns it off).
+// threads and 1, 2, 3, 4 or 6 chunks per thread.
 bool persist_ok(const RowShape& s) {
-  if (env_int("NVFP4AP_PERSIST") < 0) return false;
   const bool nv_ok = s.per_thread == 1 || s.per_thread == 2 || s.per_thread == 3 || s.per_thread == 4 ||
                      s.per_thread == 6;
   return nv_ok && s.tpr <= 256 && s.rpc == 1;
@@ -136,7 +121,7 @@ bool persist_ok(const RowShape& s) {
 
 int finish(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4AP_OK;
-  if (env_int("NVFP4AP_DEBUG") > 0) std::fprintf(stderr, "nvfp4ap: launch failed: %s\n", cudaGetErrorString(e));
+  if (debug_on()) std::fprintf(stderr, "nvfp4ap: launch failed: %s\n", cudaGetErrorString(e));
   (void)cudaGetLastError();
   return NVFP4AP_ERR_LAUNCH;
 }
@@ -172,8 +157,36 @@ int check_modfp8(const LnArgs& a) {
   return NVFP4AP_OK;
 }
 
-// FP8 family: validation shared by every modulation source, then variant +
-// shape + launch.
+// The register row kernels: the persistent broadcast kernel for the broadcast
+// sources where its shape applies, the register-capped FULL instance for NVFP4
+// rows that exactly fill the CTA's chunks, else the flat row kernel.
+int run_rows(const LnArgs& a, bool nvfp4, int mod, const RowShape& rs, int ctas, cudaStream_t st) {
+  const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
+  if (!grid_ok(work, rs.rpc)) return NVFP4AP_ERR_SHAPE;
+  const int sms = sm_count();
+  if (mod_is_bcast(mod) && persist_ok(rs) && sms > 0)
+    return finish(launch_ln_bcast_persistent(a, nvfp4, mod, rs, sms, ctas, st));
+  if (nvfp4 && rs.tpr <= 128 && rs.per_thread >= 2 && rs.per_thread <= 4 &&
+      (int64_t)rs.tpr * rs.per_thread * 8 == a.dim)
+    return finish(launch_ln_rows_full(a, true, mod, rs, st));
+  return finish(launch_ln_rows(a, nvfp4, mod, rs, st));
+}
+
+// FP8 family: validation shared by every modulation source, then the kernel
+// and its shape.
+//
+// Default kernels (measured on GB300, graphs of 32 calls over rotating
+// buffers): the layer norm form on the one-row-per-CTA block-per-lane kernel
+// where the row fits it exactly (4096x3072 7.9 -> 7.55 us); the table form on
+// the TMA pipeline (16.1 against 17.4 us for the register row kernel at
+// 4096x3072); the three broadcast sources (bf16, modfp8, AWQ: one rule, so
+// that they reduce to each other bit for bit) on the block-per-lane
+// persistent kernel from kBlkBcastRows rows where its shape has no idle lane
+// and three or more rows per CTA (3072 x 4096 rows 28.2 -> 27.1 us for the
+// three sources, x 32768 177.7 -> 143.4 us; 1536 x 32768 100.1 -> 76.0 us;
+// 6144 x 32768 351 -> 290 us), else the persistent broadcast kernel (as fast
+// or faster below 4096 rows: 3072 x 2520 20.3 against 21.1 us); the
+// per-token form on the register row kernels.
 int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -189,7 +202,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
   if (mod == MOD_MODFP8 && (rc = check_modfp8(a)) != NVFP4AP_OK) return rc;
   if (!aligned(a.act_scale, 4)) return NVFP4AP_ERR_ALIGN;
 
-  // 16-byte vector path or bf16-pair path
+  // 16-byte vector kernels, bf16-pair kernel, or the element-wise kernel
   const void* bf_in[4] = {a.x, nullptr, nullptr, nullptr};
   if (mod == MOD_BCAST || mod == MOD_PTOK || mod == MOD_AWQ) { bf_in[1] = a.scale; bf_in[2] = a.shift; }
   if (mod == MOD_AWQ) bf_in[3] = a.inv_s;
@@ -207,103 +220,50 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     pair_ok = pair_ok && aligned(p, 4);
   }
   if (!vec8 && !pair_ok) return run_scalar(a, false, mod, st);
-  const int vec = vec8 ? 8 : 2;
 
-  // NVFP4AP_KERNEL: 0 auto (below), 1 warp-per-row TMA ring, 2 first register
-  // kernel, 3 register row kernels for every form, 4 TMA pipeline for every
-  // form, 5 block-per-lane persistent kernel, 8 one-row-per-CTA block-per-lane
-  // kernel.  The ring and TMA kernels have no modfp8 / AWQ source: those run
-  // on the register kernels.
-  int kernel = env_int("NVFP4AP_KERNEL");
-  // default: the one-row-per-CTA block-per-lane kernel for the layer norm
-  // form where the row fits it exactly (measured on GB300: 4096x3072 7.9 ->
-  // 7.55 us), the TMA pipeline for the table form; for the three broadcast
-  // sources (bf16, modfp8, AWQ: one rule, so that they reduce to each other
-  // bit for bit) the block-per-lane persistent kernel from kBlkBcastRows rows
-  // where its shape has no idle lane and three or more rows per CTA, else the
-  // persistent broadcast kernel.  Measured on GB300 (graphs of 32 calls),
-  // sum over the three sources: 3072 x 4096 rows 28.2 -> 27.1 us, x 32768
-  // 177.7 -> 143.4 us; 1536 x 32768 100.1 -> 76.0 us; 6144 x 32768 351 ->
-  // 290 us; below 4096 rows the persistent kernel is as fast or faster
-  // (3072 x 2520: 20.3 against 21.1 us).
-  if (kernel == 0) {
-    BlkShape bs{};
-    if (mod_is_bcast(mod) && a.rows >= kBlkBcastRows && vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
-        aligned(a.x, 32) && aligned(a.out, 16) && blk_default_shape(a.dim, true, &bs))
-      kernel = 5;
-    else
-      kernel = (mod == MOD_NONE) ? 8 : (mod == MOD_TABLE) ? 4 : 3;
-  }
-  if (kernel == 1 && (mod == MOD_MODFP8 || mod == MOD_AWQ)) kernel = 3;
-  if (kernel == 8) {
-    // one-row-per-CTA block-per-lane kernel where the row fits it exactly
-    // (the default for the layer norm form, see above), else the other defaults
-    RbShape rb{};
-    if (vec8 && (mod == MOD_NONE || mod_is_bcast(mod)) && aligned(a.x, 32) && aligned(a.out, 16) &&
-        pick_rowblk(a.dim, env_int("NVFP4AP_RB_BPT"), &rb))
-      return finish(launch_ln_rowblk(a, false, mod, rb, st));
-    kernel = (mod == MOD_TABLE) ? 4 : 3;
-  }
-  if (kernel == 5) {
-    // block-per-lane persistent kernel where it applies, else the default
-    if (vec8 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) && aligned(a.out, 16)) {
+  const Force f = forced();
+  if (vec8) {
+    const int sms = sm_count();
+    int fam = f.family;
+    if (fam == FAM_AUTO) {
       BlkShape bs{};
-      const int sms = sm_count();
-      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs, true)) {
-        bs.ctas_per_sm = env_int("NVFP4AP_BLK_CTAS");
-        bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+      if (mod_is_bcast(mod) && a.rows >= kBlkBcastRows && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
+          aligned(a.x, 32) && aligned(a.out, 16) && blk_default_shape(a.dim, true, &bs))
+        fam = FAM_BLK;
+      else
+        fam = (mod == MOD_NONE) ? FAM_ROWBLK : (mod == MOD_TABLE) ? FAM_TMA : FAM_ROWS;
+    }
+    if (fam == FAM_ROWBLK) {
+      RbShape rb{};
+      if ((mod == MOD_NONE || mod_is_bcast(mod)) && aligned(a.x, 32) && aligned(a.out, 16) &&
+          pick_rowblk(a.dim, 0, &rb))
+        return finish(launch_ln_rowblk(a, false, mod, rb, st));
+    }
+    if (fam == FAM_BLK && sms > 0 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) &&
+        aligned(a.out, 16)) {
+      BlkShape bs{};
+      if (pick_blk(a.dim, 0, &bs, true)) {
+        bs.ctas_per_sm = f.ctas;
         return finish(launch_ln_blk(a, false, mod, bs, sms, st));
       }
     }
-    kernel = (mod == MOD_TABLE) ? 4 : 3;
-  }
-  if (kernel == 6) {
-    // warp-per-row kernel (two sweeps of each row) where it applies, else the default
-    if (vec8 && (mod == MOD_NONE || mod == MOD_BCAST) && ln_blk_supported(BLK_FP8, mod, a.dim, 0) &&
-        aligned(a.x, 32) && aligned(a.out, 16)) {
-      const int sms = sm_count();
-      if (sms > 0 && !env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0)
-        return finish(launch_warp_regs(a, false, mod, sms, st));
-      if (sms > 0) return finish(launch_ln_warp_rows_fp8(a, mod, sms, st));
+    RowShape rs{};
+    if (pick_rows(mod, a.dim, &rs)) {
+      if ((fam == FAM_TMA || mod == MOD_TABLE) && fam != FAM_ROWS && sms > 0 && ln_tma_supported(false, mod, rs))
+        return finish(launch_ln_tma(a, false, mod, rs, sms, 0, f.ctas, wait_limit_cycles(), st));
+      return run_rows(a, false, mod, rs, f.ctas, st);
     }
-    kernel = (mod == MOD_TABLE) ? 4 : 3;
+    // rows too long for the register row kernels (per-token dims above 24576):
+    // the bf16-pair kernel below
   }
-  RingShape rs{};
-  if (vec8 && kernel == 1 && pick_ring(mod, a.dim, &rs)) {
-    const int sms = sm_count();
-    if (sms > 0) return finish(launch_ln_ring(a, false, mod, rs, sms, wait_limit_cycles(), st));
-  }
-  RowShape rows_shape{};
-  if (vec8 && (kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
-    if (!grid_ok(a.rows, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
-    const int sms = sm_count();
-    if (kernel == 4 && sms > 0 && ln_tma_supported(false, mod, rows_shape))
-      return finish(launch_ln_tma(a, false, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
-                                  env_int("NVFP4AP_TMA_CTAS"), wait_limit_cycles(), st));
-    if (mod_is_bcast(mod) && persist_ok(rows_shape) && sms > 0)
-      return finish(
-          launch_ln_bcast_persistent(a, false, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
-    return finish(launch_ln_rows(a, false, mod, rows_shape, st));
-  }
-
-  static const int kVec8[] = {3, 4, 2, 6, 8, 1};
   static const int kVec2[] = {8, 4, 16, 2, 32};
   RowShape s{};
-  const bool ok = vec8 ? pick_shape(a.dim / 8, kVec8, 6, [](int nv) { return ln_fp8_max_tpr(8, nv); },
-                                    env_int("NVFP4AP_FP8_PER_THREAD"), &s)
-                       : pick_shape(a.dim / 2, kVec2, 5, [](int nv) { return ln_fp8_max_tpr(2, nv); },
-                                    env_int("NVFP4AP_FP8_PER_THREAD"), &s);
-  if (!ok) {
-    // a forced per-thread count that does not fit: fall back to the default choice
-    if (!(vec8 ? pick_shape(a.dim / 8, kVec8, 6, [](int nv) { return ln_fp8_max_tpr(8, nv); }, 0, &s)
-               : pick_shape(a.dim / 2, kVec2, 5, [](int nv) { return ln_fp8_max_tpr(2, nv); }, 0, &s)))
-      return NVFP4AP_ERR_DIM;
-  }
+  if (!pick_shape(a.dim / 2, kVec2, 5, [](int nv) { return ln_fp8_max_tpr(2, nv); }, &s)) return NVFP4AP_ERR_DIM;
   if (!grid_ok(a.rows, s.rpc)) return NVFP4AP_ERR_SHAPE;
-  return finish(launch_ln_fp8(a, mod, vec, s, st));
+  return finish(launch_ln_fp8(a, mod, 2, s, st));
 }
 
-// Segmented modulation: index and tables present and aligned.
+// Segmented modulation: index present and aligned, at least one segment.
 int check_seg(const LnArgs& a) {
   if (!a.seg_idx || !a.seg_scale || !a.seg_shift) return NVFP4AP_ERR_NULL;
   if (a.nseg < 1) return NVFP4AP_ERR_INDEX;
@@ -311,8 +271,10 @@ int check_seg(const LnArgs& a) {
   return NVFP4AP_OK;
 }
 
-// Segmented modulation producers (FP8 and single-level NVFP4) on the register
-// row kernels: dim % 8 (FP8) or % 16 (NVFP4), 16-byte aligned x and outputs.
+// Segmented modulation producers (FP8 and single-level NVFP4).  Default: for
+// FP8 on many rows the warp-per-row kernels (the row held in registers where a
+// lane's share fits, measured on GB300 at 37810x5376: 119.7 -> 101.1 us),
+// else the register row kernels.
 int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -326,37 +288,37 @@ int run_seg(LnArgs& a, bool nvfp4, cudaStream_t st) {
   if (a.dim % 8 != 0 || !aligned(a.x, 16) || !aligned(a.out, 8) || !aligned(a.seg_scale, 16) ||
       !aligned(a.seg_shift, 16))
     return run_scalar(a, nvfp4, MOD_SEG, st);
-  if (env_int("NVFP4AP_KERNEL") == 5 && ln_blk_supported(nvfp4 ? BLK_NVFP4 : BLK_FP8, MOD_SEG, a.dim, a.nseg) &&
+  const Force f = forced();
+  const int sms = sm_count();
+  if (f.family == FAM_BLK && sms > 0 && ln_blk_supported(nvfp4 ? BLK_NVFP4 : BLK_FP8, MOD_SEG, a.dim, a.nseg) &&
       aligned(a.x, 32) && aligned(a.out, 16)) {
     BlkShape bs{};
-    const int sms = sm_count();
-    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs, !nvfp4)) {
-      bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+    if (pick_blk(a.dim, 0, &bs, !nvfp4)) {
+      bs.ctas_per_sm = f.ctas;
       return finish(launch_ln_blk(a, nvfp4, MOD_SEG, bs, sms, st));
     }
   }
-  // FP8, many rows: the warp-per-row kernel (NVFP4AP_SEG_WARP=1 forces it,
-  // -1 turns it off)
-  if (!nvfp4 && env_int("NVFP4AP_KERNEL") != 5 && env_int("NVFP4AP_SEG_WARP") >= 0 &&
+  if (!nvfp4 && (f.family == FAM_AUTO || f.family == FAM_WARP) && sms > 0 &&
       ln_blk_supported(BLK_FP8, MOD_SEG, a.dim, a.nseg) && aligned(a.x, 32) && aligned(a.out, 16)) {
-    const int sms = sm_count();
-    // the row held in registers where a lane's share fits (NVFP4AP_WARPREG=0:
-    // the two-sweep kernel; measured on GB300 at 37810x5376: 119.7 -> 101.1 us)
-    const bool regs = !env_off("NVFP4AP_WARPREG") && warp_regs_bpl(a.dim) > 0;
-    if (sms > 0 && (env_int("NVFP4AP_SEG_WARP") > 0 || warp_path_rows(a.rows, a.dim, sms, regs))) {
-      if (regs) return finish(launch_warp_regs(a, false, MOD_SEG, sms, st));
-      return finish(launch_ln_warp_rows_fp8(a, MOD_SEG, sms, st));
+    const bool regs = warp_regs_bpl(a.dim) > 0;
+    if (f.family == FAM_WARP || warp_path_rows(a.rows, a.dim, sms, regs)) {
+      if (regs) return finish(launch_warp_regs(a, false, MOD_SEG, sms, f.ctas, st));
+      return finish(launch_ln_warp_rows_fp8(a, MOD_SEG, sms, f.ctas, st));
     }
   }
   RowShape s{};
-  if (!pick_rows(MOD_SEG, a.dim, &s)) return NVFP4AP_ERR_DIM;
+  if (!pick_rows(MOD_SEG, a.dim, &s)) return run_scalar(a, nvfp4, MOD_SEG, st);
   const int64_t work = nvfp4 ? (a.rows + 127) / 128 * 128 : a.rows;
   if (!grid_ok(work, s.rpc)) return NVFP4AP_ERR_SHAPE;
   return finish(launch_ln_seg(a, nvfp4, s, st));
 }
 
 // Two-level NVFP4 producers: as the NVFP4 producers, plus a 4-byte aligned
-// tensor-scale output and workspace word.
+// tensor-scale output and workspace.  Default: the block-per-lane kernels --
+// persistent, one atomic per CTA in the maximum pass, the flat quantising pass
+// (measured on GB300: 37810x5376 segmented 341 -> 284 us, 5070x3072 20.9 ->
+// 18.5 us), with the warp-per-row maximum pass for large tensors; the register
+// row kernels where those do not apply (or forced: NVFP4AP_KERNEL=3).
 int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -371,17 +333,13 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   // the workspace's statistics slots follow the word (16 bytes in)
   a.row_stats = reinterpret_cast<float*>(reinterpret_cast<char*>(a.amax_ws) + 16);
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
-  // default (and NVFP4AP_KERNEL=5): the block-per-lane kernels -- persistent,
-  // one atomic per CTA in the maximum pass -- where they apply (measured on
-  // GB300: 37810x5376 segmented 341 -> 284 us, 5070x3072 20.9 -> 18.5 us);
-  // any other NVFP4AP_KERNEL value, or a shape they do not take: the register
-  // row kernels
-  const int kernel = env_int("NVFP4AP_KERNEL");
-  if ((kernel == 0 || kernel == 5) && ln_blk_supported(BLK_2LEVEL, mod, a.dim, a.nseg) && aligned(a.x, 32)) {
+  const Force f = forced();
+  if (f.family != FAM_ROWS && ln_blk_supported(BLK_2LEVEL, mod, a.dim, a.nseg) && aligned(a.x, 32)) {
     BlkShape bs{};
     const int sms = sm_count();
-    if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
-      bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
+    if (sms > 0 && pick_blk(a.dim, 0, &bs)) {
+      bs.ctas_per_sm = f.ctas;
+      bs.warp = f.family == FAM_WARP ? 1 : f.family == FAM_BLK ? -1 : 0;
       return finish(launch_ln_2level_blk(a, mod, bs, sms, st));
     }
   }
@@ -389,13 +347,22 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   if (!pick_rows(mod, a.dim, &s)) return NVFP4AP_ERR_DIM;
   if (!grid_ok((a.rows + 127) / 128 * 128, s.rpc)) return NVFP4AP_ERR_SHAPE;
   // the register-capped instances for rows that exactly fill the CTA's
-  // chunks (NVFP4AP_FULL=0 turns them off); unmodulated rows only -- the
-  // broadcast instances spill at 40 registers
-  const bool full = !env_off("NVFP4AP_FULL") && mod == MOD_NONE && s.tpr <= 128 && s.per_thread >= 2 &&
-                    s.per_thread <= 4 && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
+  // chunks; unmodulated rows only -- the broadcast instances spill at 40
+  // registers
+  const bool full = mod == MOD_NONE && s.tpr <= 128 && s.per_thread >= 2 && s.per_thread <= 4 &&
+                    (int64_t)s.tpr * s.per_thread * 8 == a.dim;
   return finish(launch_ln_2level(a, mod, s, full, st));
 }
 
+// Single-level NVFP4 producers.  Default (measured on GB300 at dims
+// 2048-8192, 2,520-32,768 rows): the one-row-per-CTA block-per-lane kernel
+// where the row fits it exactly (5070x3072 layer norm 10.0 -> 8.5 us,
+// broadcast 12.2 -> 10.6 us against the register row and persistent
+// kernels); where it does not, the block-per-lane persistent kernel from
+// kBlkNvfp4Rows rows when its shape has no idle lane and three or more rows
+// per CTA (dims 1024, 1536, 5120: 1536 x 32768 layer norm 33.4 -> 22.2 us,
+// broadcast 36.8 -> 28.3 us; 5120 x 4096 broadcast 20.1 -> 16.0 us), else the
+// register row kernels.
 int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   int rc = check_common(a.rows, a.dim, a.eps);
   if (rc) return rc;
@@ -411,77 +378,31 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
       (mod == MOD_MODFP8 && (!aligned(a.scale8, 8) || !aligned(a.shift8, 8))))
     return run_scalar(a, true, mod, st);
 
-  int kernel = env_int("NVFP4AP_KERNEL");  // as for FP8, 8: one-row-per-CTA block-per-lane kernels
-  // default: the one-row-per-CTA block-per-lane kernel where the row fits it
-  // exactly (measured faster than the register row and persistent kernels on
-  // GB300 at dims 2048-8192, 2,520-32,768 rows: 5070x3072 layer norm 10.0 ->
-  // 8.5 us, broadcast 12.2 -> 10.6 us); where it does not, the block-per-lane
-  // persistent kernel from kBlkNvfp4Rows rows when its shape has no idle lane
-  // and three or more rows per CTA (dims 1024, 1536, 5120; measured at
-  // 2,520-32,768 rows: faster at every size, 1536 x 32768 layer norm 33.4 ->
-  // 22.2 us, broadcast 36.8 -> 28.3 us, 5120 x 4096 broadcast 20.1 -> 16.0
-  // us), else the register row kernels
+  const Force f = forced();
+  const int sms = sm_count();
   const bool blk_ok = ln_blk_supported(BLK_NVFP4, mod, a.dim, 0) && aligned(a.x, 32);
-  if (kernel == 0 || kernel == 8) {
+  int fam = f.family;
+  if (fam == FAM_AUTO || fam == FAM_ROWBLK) {
     RbShape rb{};
-    if ((mod == MOD_NONE || mod == MOD_BCAST || mod == MOD_MODFP8) && aligned(a.x, 32) &&
-        pick_rowblk(a.dim, env_int("NVFP4AP_RB_BPT"), &rb))
-      return finish(launch_ln_rowblk(a, true, mod, rb, st));
+    if (aligned(a.x, 32) && pick_rowblk(a.dim, 0, &rb)) return finish(launch_ln_rowblk(a, true, mod, rb, st));
     BlkShape bs{};
-    kernel = (kernel == 0 && a.rows >= kBlkNvfp4Rows && blk_ok && blk_default_shape(a.dim, false, &bs)) ? 5 : 3;
+    fam = (fam == FAM_AUTO && a.rows >= kBlkNvfp4Rows && blk_ok && blk_default_shape(a.dim, false, &bs)) ? FAM_BLK
+                                                                                                         : FAM_ROWS;
   }
-  if (kernel == 5) {
-    if (blk_ok) {
-      BlkShape bs{};
-      const int sms = sm_count();
-      if (sms > 0 && pick_blk(a.dim, env_int("NVFP4AP_BLK_BPT"), &bs)) {
-        bs.ctas_per_sm = env_int("NVFP4AP_BLK_CTAS");
-        bs.max_ctas = env_int("NVFP4AP_BLK_GRID");
-        return finish(launch_ln_blk(a, true, mod, bs, sms, st));
-      }
+  if (fam == FAM_BLK && blk_ok && sms > 0) {
+    BlkShape bs{};
+    if (pick_blk(a.dim, 0, &bs)) {
+      bs.ctas_per_sm = f.ctas;
+      return finish(launch_ln_blk(a, true, mod, bs, sms, st));
     }
-    kernel = 3;
   }
-  // the modfp8 source runs on the register kernels only
-  if (mod == MOD_MODFP8 && kernel != 3 && kernel != 4) kernel = 3;
-  RingShape rs{};
-  if (kernel == 1 && pick_ring(mod, a.dim, &rs)) {
-    const int sms = sm_count();
-    if (sms > 0) return finish(launch_ln_ring(a, true, mod, rs, sms, wait_limit_cycles(), st));
+  RowShape rs{};
+  if (!pick_rows(mod, a.dim, &rs)) return run_scalar(a, true, mod, st);
+  if (fam == FAM_TMA && mod != MOD_MODFP8 && sms > 0 && ln_tma_supported(true, mod, rs)) {
+    if (!grid_ok((a.rows + 127) / 128 * 128, rs.rpc)) return NVFP4AP_ERR_SHAPE;
+    return finish(launch_ln_tma(a, true, mod, rs, sms, 0, f.ctas, wait_limit_cycles(), st));
   }
-  RowShape rows_shape{};
-  if ((kernel == 3 || kernel == 4) && pick_rows(mod, a.dim, &rows_shape)) {
-    const int64_t rows_pad = (a.rows + 127) / 128 * 128;
-    if (!grid_ok(rows_pad, rows_shape.rpc)) return NVFP4AP_ERR_SHAPE;
-    const int sms = sm_count();
-    if (kernel == 4 && sms > 0 && ln_tma_supported(true, mod, rows_shape))
-      return finish(launch_ln_tma(a, true, mod, rows_shape, sms, env_int("NVFP4AP_TMA_STAGES"),
-                                  env_int("NVFP4AP_TMA_CTAS"), wait_limit_cycles(), st));
-    // four rows of a scale tile per CTA (whole 16-byte scale chunks): opt-in
-    // with NVFP4AP_TILE4=1 -- measured slower on GB300 than one row per CTA
-    const bool tile4 = env_int("NVFP4AP_TILE4") > 0 && rows_shape.tpr <= 128 && rows_shape.per_thread <= 4 &&
-                       aligned(a.sf, 16) && (mod == MOD_NONE || mod == MOD_BCAST);
-    if (mod_is_bcast(mod) && persist_ok(rows_shape) && sms > 0 && !tile4)
-      return finish(
-          launch_ln_bcast_persistent(a, true, mod, rows_shape, sms, env_int("NVFP4AP_PERSIST_CTAS"), st));
-    if (tile4) return finish(launch_ln_rows_tile4(a, mod, rows_shape, st));
-    // rows that exactly fill the CTA's chunks: the register-capped instance
-    // (NVFP4AP_FULL=0 turns it off)
-    if (!env_off("NVFP4AP_FULL") && rows_shape.tpr <= 128 && rows_shape.per_thread >= 2 && rows_shape.per_thread <= 4 &&
-        (int64_t)rows_shape.tpr * rows_shape.per_thread * 8 == a.dim)
-      return finish(launch_ln_rows_full(a, true, mod, rows_shape, st));
-    return finish(launch_ln_rows(a, true, mod, rows_shape, st));
-  }
-
-  static const int kCands[] = {2, 3, 1, 4, 6};
-  RowShape s{};
-  if (!pick_shape(a.dim / 16, kCands, 5, [](int b) { return ln_nvfp4_max_tpr(b); },
-                  env_int("NVFP4AP_NVFP4_PER_THREAD"), &s) &&
-      !pick_shape(a.dim / 16, kCands, 5, [](int b) { return ln_nvfp4_max_tpr(b); }, 0, &s))
-    return NVFP4AP_ERR_DIM;
-  const int64_t rows_pad = (a.rows + 127) / 128 * 128;
-  if (!grid_ok(rows_pad, s.rpc)) return NVFP4AP_ERR_SHAPE;
-  return finish(launch_ln_nvfp4(a, mod, s, st));
+  return run_rows(a, true, mod, rs, f.ctas, st);
 }
 
 LnArgs ln_args(const void* x, float eps, void* out, int64_t rows, int64_t dim) {

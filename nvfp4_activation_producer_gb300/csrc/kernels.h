@@ -81,8 +81,8 @@ struct RowShape {
   int tpr, per_thread, rpc;
 };
 
-// FP8 producers (every modulation source).  `vec` is 8 (16-byte vectors) or 2
-// (bf16 pairs).
+// FP8 producers on the bf16-pair kernel (every modulation source except the
+// segmented one): `vec` must be 2 (one bf16 pair per vector).
 cudaError_t launch_ln_fp8(const LnArgs& a, int mod, int vec, RowShape s, cudaStream_t st);
 // Largest threads-per-row (and threads-per-CTA) the (vec, per_thread)
 // instance accepts; 0 if there is no such instance.
@@ -96,10 +96,6 @@ int ln_rows_max_tpr(int mod, int per_thread);
 // row per CTA of tpr <= 128 threads, registers capped at 40 per thread;
 // per_thread 2..4; mod MOD_NONE, MOD_BCAST or MOD_MODFP8.
 cudaError_t launch_ln_rows_full(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st);
-// NVFP4 row kernel with four rows of one 128-row tile per CTA (rows r, r+32,
-// r+64, r+96): scale bytes leave as whole 16-byte chunks.  tpr <= 128,
-// per_thread 1..4, 16-byte aligned scale buffer.
-cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
 // Persistent broadcast-modulation variant (one row per CTA at a time, the
 // next row prefetched, fp32 modulation in registers): tpr <= 256, rpc == 1,
 // per_thread in {1, 2, 3, 4, 6}; at most `ctas_per_sm` CTAs per SM (0 = as
@@ -110,12 +106,13 @@ cudaError_t launch_ln_bcast_persistent(const LnArgs& a, bool nvfp4, int mod, Row
 // Block-per-lane persistent row kernels (ln_blk.cuh; ln_blk.cu, ln_blk2l.cu):
 // a lane owns whole 16-element blocks (`bpt` of them), `tpr` threads per row
 // (a multiple of 32, <= 256), 512-thread CTAs of 512 / tpr rows, at most
-// `ctas_per_sm` CTAs per SM (0 = as many as fit), at most `max_ctas` CTAs in
-// all (0 = no limit).  Modulation as fp32 tables in shared memory.
+// `ctas_per_sm` CTAs per SM (0 = as many as fit).  Modulation as fp32 tables in
+// shared memory.  `warp` (two-level only): 1 forces the warp-per-row maximum
+// pass, -1 the row-group one, 0 chooses by size.
 // dim % 16 == 0, dim <= kBlkMaxDim; x 32-byte aligned; FP8 out 16-byte
 // aligned; broadcast bf16 sources and segment tables 16-byte aligned.
 struct BlkShape {
-  int tpr, bpt, ctas_per_sm, max_ctas;
+  int tpr, bpt, ctas_per_sm, warp;
 };
 constexpr int64_t kBlkMaxDim = 8192;
 enum { BLK_FP8 = 0, BLK_NVFP4 = 1, BLK_2LEVEL = 2 };
@@ -131,17 +128,15 @@ cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int 
 // two-level NVFP4 on the block-per-lane kernels: clears a.amax_ws, maximum
 // pass, quantising pass; mod MOD_NONE, MOD_BCAST or MOD_SEG
 cudaError_t launch_ln_2level_blk(const LnArgs& a, int mod, BlkShape s, int sms, cudaStream_t st);
-// Warp-per-row FP8 producers (ln_blk.cuh): each warp sweeps its rows twice
-// (sums, then codes from the blocks read again through L1/L2); for at least
-// ln_warp_rows_min(sms) rows; mod MOD_NONE, MOD_BCAST or MOD_SEG (tables as
-// for the block-per-lane kernels).
-int64_t ln_warp_rows_min(int sms);
-cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStream_t st);
+// Warp-per-row FP8 segmented producer (ln_blk.cuh): each warp sweeps its rows
+// twice (sums, then codes from the blocks read again through L1/L2); mod
+// MOD_SEG (tables as for the block-per-lane kernels); ctas_per_sm as above.
+cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, int ctas_per_sm, cudaStream_t st);
 // Register-resident warp-per-row producers (ln_warpreg.cu): the same
 // operations as the warp-per-row kernels with the row read once.  Lanes hold
 // warp_regs_bpl(dim) blocks (0 when dim is not a multiple of 16 or above
-// 6144); amax: the two-level maximum pass (else FP8); mod MOD_NONE,
-// MOD_BCAST or MOD_SEG.
+// 6144); amax: the two-level maximum pass (mod MOD_NONE, MOD_BCAST or
+// MOD_SEG), else the FP8 segmented producer (MOD_SEG); ctas_per_sm as above.
 int warp_regs_bpl(int64_t dim);
 // whether the warp-per-row path takes `rows` x `dim` on `sms` SMs: the two-sweep
 // kernel from 4 rows per warp of its grid (sms * 128 rows); the
@@ -149,7 +144,7 @@ int warp_regs_bpl(int64_t dim);
 // sms * 128 * 3072 (measured on GB300: at 12000x5376 the two-level maximum pass
 // 70.4 -> 60.9 us against the row-group kernel, at 12000x3072 a tie)
 bool warp_path_rows(int64_t rows, int64_t dim, int sms, bool regs);
-cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, cudaStream_t st);
+cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, int ctas_per_sm, cudaStream_t st);
 // read and clear the segment-index fault words of the two translation units
 cudaError_t take_blk_seg_fault(unsigned int* fault);
 cudaError_t take_blk2l_seg_fault(unsigned int* fault);
@@ -172,20 +167,6 @@ cudaError_t launch_ln_rowblk(const LnArgs& a, bool nvfp4, int mod, RbShape s, cu
 cudaError_t launch_ln_scalar(const LnArgs& a, bool nvfp4, int mod, cudaStream_t st);
 cudaError_t take_scalar_seg_fault(unsigned int* fault);
 
-// NVFP4 producers (K5-K6).
-cudaError_t launch_ln_nvfp4(const LnArgs& a, int mod, RowShape s, cudaStream_t st);
-int ln_nvfp4_max_tpr(int per_thread);
-
-// TMA-staged persistent ring kernels (FP8 and NVFP4): `warps` warps per
-// CTA, each with `stages` shared-memory stages of one row; at most
-// `ctas_per_sm` CTAs per SM (0 = as many as fit).  Needs dim % 8 == 0 (FP8)
-// or % 16 == 0 (NVFP4) and 16-byte aligned inputs.
-struct RingShape {
-  int warps, stages, ctas_per_sm;
-};
-int64_t ring_smem_bytes(int mod, int64_t dim, int warps, int stages);
-cudaError_t launch_ln_ring(const LnArgs& a, bool nvfp4, int mod, RingShape rs, int sms, long long wait_limit,
-                           cudaStream_t st);
 // FP8 broadcast producer on the ring kernel with its per-CTA words in the
 // library's static scratch array; returns an NVFP4AP_* status (arguments
 // already validated, dim % 8 == 0, 16-byte aligned inputs).

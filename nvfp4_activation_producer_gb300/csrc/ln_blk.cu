@@ -1,8 +1,8 @@
 // ln_blk.cu -- instances of the block-per-lane kernel template (ln_blk.cuh)
 // for the single-level producers: FP8 (no modulation, broadcast bf16, modfp8,
 // AWQ, segmented) and NVFP4 (no modulation, broadcast bf16, modfp8,
-// segmented), and the shape choice; the warp-per-row FP8 kernels (no
-// modulation, broadcast bf16, segmented) for many rows.
+// segmented), and the shape choice; the warp-per-row FP8 segmented kernel
+// (two sweeps of each row) for many rows.
 #include "ln_blk.cuh"
 
 namespace nvfp4ap {
@@ -34,7 +34,7 @@ bool pick_blk(int64_t dim, int forced_bpt, BlkShape* s, bool fp8) {
   if (best < 0) return false;
   s->bpt = best;
   s->ctas_per_sm = 0;
-  s->max_ctas = 0;
+  s->warp = 0;
   return true;
 }
 
@@ -74,15 +74,9 @@ cudaError_t launch_ln_blk(const LnArgs& a, bool nvfp4, int mod, BlkShape s, int 
   }
 }
 
-int64_t ln_warp_rows_min(int sms) { return warp_rows_min(sms); }
-
-cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, cudaStream_t st) {
-  switch (mod) {
-    case MOD_NONE: return launch_warp_rows<BK_FP8, MOD_NONE>(a, sms, st);
-    case MOD_BCAST: return launch_warp_rows<BK_FP8, MOD_BCAST>(a, sms, st);
-    case MOD_SEG: return launch_warp_rows<BK_FP8, MOD_SEG>(a, sms, st);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_ln_warp_rows_fp8(const LnArgs& a, int mod, int sms, int ctas_per_sm, cudaStream_t st) {
+  if (mod != MOD_SEG) return cudaErrorInvalidValue;
+  return launch_warp_rows<BK_FP8, MOD_SEG>(a, sms, ctas_per_sm, st);
 }
 
 cudaError_t take_blk_seg_fault(unsigned int* fault) { return take_blk_word(fault); }

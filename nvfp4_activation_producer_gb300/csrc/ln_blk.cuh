@@ -519,8 +519,9 @@ inline bool flat_smem_limit(const void* k) {
 // several (one 1024-thread CTA per SM)
 inline int64_t warp_rows_min(int sms) { return (int64_t)sms * (kWarpRowThreads / 32) * 4; }
 
+// ctas_per_sm > 0 caps the resident CTAs per SM (tests: many rows per warp)
 template <int KIND, int MOD>
-cudaError_t launch_warp_rows(const LnArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_warp_rows(const LnArgs& a, int sms, int ctas_per_sm, cudaStream_t st) {
   auto k = warp_rows_kernel<KIND, MOD>;
   const int64_t smem64 = blk_tab_float4s(MOD, a.dim / 16, a.nseg) * (int64_t)sizeof(float4);
   if (smem64 > kBlkMaxSmem || !flat_smem_limit((const void*)k)) return cudaErrorInvalidValue;
@@ -528,6 +529,7 @@ cudaError_t launch_warp_rows(const LnArgs& a, int sms, cudaStream_t st) {
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kWarpRowThreads, smem) != cudaSuccess || occ < 1)
     return cudaErrorInvalidConfiguration;
+  if (ctas_per_sm > 0 && ctas_per_sm < occ) occ = ctas_per_sm;
   int64_t grid = (int64_t)sms * occ;
   const int64_t need = (a.rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
   if (grid > need) grid = need;
@@ -574,7 +576,6 @@ cudaError_t launch_blk(const LnArgs& a, BlkShape s, int sms, cudaStream_t st) {
   const int64_t need = (a.rows + ngrp - 1) / ngrp;
   int64_t grid = (int64_t)sms * occ;
   if (grid > need) grid = need;
-  if (s.max_ctas > 0 && grid > s.max_ctas) grid = s.max_ctas;
   if (grid < 1) grid = 1;
   const float inv_d = (float)(1.0 / (double)a.dim);
   return launch_maybe_pdl(k, dim3((unsigned)grid), dim3(ngrp * s.tpr), (size_t)smem, st, a, inv_d, s.tpr);

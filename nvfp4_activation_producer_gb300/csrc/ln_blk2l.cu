@@ -134,19 +134,15 @@ template <int MOD>
 cudaError_t run_blk_2level(const LnArgs& a, BlkShape s, int sms, cudaStream_t st) {
   cudaError_t e = launch_maybe_pdl(blk_clear_word_kernel, dim3(1), dim3(1), 0, st, a.amax_ws);
   if (e != cudaSuccess) return e;
-  // maximum pass: warp per row for large tensors (warp_path_rows;
-  // NVFP4AP_2L_AMAX=1 forces it, 2 the row-group kernel)
-  const char* v = env_get("NVFP4AP_2L_AMAX");
-  const int force = v ? std::atoi(v) : 0;
-  // the warp-per-row pass with the row held in registers where a lane's share
-  // fits (NVFP4AP_WARPREG=0: the two-sweep kernel)
-  const char* wr = env_get("NVFP4AP_WARPREG");
-  const bool regs_ok = !(wr != nullptr && wr[0] == '0') && warp_regs_bpl(a.dim) > 0;
+  // maximum pass: warp per row for large tensors (warp_path_rows; s.warp = 1
+  // forces it, -1 the row-group kernel), the row held in registers where a
+  // lane's share fits, else two sweeps of each row
+  const bool regs_ok = warp_regs_bpl(a.dim) > 0;
   const bool warp_rows = a.row_stats != nullptr &&
-                         (force == 1 || (force == 0 && warp_path_rows(a.rows, a.dim, sms, regs_ok)));
+                         (s.warp > 0 || (s.warp == 0 && warp_path_rows(a.rows, a.dim, sms, regs_ok)));
   const bool regs = warp_rows && regs_ok;
-  e = regs        ? launch_warp_regs(a, true, MOD, sms, st)
-      : warp_rows ? launch_warp_rows<BK_AMAX, MOD>(a, sms, st)
+  e = regs        ? launch_warp_regs(a, true, MOD, sms, s.ctas_per_sm, st)
+      : warp_rows ? launch_warp_rows<BK_AMAX, MOD>(a, sms, s.ctas_per_sm, st)
                   : launch_blk_bpt<BK_AMAX, MOD>(a, s, sms, st);
   if (e != cudaSuccess) return e;
   // flat quantising pass when the statistics were kept and the block index

@@ -12,6 +12,11 @@
 // y = (x - mean) * rstd * (1 + scale) + shift, out = e4m3fn(y / act_scale)
 // rounded to nearest-even and saturated to +-448.
 //
+// This file serves the bf16-pair path: rows whose dim is even but not a
+// multiple of 8, or bf16 pointers that are 4-byte but not 16-byte aligned (a
+// thread loads one bf16 pair per vector, VEC = 2), and per-token rows too
+// long for the register row kernels.
+//
 // Design: a row is owned by `tpr` threads (one warp up to one CTA, picked by
 // dim on the host).  Every thread issues all of its loads of the row (and of
 // per-token modulation rows) before any arithmetic, so x is read from HBM
@@ -200,25 +205,13 @@ cudaError_t launch_mod(const LnArgs& a, RowShape s, cudaStream_t st) {
   case N:                                                   \
     ln_fp8_kernel<MOD, N, VEC><<<grid, block, 0, st>>>(a);  \
     break;
-  if constexpr (VEC == 8) {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(1)
-      NVFP4AP_CASE(2)
-      NVFP4AP_CASE(3)
-      NVFP4AP_CASE(4)
-      NVFP4AP_CASE(6)
-      NVFP4AP_CASE(8)
-      default: return cudaErrorInvalidValue;
-    }
-  } else {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(2)
-      NVFP4AP_CASE(4)
-      NVFP4AP_CASE(8)
-      NVFP4AP_CASE(16)
-      NVFP4AP_CASE(32)
-      default: return cudaErrorInvalidValue;
-    }
+  switch (s.per_thread) {
+    NVFP4AP_CASE(2)
+    NVFP4AP_CASE(4)
+    NVFP4AP_CASE(8)
+    NVFP4AP_CASE(16)
+    NVFP4AP_CASE(32)
+    default: return cudaErrorInvalidValue;
   }
 #undef NVFP4AP_CASE
   return cudaGetLastError();
@@ -240,12 +233,6 @@ cudaError_t launch_vec(const LnArgs& a, int mod, RowShape s, cudaStream_t st) {
 }  // namespace
 
 int ln_fp8_max_tpr(int vec, int per_thread) {
-  if (vec == 8) {
-    switch (per_thread) {
-      case 1: case 2: case 3: case 4: case 6: case 8: return fp8_max_tpr(per_thread, 8);
-      default: return 0;
-    }
-  }
   if (vec == 2) {
     switch (per_thread) {
       case 2: case 4: case 8: case 16: case 32: return fp8_max_tpr(per_thread, 2);
@@ -256,7 +243,6 @@ int ln_fp8_max_tpr(int vec, int per_thread) {
 }
 
 cudaError_t launch_ln_fp8(const LnArgs& a, int mod, int vec, RowShape s, cudaStream_t st) {
-  if (vec == 8) return launch_vec<8>(a, mod, s, st);
   if (vec == 2) return launch_vec<2>(a, mod, s, st);
   return cudaErrorInvalidValue;
 }

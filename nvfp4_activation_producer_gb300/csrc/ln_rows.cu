@@ -246,9 +246,7 @@ cudaError_t launch_persist(const LnArgs& a, RowShape s, int sms, int ctas_per_sm
   const float inv_d = (float)(1.0 / (double)a.dim);
   const int64_t work_rows = KIND == KIND_NVFP4 ? (a.rows + 127) / 128 * 128 : a.rows;
   // rows that exactly fill the threads' chunks take the FULL instance
-  // (NVFP4AP_FULL=0 turns it off)
-  const char* full_env = env_get("NVFP4AP_FULL");
-  const bool full = !(full_env && full_env[0] == '0') && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
+  const bool full = (int64_t)s.tpr * s.per_thread * 8 == a.dim;
 #define NVFP4AP_CASE(N)                                                                        \
   case N: {                                                                                    \
     auto k = (full && N >= 2 && N <= 4) ? ln_bcast_persist_kernel<KIND, MOD, N, (N >= 2 && N <= 4)> \
@@ -310,7 +308,7 @@ cudaError_t launch_ln_rows_full(const LnArgs& a, bool nvfp4, int mod, RowShape s
   const float inv_d = (float)(1.0 / (double)a.dim);
 #define NVFP4AP_CASE(M, N)                                                                                        \
   case N:                                                                                                         \
-    return launch_maybe_pdl(ln_rows_kernel<KIND_NVFP4, M, N, false, kFullMinBlocks>, grid, block, 0, st, a, inv_d);
+    return launch_maybe_pdl(ln_rows_kernel<KIND_NVFP4, M, N, kFullMinBlocks>, grid, block, 0, st, a, inv_d);
 #define NVFP4AP_MOD(M)          \
   case M:                       \
     switch (s.per_thread) {     \
@@ -327,35 +325,6 @@ cudaError_t launch_ln_rows_full(const LnArgs& a, bool nvfp4, int mod, RowShape s
   }
 #undef NVFP4AP_MOD
 #undef NVFP4AP_CASE
-}
-
-cudaError_t launch_ln_rows_tile4(const LnArgs& a, int mod, RowShape s, cudaStream_t st) {
-  if (s.tpr > 128) return cudaErrorInvalidValue;
-  const int64_t rows_pad = (a.rows + 127) / 128 * 128;
-  const dim3 block(s.tpr, 4), grid((unsigned)(rows_pad / 4));
-  const float inv_d = (float)(1.0 / (double)a.dim);
-#define NVFP4AP_CASE(M, N)                                                                          \
-  case N:                                                                                           \
-    return launch_maybe_pdl(ln_rows_kernel<KIND_NVFP4, M, N, true>, grid, block, 0, st, a, inv_d);
-  if (mod == MOD_NONE) {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(MOD_NONE, 1)
-      NVFP4AP_CASE(MOD_NONE, 2)
-      NVFP4AP_CASE(MOD_NONE, 3)
-      NVFP4AP_CASE(MOD_NONE, 4)
-      default: return cudaErrorInvalidValue;
-    }
-  } else if (mod == MOD_BCAST) {
-    switch (s.per_thread) {
-      NVFP4AP_CASE(MOD_BCAST, 1)
-      NVFP4AP_CASE(MOD_BCAST, 2)
-      NVFP4AP_CASE(MOD_BCAST, 3)
-      NVFP4AP_CASE(MOD_BCAST, 4)
-      default: return cudaErrorInvalidValue;
-    }
-  }
-#undef NVFP4AP_CASE
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_ln_rows(const LnArgs& a, bool nvfp4, int mod, RowShape s, cudaStream_t st) {

@@ -83,18 +83,11 @@ __host__ __device__ constexpr int rows_max_tpr(int nv) {
 // Measured on GB300 for the NVFP4 layer norm at 5070 rows: 15% faster than
 // the uncapped kernel at dim 3072, 13% at 4096 -- the NVFP4 encode is a chain
 // of dependent steps, and more resident warps hide its latency.
-//
-// TILE4 (NVFP4 only, blockDim.y == 4): the CTA owns rows t0 + r32 + 32*ry of
-// one 128-row tile (t0 = 128 * (blockIdx.x / 32), r32 = blockIdx.x % 32), so
-// the four rows' scale bytes of every 4-column group form one contiguous
-// 16-byte chunk of the 128x4 layout; they are gathered in shared memory and
-// written with one 16-byte store per chunk (padding rows and columns as 0).
-template <int KIND, int MOD, int NV, bool TILE4 = false, int FULLMB = 0>
+template <int KIND, int MOD, int NV, int FULLMB = 0>
 __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_rows_kernel(const LnArgs a, const float inv_d) {
   constexpr bool kPerToken = (MOD == MOD_PTOK || MOD == MOD_TABLE);
   constexpr bool kScales = (KIND == KIND_NVFP4 || KIND == KIND_NV2L);  // writes codes and scales
   __shared__ float2 red[16][16];  // [row group][warp of the row]
-  __shared__ uint32_t sft[TILE4 ? 4 : 1][TILE4 ? 1024 : 1];  // [row group][4-column group]: 4 scale bytes
 
   const int tpr = blockDim.x;
   const int t = threadIdx.x, ry = FULLMB ? 0 : threadIdx.y;  // FULL: one row per CTA
@@ -102,8 +95,7 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
   const int64_t D = a.dim;
   const int nch = (int)(D >> 3);
   constexpr bool FULL = FULLMB > 0;
-  const int64_t row = TILE4 ? (int64_t)(blockIdx.x >> 5) * 128 + (blockIdx.x & 31) + 32 * ry
-                            : (int64_t)blockIdx.x * blockDim.y + ry;
+  const int64_t row = (int64_t)blockIdx.x * blockDim.y + ry;
   const bool active = row < a.rows;
   const int64_t rbase = active ? row * D : 0;
   pdl_enter();
@@ -181,7 +173,7 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
       s.y += u.y;
     }
   }
-  if (!active && !TILE4) {
+  if (!active) {
     if constexpr (kScales) {
       // rows past the end inside the last 128-row tile: zero scale bytes
       const int nblk = nch >> 1, padc = (nblk + 3) & ~3, ct = padc >> 2;
@@ -345,7 +337,9 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
         scl = e4m3_to_f32(sbyte[k]) * ts;
       } else {
         // e4m3(amax/6) via the fp32 constant 1/6 gives the byte of the exact
-        // quotient (see ln_nvfp4.cu).
+        // quotient: amax has 8 significant bits, so amax/6 is either exact or
+        // far from every e4m3 rounding boundary (checked on the CPU for every
+        // bf16 amax).
         sbyte[k] = f2_to_e4m3x2(make_float2(amax[k] * (1.0f / 6.0f), 0.f)) & 0xFFu;
         scl = e4m3_to_f32(sbyte[k]);
       }
@@ -375,53 +369,18 @@ __global__ void __launch_bounds__(FULLMB ? 128 : 512, FULLMB ? FULLMB : 1) ln_ro
       }
       codes[k] = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
     }
-    if constexpr (TILE4) {
-      // gather this row's scale bytes: lane j (even) holds column j/2; the four
-      // columns of group g sit in lanes 8g, 8g+2, 8g+4, 8g+6 of the warp
 #pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int j = t + k * tpr;
-        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 2);
-        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 4);
-        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sbyte[k], 6);
-        if (FULL || j < nch) {
-          if (active) st_stream_b32(prow + (int64_t)j * 4, codes[k]);
-          if ((j & 7) == 0) {
-            // columns 4g..4g+3 (g = j/8); those at or past nblk are padding (0)
-            const int c0 = j >> 1;
-            uint32_t w = 0u;
-            if (active) {
-              w = sbyte[k];
-              if (c0 + 1 < nblk) w |= b1 << 8;
-              if (c0 + 2 < nblk) w |= b2 << 16;
-              if (c0 + 3 < nblk) w |= b3 << 24;
-            }
-            sft[ry][j >> 3] = w;
-          }
+    for (int k = 0; k < NV; ++k) {
+      const int j = t + k * tpr;
+      if (FULL || j < nch) {
+        st_stream_b32(prow + (int64_t)j * 4, codes[k]);
+        if ((j & 1) == 0) {
+          const int c = j >> 1;
+          st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte[k]);
         }
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int j = t + k * tpr;
-        if (FULL || j < nch) {
-          st_stream_b32(prow + (int64_t)j * 4, codes[k]);
-          if ((j & 1) == 0) {
-            const int c = j >> 1;
-            st_b8(sfrow + (c >> 2) * 512 + (c & 3), sbyte[k]);
-          }
-        }
-      }
-      for (int c = nblk + t; c < padc; c += tpr) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
     }
-    if constexpr (TILE4) {
-      // the CTA's four rows are done: one 16-byte chunk per 4-column group
-      __syncthreads();
-      uint8_t* base = reinterpret_cast<uint8_t*>(a.sf) + (int64_t)(blockIdx.x >> 5) * ct * 512 +
-                      (int)((blockIdx.x & 31) << 4);
-      for (int g = ry * tpr + t; g < ct; g += 4 * tpr)
-        st_stream_v4(base + (int64_t)g * 512, make_uint4(sft[0][g], sft[1][g], sft[2][g], sft[3][g]));
-    }
+    for (int c = nblk + t; c < padc; c += tpr) st_b8(sfrow + (c >> 2) * 512 + (c & 3), 0u);
   }
 }
 

@@ -266,8 +266,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         const int j = t + k * tpr;
-        // e4m3(amax/6) via the fp32 constant 1/6 and the head/tail reciprocal
-        // quotient: see ln_rows.cu, ln_nvfp4.cu
+        // e4m3(amax/6) via the fp32 constant 1/6 (the byte of the exact
+        // quotient, as in ln_rows.cuh) and the head/tail reciprocal quotient
         const uint32_t sbyte = f2_to_e4m3x2(make_float2(amax[k] * (1.0f / 6.0f), 0.f)) & 0xFFu;
         const float scl = e4m3_to_f32(sbyte);
         const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
@@ -395,9 +395,7 @@ bool ln_tma_supported(bool nvfp4, int mod, RowShape s) {
 cudaError_t launch_ln_tma(const LnArgs& a, bool nvfp4, int mod, RowShape s, int sms, int forced_stages,
                           int ctas_per_sm, long long wait_limit, cudaStream_t st) {
   // rows that exactly fill the threads' chunks take the FULL instance
-  // (NVFP4AP_FULL=0 turns it off)
-  const char* full_env = env_get("NVFP4AP_FULL");
-  const bool full = !(full_env && full_env[0] == '0') && (int64_t)s.tpr * s.per_thread * 8 == a.dim;
+  const bool full = (int64_t)s.tpr * s.per_thread * 8 == a.dim;
   TmaKernel k = pick(nvfp4, mod, s.per_thread, full);
   if (!k || s.tpr > 256 || s.rpc != 1) return cudaErrorInvalidValue;
   const TmaPlan p = tma_plan(k, mod, a.dim, s.tpr, forced_stages);

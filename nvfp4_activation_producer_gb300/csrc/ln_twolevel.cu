@@ -32,9 +32,9 @@ cudaError_t launch_full(const LnArgs& a, RowShape s, bool pdl, cudaStream_t st) 
     return cudaGetLastError();
   };
   switch (s.per_thread) {
-    case 2: return go(ln_rows_kernel<KIND, MOD, 2, false, kFullMinBlocks>);
-    case 3: return go(ln_rows_kernel<KIND, MOD, 3, false, kFullMinBlocks>);
-    case 4: return go(ln_rows_kernel<KIND, MOD, 4, false, kFullMinBlocks>);
+    case 2: return go(ln_rows_kernel<KIND, MOD, 2, kFullMinBlocks>);
+    case 3: return go(ln_rows_kernel<KIND, MOD, 3, kFullMinBlocks>);
+    case 4: return go(ln_rows_kernel<KIND, MOD, 4, kFullMinBlocks>);
     default: return cudaErrorInvalidValue;
   }
 }

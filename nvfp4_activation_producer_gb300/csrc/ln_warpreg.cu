@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kWarpRegThreads, 1) warp_regs_kernel(const LnA
 }
 
 template <int KIND, int MOD, int BPL>
-cudaError_t launch_bpl(const LnArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_bpl(const LnArgs& a, int sms, int ctas_per_sm, cudaStream_t st) {
   auto k = warp_regs_kernel<KIND, MOD, BPL>;
   const int64_t smem64 = blk_tab_float4s(MOD, a.dim / 16, a.nseg) * (int64_t)sizeof(float4);
   if (smem64 > kBlkMaxSmem || !flat_smem_limit((const void*)k)) return cudaErrorInvalidValue;
@@ -131,6 +131,7 @@ cudaError_t launch_bpl(const LnArgs& a, int sms, cudaStream_t st) {
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kWarpRegThreads, smem) != cudaSuccess || occ < 1)
     return cudaErrorInvalidConfiguration;
+  if (ctas_per_sm > 0 && ctas_per_sm < occ) occ = ctas_per_sm;
   int64_t grid = (int64_t)sms * occ;
   const int64_t need = (a.rows + kWarpRegThreads / 32 - 1) / (kWarpRegThreads / 32);
   if (grid > need) grid = need;
@@ -139,13 +140,13 @@ cudaError_t launch_bpl(const LnArgs& a, int sms, cudaStream_t st) {
 }
 
 template <int KIND, int MOD>
-cudaError_t launch_kind_mod(const LnArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_kind_mod(const LnArgs& a, int sms, int ctas_per_sm, cudaStream_t st) {
   const int bpl = warp_regs_bpl(a.dim);
   switch (bpl) {
-    case 6: return launch_bpl<KIND, MOD, 6>(a, sms, st);
-    case 8: return launch_bpl<KIND, MOD, 8>(a, sms, st);
-    case 11: return launch_bpl<KIND, MOD, 11>(a, sms, st);
-    case 12: return launch_bpl<KIND, MOD, 12>(a, sms, st);
+    case 6: return launch_bpl<KIND, MOD, 6>(a, sms, ctas_per_sm, st);
+    case 8: return launch_bpl<KIND, MOD, 8>(a, sms, ctas_per_sm, st);
+    case 11: return launch_bpl<KIND, MOD, 11>(a, sms, ctas_per_sm, st);
+    case 12: return launch_bpl<KIND, MOD, 12>(a, sms, ctas_per_sm, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -168,21 +169,17 @@ bool warp_path_rows(int64_t rows, int64_t dim, int sms, bool regs) {
 // this translation unit's copy of the segment fault word (ln_blk.cuh), read and cleared
 cudaError_t take_warpreg_seg_fault(unsigned int* fault) { return take_blk_word(fault); }
 
-cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, cudaStream_t st) {
+cudaError_t launch_warp_regs(const LnArgs& a, bool amax, int mod, int sms, int ctas_per_sm, cudaStream_t st) {
   if (amax) {
     switch (mod) {
-      case MOD_NONE: return launch_kind_mod<BK_AMAX, MOD_NONE>(a, sms, st);
-      case MOD_BCAST: return launch_kind_mod<BK_AMAX, MOD_BCAST>(a, sms, st);
-      case MOD_SEG: return launch_kind_mod<BK_AMAX, MOD_SEG>(a, sms, st);
+      case MOD_NONE: return launch_kind_mod<BK_AMAX, MOD_NONE>(a, sms, ctas_per_sm, st);
+      case MOD_BCAST: return launch_kind_mod<BK_AMAX, MOD_BCAST>(a, sms, ctas_per_sm, st);
+      case MOD_SEG: return launch_kind_mod<BK_AMAX, MOD_SEG>(a, sms, ctas_per_sm, st);
       default: return cudaErrorInvalidValue;
     }
   }
-  switch (mod) {
-    case MOD_NONE: return launch_kind_mod<BK_FP8, MOD_NONE>(a, sms, st);
-    case MOD_BCAST: return launch_kind_mod<BK_FP8, MOD_BCAST>(a, sms, st);
-    case MOD_SEG: return launch_kind_mod<BK_FP8, MOD_SEG>(a, sms, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (mod != MOD_SEG) return cudaErrorInvalidValue;
+  return launch_kind_mod<BK_FP8, MOD_SEG>(a, sms, ctas_per_sm, st);
 }
 
 }  // namespace nvfp4ap

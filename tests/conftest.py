@@ -49,30 +49,20 @@ def ap(dev):
     return ap
 
 
-@pytest.fixture(params=["auto", "rows", "rows_flat", "tile4", "tma", "ring", "legacy", "blk"])
+@pytest.fixture(params=["auto", "rows", "rows_c1", "tma", "blk", "rowblk"])
 def path(request, monkeypatch):
-    """Run a LayerNorm-producer test on each kernel family: the default choice
-    (TMA pipeline for the table form, register row kernels otherwise), the
-    register row kernels for every form (NVFP4AP_KERNEL=3) with and without
-    the persistent broadcast variant and the register-capped NVFP4 instance
-    (NVFP4AP_PERSIST=-1, NVFP4AP_FULL=0), the NVFP4
-    four-row-tile variant (NVFP4AP_TILE4=1), the TMA pipeline
-    for every form (4), the warp-per-row TMA ring (1), the first register
-    kernels (2) and the block-per-lane persistent kernels (5)."""
-    kernel = {"auto": None, "rows": "3", "rows_flat": "3", "tile4": "3", "tma": "4", "ring": "1",
-              "legacy": "2", "blk": "5"}[request.param]
+    """Run a LayerNorm-producer test on each kernel family through the one
+    selection setting the library reads (NVFP4AP_KERNEL=F[:C]): the default
+    choice, the register row kernels for every form (3; the persistent
+    broadcast kernel for the broadcast sources, the register-capped NVFP4
+    instance where a row fills the CTA exactly), the same with one persistent
+    CTA per SM (3:1, so every CTA walks many rows), the TMA pipeline wherever
+    it applies (4), the block-per-lane persistent kernels (5) and the
+    one-row-per-CTA block-per-lane kernels (8); a family that does not take a
+    form or shape falls back to the register row kernels."""
+    kernel = {"auto": None, "rows": "3", "rows_c1": "3:1", "tma": "4", "blk": "5", "rowblk": "8"}[request.param]
     if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
         monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
-    if request.param == "rows_flat":
-        monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
-        monkeypatch.setenv("NVFP4AP_FULL", "0")
-    else:
-        monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
-        monkeypatch.delenv("NVFP4AP_FULL", raising=False)
-    if request.param == "tile4":
-        monkeypatch.setenv("NVFP4AP_TILE4", "1")
-    else:
-        monkeypatch.delenv("NVFP4AP_TILE4", raising=False)
     return request.param

@@ -24,8 +24,7 @@ from parity import check_fp8, check_nvfp4
 
 pytestmark = pytest.mark.gpu
 
-KNOBS = ("NVFP4AP_KERNEL", "NVFP4AP_PERSIST", "NVFP4AP_FULL", "NVFP4AP_TILE4", "NVFP4AP_TMA_CTAS",
-         "NVFP4AP_TMA_STAGES", "NVFP4AP_BLK_BPT", "NVFP4AP_BLK_GRID", "NVFP4AP_BLK_CTAS", "NVFP4AP_RB_BPT")
+KNOBS = ("NVFP4AP_KERNEL",)
 
 
 @pytest.fixture
@@ -88,7 +87,7 @@ def test_c3_table_kernel_one_cta_per_sm(ap, dev, default):
     # the staged (TMA) kernel of the table form, full-row instance at dim
     # 3072, one persistent CTA per SM: every CTA walks its rows through the
     # stage ring many times over
-    default.setenv("NVFP4AP_TMA_CTAS", "1")
+    default.setenv("NVFP4AP_KERNEL", "4:1")
     _table(ap, dev, "C3 one CTA per SM")
 
 

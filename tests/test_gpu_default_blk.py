@@ -37,9 +37,7 @@ def _act(w):
 
 @pytest.fixture
 def auto(monkeypatch):
-    for k in ("NVFP4AP_KERNEL", "NVFP4AP_BLK_BPT", "NVFP4AP_BLK_GRID", "NVFP4AP_BLK_CTAS", "NVFP4AP_PERSIST",
-              "NVFP4AP_FULL", "NVFP4AP_TILE4"):
-        monkeypatch.delenv(k, raising=False)
+    monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     return monkeypatch
 
 

@@ -174,55 +174,35 @@ def test_side_stream_and_graph_capture(ap, dev, path):
     assert np.array_equal(_codes(out2), ref)
 
 
-@pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
-def test_ring_wraps_many_rows_per_warp(ap, dev, op, monkeypatch):
-    monkeypatch.setenv("NVFP4AP_KERNEL", "1")
-    # one warp with one or two stages per CTA and one CTA per SM: every warp
-    # walks many rows, so each stage's mbarrier goes through many phases
-    rows, dim = 6000, 256
-    for warps, stages in ((1, 1), (2, 2), (3, 4)):
-        monkeypatch.setenv("NVFP4AP_RING_WARPS", str(warps))
-        monkeypatch.setenv("NVFP4AP_RING_STAGES", str(stages))
-        monkeypatch.setenv("NVFP4AP_RING_CTAS", "1")
-        if op == "table":
-            w = synth.fp8_table(rows, dim, seed=warps)
-            d = _d(w, dev)
-            out = ap.ada_layer_norm_quant_fp8_ptok_table_bf16(d["x"], d["temb"], d["table"], d["act_scale"], 0, 1)
-            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_TABLE,
-                                      temb=synth.u16(w.inputs["temb"]), table=w.inputs["table"].numpy(),
-                                      shift_idx=0, scale_idx=1)
-        elif op == "ptok":
-            w = synth.fp8_ptok(rows, dim, seed=warps)
-            d = _d(w, dev)
-            out = ap.ada_layer_norm_quant_fp8_ptok_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
-            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
-            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_PTOK, scale=u["scale"], shift=u["shift"])
-        elif op == "bcast":
-            w = synth.fp8_broadcast(rows, dim, seed=warps)
-            d = _d(w, dev)
-            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
-            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
-            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
-        else:
-            w = synth.fp8_ln(rows, dim, seed=warps)
-            d = _d(w, dev)
-            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
-            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
-        check_fp8(_codes(out), ref, _act(w))
+@pytest.mark.parametrize("rows,dim", [(40000, 256), (6000, 3072)])
+def test_noalloc_ring_wraps_many_rows_per_warp(ap, dev, rows, dim):
+    # the allocation-free producer's warp-per-row ring kernel: with more rows
+    # than warps in its persistent grid every warp walks several rows, so each
+    # stage's mbarrier goes through many phases and refills
+    import ctypes
+    w = synth.fp8_broadcast(rows, dim, seed=rows % 97)
+    d = _d(w, dev)
+    out = torch.empty((rows, dim), dtype=torch.uint8, device=dev)
+    rc = ap._load().ada_layer_norm_quant_fp8_bf16_noalloc(
+        d["x"].data_ptr(), d["scale"].data_ptr(), d["shift"].data_ptr(), d["act_scale"].data_ptr(),
+        ctypes.c_float(1e-5), out.data_ptr(), rows, dim, torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
+    ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
+    check_fp8(out.cpu().numpy(), ref, _act(w))
+    words = ap.noalloc_progress()
+    assert sum(words) == rows and len(words) * 8 < rows  # every warp had several rows
     ap.take_device_fault()  # no bounded wait ran out
 
 
-@pytest.mark.parametrize("rows,dim,bpt", [(131, 2048, 0), (3001, 4096, 0), (257, 6144, 0), (129, 4096, 4),
-                                          (77, 6144, 4), (1, 3072, 0)])
-def test_rowblk_layer_norm_shapes(ap, dev, rows, dim, bpt, monkeypatch):
+@pytest.mark.parametrize("rows,dim", [(131, 2048), (3001, 4096), (257, 6144), (129, 8192), (77, 4608), (1, 3072)])
+def test_rowblk_layer_norm_shapes(ap, dev, rows, dim, monkeypatch):
     # the FP8 layer norm on the one-row-per-CTA block-per-lane kernel (its
-    # default where a row is exactly 64-128 threads x 2-4 blocks)
+    # default where a row is exactly 64-128 threads x 2-4 blocks): 3 blocks per
+    # lane at dims 3072, 4608, 6144, 2 at 2048 and 4096, 4 at 8192
     monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
-    if bpt:
-        monkeypatch.setenv("NVFP4AP_RB_BPT", str(bpt))
-    else:
-        monkeypatch.delenv("NVFP4AP_RB_BPT", raising=False)
-    w = synth.fp8_ln(rows, dim, seed=rows + dim + bpt)
+    w = synth.fp8_ln(rows, dim, seed=rows + dim)
     d = _d(w, dev)
     out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
     ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
@@ -261,12 +241,10 @@ def test_rowblk_broadcast_sources_when_forced(ap, dev, op, monkeypatch):
 
 @pytest.mark.parametrize("op", ["ln", "bcast"])
 def test_blk_many_rows_per_group(ap, dev, op, monkeypatch):
-    # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows
-    # (prefetch buffer, parity slots); 17 and 192 blocks per row
-    monkeypatch.setenv("NVFP4AP_KERNEL", "5")
-    rows = 3001
-    for ctas, dim in ((1, 272), (3, 3072)):
-        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
+    # block-per-lane kernels with one CTA per SM: every row group walks many
+    # rows (prefetch buffer, parity slots); 17 and 192 blocks per row
+    monkeypatch.setenv("NVFP4AP_KERNEL", "5:1")  # one CTA per SM: ~16 rows per row group
+    for ctas, (rows, dim) in enumerate(((40000, 272), (20000, 3072))):
         if op == "bcast":
             w = synth.fp8_broadcast(rows, dim, seed=ctas)
             d = _d(w, dev)
@@ -283,14 +261,12 @@ def test_blk_many_rows_per_group(ap, dev, op, monkeypatch):
 
 @pytest.mark.parametrize("op", ["ln", "bcast", "ptok", "table"])
 def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
-    # one CTA per SM and 1, 2 or 5 stages: each CTA walks ~40 rows, so every
-    # stage's mbarrier goes through many phases and refills
-    monkeypatch.setenv("NVFP4AP_KERNEL", "4")
+    # one and two CTAs per SM: each CTA walks ~20-40 rows, so every stage's
+    # mbarrier goes through many phases and refills
     rows, dim = 6000, 1024
-    for stages in (1, 2, 5):
-        monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))
-        monkeypatch.setenv("NVFP4AP_TMA_CTAS", "1")
-        seed = 40 + stages
+    for ctas in (1, 2):
+        monkeypatch.setenv("NVFP4AP_KERNEL", f"4:{ctas}")
+        seed = 40 + ctas
         if op == "table":
             w = synth.fp8_table(rows, dim, seed=seed, shift_idx=4, scale_idx=2)
             d = _d(w, dev)
@@ -317,26 +293,3 @@ def test_tma_pipeline_many_rows_per_cta(ap, dev, op, monkeypatch):
             ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
         check_fp8(_codes(out), ref, _act(w))
     ap.take_device_fault()
-
-
-@pytest.mark.parametrize("regs", ["1", "0"])
-@pytest.mark.parametrize("op", ["ln", "bcast"])
-def test_warp_rows_when_forced(ap, dev, op, regs, monkeypatch):
-    # the warp-per-row kernels for the layer norm and broadcast forms
-    # (NVFP4AP_KERNEL=6): rows well above and below one per warp of the grid;
-    # the row held in registers (default) or read twice (NVFP4AP_WARPREG=0)
-    monkeypatch.setenv("NVFP4AP_KERNEL", "6")
-    monkeypatch.setenv("NVFP4AP_WARPREG", regs)
-    for rows, dim in ((3001, 3072), (517, 1536), (40000, 272)):
-        if op == "bcast":
-            w = synth.fp8_broadcast(rows, dim, seed=rows)
-            d = _d(w, dev)
-            out = ap.ada_layer_norm_quant_fp8_bf16(d["x"], d["scale"], d["shift"], d["act_scale"])
-            u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
-            ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
-        else:
-            w = synth.fp8_ln(rows, dim, seed=rows)
-            d = _d(w, dev)
-            out = ap.layer_norm_no_affine_quant_fp8_static_bf16(d["x"], d["act_scale"])
-            ref = oracle.ln_quant_fp8(synth.u16(w.inputs["x"]), _act(w), oracle.MOD_NONE)
-        check_fp8(_codes(out), ref, _act(w), f"{op} {rows}x{dim}")

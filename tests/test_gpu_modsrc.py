@@ -97,24 +97,16 @@ def _exact_codes(rng, n):
 
 
 # Bit-for-bit reductions compare two calls that must run the same kernel: the
-# default choice, the flat register kernels (NVFP4AP_PERSIST=-1) and the
-# block-per-lane kernels (NVFP4AP_KERNEL=5).  The
-# warp-ring, TMA, four-row-tile and first-kernel families have no modfp8 / AWQ
-# variant, so there the two calls run different kernels whose fp32 rounding
-# order differs (each is compared with the oracle above).
-@pytest.fixture(params=["auto", "rows_flat", "blk"])
+# default choice, the register row kernels (NVFP4AP_KERNEL=3) and the
+# block-per-lane kernels (NVFP4AP_KERNEL=5).  The TMA family has no modfp8 /
+# AWQ variant, so there the two calls run different kernels whose fp32
+# rounding order differs (each is compared with the oracle above).
+@pytest.fixture(params=["auto", "rows", "blk"])
 def same_kernel(request, monkeypatch):
-    if request.param == "blk":
-        monkeypatch.setenv("NVFP4AP_KERNEL", "5")
-    else:
+    if request.param == "auto":
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
-    monkeypatch.delenv("NVFP4AP_TILE4", raising=False)
-    if request.param == "rows_flat":
-        monkeypatch.setenv("NVFP4AP_PERSIST", "-1")
-        monkeypatch.setenv("NVFP4AP_FULL", "0")
     else:
-        monkeypatch.delenv("NVFP4AP_PERSIST", raising=False)
-        monkeypatch.delenv("NVFP4AP_FULL", raising=False)
+        monkeypatch.setenv("NVFP4AP_KERNEL", "3" if request.param == "rows" else "5")
     return request.param
 
 

@@ -132,47 +132,26 @@ def test_misaligned_input_takes_the_element_wise_kernel(ap, dev):
 
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
-def test_ring_wraps_many_rows_per_warp(ap, dev, kind, monkeypatch):
-    monkeypatch.setenv("NVFP4AP_KERNEL", "1")
-    rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
-    for warps, stages in ((1, 1), (2, 3)):
-        monkeypatch.setenv("NVFP4AP_RING_WARPS", str(warps))
-        monkeypatch.setenv("NVFP4AP_RING_STAGES", str(stages))
-        monkeypatch.setenv("NVFP4AP_RING_CTAS", "1")
-        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=warps)
-        gp, gs = _run(ap, kind, w, dev)
-        op, os_, v = _oracle(w, kind)
-        check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
-    ap.take_device_fault()
-
-
-@pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_tma_pipeline_many_rows_per_cta(ap, dev, kind, monkeypatch):
-    monkeypatch.setenv("NVFP4AP_KERNEL", "4")
     rows, dim = 3000, 272   # 17 blocks per row: column padding; 3000 rows: row padding
-    for stages in (1, 3):
-        monkeypatch.setenv("NVFP4AP_TMA_STAGES", str(stages))
-        monkeypatch.setenv("NVFP4AP_TMA_CTAS", "1")
-        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=stages)
+    for ctas in (1, 2):  # persistent CTAs per SM: each walks many rows through its stages
+        monkeypatch.setenv("NVFP4AP_KERNEL", f"4:{ctas}")
+        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=ctas)
         gp, gs = _run(ap, kind, w, dev)
         op, os_, v = _oracle(w, kind)
         check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
     ap.take_device_fault()
 
 
-@pytest.mark.parametrize("rows,dim,bpt", [(131, 2048, 0), (3001, 4096, 0), (257, 6144, 0), (129, 4096, 4),
-                                          (77, 6144, 4), (130, 3072, 0)])
+@pytest.mark.parametrize("rows,dim", [(131, 2048), (3001, 4096), (257, 6144), (129, 8192), (77, 4608), (130, 3072)])
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
-def test_rowblk_shapes(ap, dev, kind, rows, dim, bpt, monkeypatch):
+def test_rowblk_shapes(ap, dev, kind, rows, dim, monkeypatch):
     # the one-row-per-CTA block-per-lane kernel (the default where a row is
-    # exactly 64-128 threads x 2-4 blocks): 2, 3 and 4 blocks per lane, 64-128
-    # threads per row, ragged row counts (padding rows of the last scale tile)
+    # exactly 64-128 threads x 2-4 blocks): 2 (dims 2048, 4096), 3 (3072, 4608,
+    # 6144) and 4 (8192) blocks per lane, 64-128 threads per row, ragged row
+    # counts (padding rows of the last scale tile)
     monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
-    if bpt:
-        monkeypatch.setenv("NVFP4AP_RB_BPT", str(bpt))
-    else:
-        monkeypatch.delenv("NVFP4AP_RB_BPT", raising=False)
-    w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=rows + dim + bpt)
+    w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=rows + dim)
     gp, gs = _run(ap, kind, w, dev)
     op, os_, v = _oracle(w, kind)
     check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
@@ -180,16 +159,16 @@ def test_rowblk_shapes(ap, dev, kind, rows, dim, bpt, monkeypatch):
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])
 def test_blk_many_rows_per_group(ap, dev, kind, monkeypatch):
-    # block-per-lane kernels on 1 and 3 CTAs: every row group walks many rows
-    # (prefetch buffer, parity slots); 17 and 192 blocks per row (one idle lane
-    # range and an exact fit), 3000 rows (row padding of the last scale tile)
-    monkeypatch.setenv("NVFP4AP_KERNEL", "5")
-    for ctas, dim in ((1, 272), (3, 3072)):
-        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
-        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(3000, dim, seed=ctas)
+    # block-per-lane kernels with one CTA per SM: every row group walks many
+    # rows (prefetch buffer, parity slots); 17 and 192 blocks per row (one idle
+    # lane range and an exact fit); 20000 rows (row padding of the last scale
+    # tile)
+    monkeypatch.setenv("NVFP4AP_KERNEL", "5:1")  # one CTA per SM: ~16 rows per row group
+    for rows, dim in ((40000, 272), (20000, 3072)):
+        w = (synth.nvfp4_broadcast if kind == "bcast" else synth.nvfp4_ln)(rows, dim, seed=dim)
         gp, gs = _run(ap, kind, w, dev)
         op, os_, v = _oracle(w, kind)
-        check_nvfp4(gp, gs, op, os_, 3000, dim, v_orc=v)
+        check_nvfp4(gp, gs, op, os_, rows, dim, v_orc=v)
 
 
 @pytest.mark.parametrize("kind", ["ln", "bcast"])

@@ -14,10 +14,9 @@ graph capture of the three operations.  Every case runs on the default
 kernels (block-per-lane for the two-level forms, register row kernels for the
 single-level segmented forms), on the register row kernels
 (NVFP4AP_KERNEL=3), on the block-per-lane kernels (NVFP4AP_KERNEL=5) and with
-the warp-per-row kernels forced at every size (NVFP4AP_2L_AMAX=1 for the
-two-level maximum pass, NVFP4AP_SEG_WARP=1 for the FP8 segmented producer),
-once with the row held in registers (the default where a lane's share fits)
-and once read twice (NVFP4AP_WARPREG=0); the two give identical bytes.
+the warp-per-row kernels forced at every size (NVFP4AP_KERNEL=6: the two-level
+maximum pass and the FP8 segmented producer; the row held in registers where a
+lane's share fits, dims up to 6144, else read twice, dim 8192).
 """
 import numpy as np
 import pytest
@@ -29,29 +28,17 @@ from parity import check_fp8, check_nvfp4
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (130, 4096), (5, 32768), (257, 1536)]
+SHAPES = [(1, 16), (3, 48), (127, 64), (129, 80), (300, 3072), (64, 5376), (130, 4096), (5, 32768), (257, 1536),
+          (41, 8192)]
 
 
-@pytest.fixture(autouse=True, params=["auto", "rows", "blk", "warp", "warp2"])
+@pytest.fixture(autouse=True, params=["auto", "rows", "blk", "warp"])
 def family(request, monkeypatch):
-    if request.param in ("auto", "warp", "warp2"):
+    kernel = {"auto": None, "rows": "3", "blk": "5", "warp": "6"}[request.param]
+    if kernel is None:
         monkeypatch.delenv("NVFP4AP_KERNEL", raising=False)
     else:
-        monkeypatch.setenv("NVFP4AP_KERNEL", "3" if request.param == "rows" else "5")
-    if request.param in ("warp", "warp2"):
-        # the warp-per-row kernels at every size: the two-level maximum pass and
-        # the FP8 segmented producer; "warp" holds the row in registers where a
-        # lane's share fits, "warp2" reads it twice (NVFP4AP_WARPREG=0)
-        monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")
-        monkeypatch.setenv("NVFP4AP_SEG_WARP", "1")
-    else:
-        monkeypatch.delenv("NVFP4AP_2L_AMAX", raising=False)
-        monkeypatch.delenv("NVFP4AP_SEG_WARP", raising=False)
-    if request.param == "warp2":
-        monkeypatch.setenv("NVFP4AP_WARPREG", "0")
-    else:
-        monkeypatch.delenv("NVFP4AP_WARPREG", raising=False)
-    monkeypatch.delenv("NVFP4AP_BLK_GRID", raising=False)
+        monkeypatch.setenv("NVFP4AP_KERNEL", kernel)
     return request.param
 
 
@@ -217,14 +204,13 @@ def test_two_level_workspace_reuse_and_graph(ap, dev):
 
 @pytest.mark.parametrize("kind", ["none", "bcast", "seg"])
 def test_two_level_many_rows_per_group(ap, dev, family, kind, monkeypatch):
-    # block-per-lane kernels on 1 and 3 CTAs: each row group walks many rows and
-    # the maximum pass reduces them in one CTA
-    if family in ("rows", "warp"):
-        pytest.skip("grid limit of the block-per-lane row-group kernels")
-    for ctas, dim in ((1, 272), (3, 3072)):
-        monkeypatch.setenv("NVFP4AP_BLK_GRID", str(ctas))
-        rows = 3000
-        w = synth.segmented(rows, dim, seed=ctas + 7)
+    # block-per-lane kernels with one CTA per SM: each row group walks ~16 rows
+    # and the maximum pass reduces them in one atomic per CTA
+    if family != "blk":
+        pytest.skip("runs once")
+    monkeypatch.setenv("NVFP4AP_KERNEL", "5:1")
+    for dim, rows in ((272, 40000), (3072, 20000)):
+        w = synth.segmented(rows, dim, seed=dim + 7)
         d = {k: v.to(dev) for k, v in w.inputs.items()}
         x = _u(w.inputs["x"])
         if kind == "seg":
@@ -244,28 +230,7 @@ def test_two_level_many_rows_per_group(ap, dev, family, kind, monkeypatch):
         opk, osf, ots = oracle.ln_quant_nvfp4_2level(x, mk, **src)
         assert float(ts.cpu()[0]) == ots
         check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(x, mk, **src),
-                    f"two-level {kind} on {ctas} CTAs", ts=ots)
-
-
-@pytest.mark.parametrize("rows,dim", [(2001, 5376), (1500, 3072), (700, 4096), (333, 80)])
-def test_register_rows_equal_two_sweeps(ap, dev, family, rows, dim, monkeypatch):
-    # the register-resident and the two-sweep warp kernels run the same fp32
-    # operations in the same order: every output byte and the tensor scale agree
-    if family != "warp":
-        pytest.skip("runs once")
-    w = synth.segmented(rows, dim, seed=rows + dim)
-    d = {k: v.to(dev) for k, v in w.inputs.items() if isinstance(v, torch.Tensor)}
-    res = []
-    for wr in ("1", "0"):
-        monkeypatch.setenv("NVFP4AP_WARPREG", wr)
-        q = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"],
-                                                 d["act_scale"])
-        pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"],
-                                                                   d["seg_shift"])
-        res.append((q.view(torch.uint8).clone(), pk.clone(), sf.clone(), ts.clone()))
-    for a, b in zip(*res):
-        assert torch.equal(a, b)
-    ap.take_device_fault()
+                    f"two-level {kind} {rows}x{dim}, one CTA per SM", ts=ots)
 
 
 def test_register_warp_path_from_the_element_threshold(ap, dev, family, monkeypatch):
@@ -284,8 +249,7 @@ def test_register_warp_path_from_the_element_threshold(ap, dev, family, monkeypa
     q = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"], d["act_scale"])
     pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"])
     default = (q.view(torch.uint8).clone(), pk.clone(), sf.clone(), ts.clone())
-    monkeypatch.setenv("NVFP4AP_SEG_WARP", "1")
-    monkeypatch.setenv("NVFP4AP_2L_AMAX", "1")
+    monkeypatch.setenv("NVFP4AP_KERNEL", "6")
     q = ap.ada_layer_norm_quant_fp8_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"], d["act_scale"])
     pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], d["seg_idx"], d["seg_scale"], d["seg_shift"])
     for a, b in zip(default, (q.view(torch.uint8), pk, sf, ts)):
