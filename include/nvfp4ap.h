@@ -86,9 +86,10 @@ enum nvfp4ap_status {
 #define NVFP4AP_MAX_DIM 32768
 
 /* Bytes of the caller-owned device workspace of the two-level LayerNorm
- * NVFP4 producers for `rows` rows: the maximum word, padding to 16 bytes, then
- * one 16-byte slot per row where the maximum pass keeps the row's statistics
- * for the quantising pass (16-byte aligned).  The SwiGLU producer uses the
+ * NVFP4 producers for `rows` rows: the maximum word, a grid-barrier count word
+ * (used when the whole tensor is encoded in one launch), padding to 16 bytes,
+ * then one 16-byte slot per row where the maximum pass keeps the row's
+ * statistics for the quantising pass (16-byte aligned).  The SwiGLU producer uses the
  * word only (4 bytes, 4-byte aligned). */
 #define NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows) (16 + 16 * (int64_t)(rows))
 /* The same as a function (for callers that cannot use the macro); -1 for
@@ -315,8 +316,11 @@ int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* s
  * workspace: caller-owned device memory of NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows)
  * bytes, 16-byte aligned (NVFP4AP_ERR_ALIGN), cleared and used by the call
  * (two calls on concurrent streams need two workspaces); a smaller buffer is
- * written past its end.  Three kernels on `stream`: a clear of the word, the
- * maximum pass, the quantising pass (graph-capturable). */
+ * written past its end.  Kernels on `stream`: a clear of the workspace words,
+ * then -- when every SM's share of the rows fits in its shared memory -- one
+ * cooperative launch that reads the tensor once (statistics and maximum, a
+ * grid-wide barrier, then the codes), else the maximum pass and the
+ * quantising pass (graph-capturable either way). */
 int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed, void* sf_swizzled,
                                                  float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
                                                  nvfp4ap_stream_t stream);

@@ -334,6 +334,13 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   a.row_stats = reinterpret_cast<float*>(reinterpret_cast<char*>(a.amax_ws) + 16);
   if (mod == MOD_BCAST && (!aligned(a.scale, 16) || !aligned(a.shift, 16))) return NVFP4AP_ERR_ALIGN;
   const Force f = forced();
+  // default: one cooperative launch that reads the tensor once, where its rows
+  // fit in the SMs' shared memory
+  if (f.family == FAM_AUTO) {
+    const int sms = sm_count();
+    if (ln_2level_onchip_fits(mod, a.rows, a.dim, sms))
+      return finish(launch_ln_2level_onchip(a, mod, sms, wait_limit_cycles(), st));
+  }
   if (f.family != FAM_ROWS && ln_blk_supported(BLK_2LEVEL, mod, a.dim, a.nseg) && aligned(a.x, 32)) {
     BlkShape bs{};
     const int sms = sm_count();
@@ -493,15 +500,16 @@ NVFP4AP_EXPORT int nvfp4ap_version(void) { return 100; }
 
 NVFP4AP_EXPORT int nvfp4ap_take_device_fault(void) {
   // wait words (ring and TMA kernels), then the segment-index words
-  unsigned int f = 0u, g = 0u, h = 0u, i = 0u, j = 0u, k = 0u, l = 0u;
-  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_seg_fault(&h) != cudaSuccess ||
-      take_blk_seg_fault(&i) != cudaSuccess || take_blk2l_seg_fault(&j) != cudaSuccess ||
-      take_warpreg_seg_fault(&k) != cudaSuccess || take_scalar_seg_fault(&l) != cudaSuccess) {
+  unsigned int f = 0u, g = 0u, o = 0u, h = 0u, i = 0u, j = 0u, k = 0u, l = 0u, m = 0u;
+  if (take_ring_fault(&f) != cudaSuccess || take_tma_fault(&g) != cudaSuccess || take_onchip_fault(&o) != cudaSuccess ||
+      take_seg_fault(&h) != cudaSuccess || take_blk_seg_fault(&i) != cudaSuccess ||
+      take_blk2l_seg_fault(&j) != cudaSuccess || take_warpreg_seg_fault(&k) != cudaSuccess ||
+      take_scalar_seg_fault(&l) != cudaSuccess || take_onchip_seg_fault(&m) != cudaSuccess) {
     (void)cudaGetLastError();
     return NVFP4AP_ERR_LAUNCH;
   }
-  if (f | g) return NVFP4AP_ERR_TIMEOUT;
-  return (h | i | j | k | l) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
+  if (f | g | o) return NVFP4AP_ERR_TIMEOUT;
+  return (h | i | j | k | l | m) ? NVFP4AP_ERR_FAULT : NVFP4AP_OK;
 }
 
 NVFP4AP_EXPORT int nvfp4ap_set_wait_limit(int64_t cycles) {

@@ -198,6 +198,18 @@ cudaError_t launch_ln_2level(const LnArgs& a, int mod, RowShape s, bool full, cu
 // Reads and clears the word set when a segment index was out of range.
 cudaError_t take_seg_fault(unsigned int* fault);
 
+// Two-level NVFP4 in one cooperative launch (ln_2l_onchip.cu) for tensors
+// whose rows fit in the SMs' shared memory (one CTA per SM, ceil(rows / sms)
+// rows each): the tensor is read from HBM once.  mod MOD_NONE, MOD_BCAST or
+// MOD_SEG; dim % 16 == 0; x 16-byte aligned; a.amax_ws holds the maximum word
+// and, in the next word, the grid barrier's count (both cleared by a kernel
+// launched first).  Copy waits bounded by wait_limit, the grid barrier by the
+// normal bound; on expiry the fault word is set (take_onchip_fault).
+bool ln_2level_onchip_fits(int mod, int64_t rows, int64_t dim, int sms);
+cudaError_t launch_ln_2level_onchip(const LnArgs& a, int mod, int sms, long long wait_limit, cudaStream_t st);
+cudaError_t take_onchip_fault(unsigned int* fault);
+cudaError_t take_onchip_seg_fault(unsigned int* fault);
+
 // SwiGLU work items (8-element chunks) of a (rows, dim) call fit the kernels'
 // 32-bit item index: rows * (dim / 8) < 2^32.
 bool swiglu_items_fit(int64_t rows, int64_t dim);

@@ -105,28 +105,6 @@ __device__ __forceinline__ float block_amax(const uint32_t (&vb)[8]) {
   return fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
 }
 
-// e2m1 codes of v / scl for the block's 16 values, in two words (element 0 in
-// the lowest nibble).  The quotient is v * (r_hi + r_lo) with r_hi ~ 1/scl
-// refined by one Newton step (r_lo = r_hi * (1 - scl * r_hi)): exact at every
-// e2m1 midpoint and otherwise on the same side of each midpoint as v/scl.
-// scl = 0 gives r = 0 and signed-zero codes.  `pre` (a power of two) scales
-// the values and the divisor alike (exact).
-__device__ __forceinline__ void block_codes(const uint32_t (&vb)[8], float scl, float pre, uint32_t& c0,
-                                            uint32_t& c1) {
-  const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
-  const float rl = rh * fmaf(-scl, rh, 1.0f);
-  const float2 rh2 = splat2(rh), rl2 = splat2(rl), pre2 = splat2(pre);
-  float2 q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float2 v = bf16x2_to_f2(vb[i]);
-    if (pre != 1.0f) v = mul2(v, pre2);
-    q[i] = fma2(v, rh2, mul2(v, rl2));
-  }
-  c0 = f8_to_e2m1x8(q[0], q[1], q[2], q[3]);
-  c1 = f8_to_e2m1x8(q[4], q[5], q[6], q[7]);
-}
-
 // fp32 G/H of the 8 columns [8 c8, 8 c8 + 8) into the chunk-major table `tab`
 // (FP8: times 1/act_scale, AWQ also times inv_s)
 template <int KIND, int MOD>
@@ -324,27 +302,20 @@ __global__ void __launch_bounds__(kBlkThreads, 1) ln_blk_kernel(const LnArgs a, 
           run = fmaxf(run, amax);
         } else {
           uint32_t sbyte, c0, c1;
-          float scl, pre = 1.0f;
           if constexpr (KIND == BK_NV2L) {
             // (amax_b / 6) / ts, both quotients correctly rounded (two_level_quot),
             // clamped at 448 (fminf takes
             // 448 for the 0/0 of an all-zero tensor); the divisor of the codes
-            // is s * ts, exact in fp32 (4 + 8 significant bits); a divisor
-            // below 2^-64 and the block's values are both scaled by 2^64
+            // is s * ts, exact in fp32 (4 + 8 significant bits)
             sbyte = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax, ts, rts), 448.0f), 0.f)) & 0xFFu;
-            scl = e4m3_to_f32(sbyte) * ts;
-            if (scl != 0.f && scl < 0x1p-64f) {
-              scl *= 0x1p64f;
-              pre = 0x1p64f;
-            }
+            block_codes_2l(vb, e4m3_to_f32(sbyte) * ts, c0, c1);
           } else {
             // amax * (1/6) in fp32 rounds to the same e4m3 byte as the exact
             // quotient: amax has 8 significant bits, so amax/6 is exact or
             // lies far from every e4m3 rounding boundary
             sbyte = f2_to_e4m3x2(make_float2(amax * (1.0f / 6.0f), 0.f)) & 0xFFu;
-            scl = e4m3_to_f32(sbyte);
+            block_codes(vb, e4m3_to_f32(sbyte), c0, c1);
           }
-          block_codes(vb, scl, pre, c0, c1);
           st_stream_v2(orow + (int64_t)b * 8, c0, c1);
           st_b8(sfrow + (b >> 2) * 512 + (b & 3), sbyte);
         }

@@ -74,16 +74,10 @@ __global__ void __launch_bounds__(kFlatThreads, 1) flat_nv2l_kernel(const LnArgs
     const float amax = block_amax(vb);
     // (amax_b / 6) / ts, each quotient correctly rounded (two_level_quot),
     // clamped at 448 (fminf takes 448 for the 0/0 of an all-zero tensor); the
-    // divisor of the codes is s * ts, exact in fp32; a divisor below 2^-64 and
-    // the values are scaled by 2^64
+    // divisor of the codes is s * ts, exact in fp32
     const uint32_t sbyte = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax, ts, rts), 448.0f), 0.f)) & 0xFFu;
-    float scl = e4m3_to_f32(sbyte) * ts, pre = 1.0f;
-    if (scl != 0.f && scl < 0x1p-64f) {
-      scl *= 0x1p64f;
-      pre = 0x1p64f;
-    }
     uint32_t c0, c1;
-    block_codes(vb, scl, pre, c0, c1);
+    block_codes_2l(vb, e4m3_to_f32(sbyte) * ts, c0, c1);
     st_stream_v2(reinterpret_cast<uint8_t*>(a.out) + row * (D >> 1) + (int64_t)b * 8, c0, c1);
     st_b8(reinterpret_cast<uint8_t*>(a.sf) + ((row >> 7) * ct + (b >> 2)) * 512 + (int)((row & 31) << 4) +
               (int)(((row >> 5) & 3) << 2) + (b & 3),

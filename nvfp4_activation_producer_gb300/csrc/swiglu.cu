@@ -116,28 +116,11 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_kernel(const SwArgs a) {
     } else {
       // (amax_b / 6) / ts, each quotient correctly rounded (two_level_quot),
       // clamped at 448 (fminf takes 448 for the 0/0 of an all-zero tensor); the
-      // divisor of the codes is s * ts, exact in fp32; a divisor below 2^-64
-      // and the values are scaled by 2^64
+      // divisor of the codes is s * ts, exact in fp32
       const uint32_t sbyte = f2_to_e4m3x2(make_float2(fminf(two_level_quot(amax, ts, rts), 448.0f), 0.f)) & 0xFFu;
-      float scl = e4m3_to_f32(sbyte) * ts, pre = 1.0f;
-      if (scl != 0.f && scl < 0x1p-64f) {
-        scl *= 0x1p64f;
-        pre = 0x1p64f;
-      }
-      // v / (s * ts) as v * (r_hi + r_lo), r_lo the Newton correction of
-      // r_hi ~ 1/divisor: exact at every e2m1 midpoint (see ln_rows.cuh)
-      const float rh = (scl == 0.f) ? 0.f : rcp_approx(scl);
-      const float rl = rh * fmaf(-scl, rh, 1.0f);
-      const float2 rh2 = splat2(rh), rl2 = splat2(rl);
-      float2 q[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float2 v = bf16x2_to_f2(vb[i]);
-        if (pre != 1.0f) v = mul2(v, splat2(pre));
-        q[i] = fma2(v, rh2, mul2(v, rl2));
-      }
-      st_stream_v2(a.packed + (int64_t)r * (a.dim >> 1) + (int64_t)b * 8, f8_to_e2m1x8(q[0], q[1], q[2], q[3]),
-                   f8_to_e2m1x8(q[4], q[5], q[6], q[7]));
+      uint32_t c0, c1;
+      block_codes_2l(vb, e4m3_to_f32(sbyte) * ts, c0, c1);
+      st_stream_v2(a.packed + (int64_t)r * (a.dim >> 1) + (int64_t)b * 8, c0, c1);
       st_b8(a.sf + ((int64_t)(r >> 7) * ct + (b >> 2)) * 512 + (int)((r & 31) << 4) + (int)(((r >> 5) & 3) << 2) +
                 (b & 3),
             sbyte);

@@ -256,3 +256,42 @@ def test_register_warp_path_from_the_element_threshold(ap, dev, family, monkeypa
         assert torch.equal(a, b)
     ref = oracle.ln_quant_fp8(_u(w.inputs["x"]), 0.025, oracle.MOD_SEG, **_seg_src(w))
     check_fp8(default[0].cpu().numpy(), ref, 0.025, "fp8 segmented above the element threshold")
+
+
+def _kernel_names(fn):
+    """Names of the CUDA kernels that fn() launches (torch profiler), or None."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = {e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA}
+    return names or None
+
+
+# (rows, dim, single read expected): several rows per row group (1300 x 1040,
+# dim / 8 not a multiple of 32), the largest share of rows one CTA takes
+# (128 rows of 32 bytes), the largest tensor at dim 3072 whose rows fit in the
+# SMs' shared memory and the first that does not
+ONCHIP_SHAPES = [(1300, 1040, True), (19456, 16, True), (5320, 3072, True), (5321, 3072, False)]
+
+
+@pytest.mark.parametrize("rows,dim,onchip", ONCHIP_SHAPES)
+@pytest.mark.parametrize("kind", ["none", "bcast", "seg"])
+def test_two_level_single_read_path(ap, dev, family, kind, rows, dim, onchip):
+    if family != "auto":
+        pytest.skip("default dispatch only")
+    if torch.cuda.get_device_properties(dev).multi_processor_count != 152:
+        pytest.skip("the shapes are chosen for 152 SMs")
+    seed = 3 * rows + dim
+    w = synth.segmented(rows, dim, seed) if kind == "seg" else \
+        (synth.nvfp4_broadcast(rows, dim, seed) if kind == "bcast" else synth.nvfp4_ln(rows, dim, seed))
+    gpk, gsf, gts, opk, osf, ots, v = _two_level(ap, dev, kind, w)
+    assert gts == ots, (gts, ots)
+    check_nvfp4(gpk, gsf, opk, osf, rows, dim, v, f"two-level {kind} {rows}x{dim}", ts=ots)
+    if kind == "none":
+        x = w.inputs["x"].to(dev)
+        names = _kernel_names(lambda: ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x))
+        if names is None:
+            pytest.skip("the profiler recorded no CUDA kernels")
+        assert any("nv2l_onchip" in n for n in names) == onchip, sorted(names)
