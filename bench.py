@@ -154,13 +154,15 @@ def alg_bytes(name: str, w) -> int:
         sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
         return 2 * 4 * R * D + R * D // 2 + sf + 4
     if name in ("nvfp4_2level_seg_h3", "nvfp4_2level_layer_norm"):
-        # two passes over the input (no block can be encoded before the whole
-        # tensor's maximum is known), then codes, scales and the tensor scale
+        # the input once per pass (no block can be encoded before the whole
+        # tensor's maximum is known: two passes, or one where the library
+        # stages the whole tensor in shared memory), then codes, scales and
+        # the tensor scale
         sf = ((R + 127) // 128 * 128) * ((D // 16 + 3) // 4 * 4)
         src = 0
         if name == "nvfp4_2level_seg_h3":
             src = 4 * R + 4 * w.inputs["seg_scale"].shape[0] * D
-        return 2 * (2 * R * D + src) + R * D // 2 + sf + 4
+        return two_level_passes(name, w) * (2 * R * D + src) + R * D // 2 + sf + 4
     if name == "fp8_layer_norm":
         return 2 * R * D + R * D + 4
     if name == "fp8_per_token":
@@ -176,11 +178,29 @@ def alg_bytes(name: str, w) -> int:
     raise KeyError(name)
 
 
-def launches_per_call(name: str) -> int:
+def two_level_passes(name: str, w) -> int:
+    """Passes over the input of a two-level LayerNorm producer on the current
+    device: 1 where the library reads the tensor once (its rows fit in the SMs'
+    shared memory), else 2 (also without a CUDA device)."""
+    if not torch.cuda.is_available():
+        return 2
+    mod = "segmented" if op_kind(name) == "nvfp4_2level_seg_h3" else "none"
+    try:
+        import nvfp4_activation_producer_gb300 as ap
+        return 1 if ap.two_level_single_read(w.rows, w.dim, mod) else 2
+    except (OSError, RuntimeError):
+        return 2
+
+
+def launches_per_call(name: str, w=None) -> int:
     """Kernels one call of the producer launches: the two-level producers (the
-    LayerNorm forms and SwiGLU) clear their word, then run the maximum and the
-    quantising pass."""
-    return 3 if op_kind(name).startswith("nvfp4_2level") else 1
+    LayerNorm forms and SwiGLU) clear their words, then run the maximum and the
+    quantising pass, or one cooperative kernel where a LayerNorm form reads the
+    tensor once."""
+    kind = op_kind(name)
+    if kind in ("nvfp4_2level_seg_h3", "nvfp4_2level_layer_norm") and w is not None:
+        return 1 + two_level_passes(name, w)
+    return 3 if kind.startswith("nvfp4_2level") else 1
 
 
 class DeviceOp:
@@ -592,8 +612,8 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = elapsed_ms / steps
     value = job_gbs(step_bytes, world, ms_per_step)
     args.steps = steps
-    launches = sum(launches_per_call(o.name) for o in ops) * steps + \
-        sum(launches_per_call(o.name) * n * args.op_replays for o, _, n, _, _ in per_op_graphs)
+    launches = sum(launches_per_call(o.name, o.w) for o in ops) * steps + \
+        sum(launches_per_call(o.name, o.w) * n * args.op_replays for o, _, n, _, _ in per_op_graphs)
     del per_op_graphs, copy_graphs
 
     peaks = measured_peaks()
@@ -641,7 +661,7 @@ def run_ours(args, rank, world, local_rank):
                          "of any producer", "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": roofline, "per_op": per_op, "e2e": e2e, "chain": chain,
         "step_repeat": step_repeat,
-        "gpu_launches": launches + rep_n * M * sum(launches_per_call(o.name) for o in ops),
+        "gpu_launches": launches + rep_n * M * sum(launches_per_call(o.name, o.w) for o in ops),
         "clocks": clocks.summary(),
         "timing": ("step: exactly %d steps timed, %d replay(s) of a CUDA graph of %d steps (%.2f ms of GPU time); "
                    "step_repeat: the same graph replayed %d times (%d steps) right after, a longer look at the same "

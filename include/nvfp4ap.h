@@ -96,6 +96,16 @@ enum nvfp4ap_status {
  * rows < 0 or a size past INT64_MAX. */
 int64_t nvfp4ap_2level_workspace_bytes(int64_t rows);
 
+/* Whether the two-level LayerNorm producers, for a (rows, dim) tensor on the
+ * current device, read it from HBM once (*single_read = 1: one cooperative
+ * launch, its rows staged in shared memory) or twice (0: the maximum pass,
+ * then the quantising pass), with the default kernel choice.  modulation: 0
+ * none, 1 broadcast, 2 segmented.  Status: NVFP4AP_ERR_NULL (single_read),
+ * _SHAPE, _DIM, _VALUE (modulation), _LAUNCH (no CUDA device); *single_read
+ * is 0 whenever the status is not NVFP4AP_OK, for rows = 0, and when
+ * NVFP4AP_KERNEL forces a kernel family.  Host-only: launches nothing. */
+int nvfp4ap_2level_single_read(int64_t rows, int64_t dim, int modulation, int* single_read);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvfp4ap_status_string(int status);
 

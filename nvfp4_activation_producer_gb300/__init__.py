@@ -171,6 +171,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.nvfp4ap_wait_limit.argtypes = []
     L.nvfp4ap_noalloc_progress.restype = i32
     L.nvfp4ap_noalloc_progress.argtypes = [p, i64, ctypes.POINTER(ctypes.c_int64)]
+    L.nvfp4ap_2level_single_read.restype = i32
+    L.nvfp4ap_2level_single_read.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_int)]
     for name in ("ada_layer_norm_quant_fp8_bf16", "ada_layer_norm_quant_fp8_ptok_bf16"):
         fn = getattr(L, name)
         fn.restype = i32
@@ -242,6 +244,22 @@ def noalloc_progress():
     words = (ctypes.c_uint32 * max(n, 1))()
     _raise("nvfp4ap_noalloc_progress", L.nvfp4ap_noalloc_progress(words, n, ctypes.byref(used)))
     return [int(w) for w in words[:n]]
+
+
+_MODULATION = {"none": 0, "broadcast": 1, "segmented": 2}
+
+
+def two_level_single_read(rows: int, dim: int, modulation: str = "none") -> bool:
+    """Whether the two-level LayerNorm producers read a (rows, dim) tensor from
+    HBM once on the current device (one cooperative launch) rather than twice,
+    with the default kernel choice; modulation: "none", "broadcast" or
+    "segmented"."""
+    if modulation not in _MODULATION:
+        raise ValueError(f"modulation must be one of {sorted(_MODULATION)}")
+    flag = ctypes.c_int(0)
+    _raise("nvfp4ap_2level_single_read",
+           _load().nvfp4ap_2level_single_read(int(rows), int(dim), _MODULATION[modulation], ctypes.byref(flag)))
+    return bool(flag.value)
 
 
 def library_path() -> str:

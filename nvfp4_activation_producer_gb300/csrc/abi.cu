@@ -763,6 +763,20 @@ NVFP4AP_EXPORT int64_t nvfp4ap_2level_workspace_bytes(int64_t rows) {
   return NVFP4AP_2LEVEL_WORKSPACE_BYTES(rows);
 }
 
+NVFP4AP_EXPORT int nvfp4ap_2level_single_read(int64_t rows, int64_t dim, int modulation, int* single_read) {
+  if (!single_read) return NVFP4AP_ERR_NULL;
+  *single_read = 0;
+  if (rows < 0 || dim <= 0) return NVFP4AP_ERR_SHAPE;
+  if (dim > NVFP4AP_MAX_DIM || dim % 16 != 0) return NVFP4AP_ERR_DIM;
+  const int mod = modulation == 0 ? MOD_NONE : modulation == 1 ? MOD_BCAST : modulation == 2 ? MOD_SEG : -1;
+  if (mod < 0) return NVFP4AP_ERR_VALUE;
+  if (rows == 0 || forced().family != FAM_AUTO) return NVFP4AP_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4AP_ERR_LAUNCH;
+  *single_read = ln_2level_onchip_fits(mod, rows, dim, sms) ? 1 : 0;
+  return NVFP4AP_OK;
+}
+
 NVFP4AP_EXPORT int64_t swizzled_sf_size(int64_t rows, int64_t dim) {
   if (rows < 0 || dim <= 0 || dim % 16 != 0) return -1;
   const int64_t rows_pad = (rows + 127) / 128 * 128;

@@ -162,4 +162,9 @@ int nvfp4ap_noalloc_progress(uint32_t* words, int64_t n, int64_t* used) {
   if (used) *used = 0;
   return 0;
 }
+int nvfp4ap_2level_single_read(int64_t rows, int64_t dim, int modulation, int* single_read) {
+  (void)rows; (void)dim; (void)modulation;
+  if (single_read) *single_read = 0;
+  return 0;
+}
 int64_t swizzled_sf_size(int64_t rows, int64_t dim) { return (rows + 127) / 128 * 128 * ((dim / 16 + 3) / 4 * 4); }

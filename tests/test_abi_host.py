@@ -39,7 +39,7 @@ def test_exports_match_header(lib):
     exported = sorted(l.split()[-1] for l in out.splitlines() if re.search(r" T ", l))
     declared = declared_functions()
     assert declared == exported, (declared, exported)
-    assert len(declared) == 26
+    assert len(declared) == 27
 
 
 def test_status_strings_and_version(lib):
@@ -54,6 +54,21 @@ def test_status_strings_and_version(lib):
     assert b"wait ran out" in L.nvfp4ap_status_string(ap.ERR_TIMEOUT)
     assert b"segment index" in L.nvfp4ap_status_string(ap.ERR_FAULT)
     assert L.nvfp4ap_version() >= 100
+
+
+def test_two_level_single_read_query_arguments(lib):
+    # argument errors come before any device query; *single_read stays 0
+    L, _ = lib
+    flag = ctypes.c_int(7)
+    assert L.nvfp4ap_2level_single_read(10, 3072, 0, None) == 1              # NVFP4AP_ERR_NULL
+    assert L.nvfp4ap_2level_single_read(-1, 3072, 0, ctypes.byref(flag)) == 2 and flag.value == 0
+    flag.value = 7
+    assert L.nvfp4ap_2level_single_read(10, 0, 0, ctypes.byref(flag)) == 2 and flag.value == 0
+    assert L.nvfp4ap_2level_single_read(10, 40, 0, ctypes.byref(flag)) == 3    # dim % 16
+    assert L.nvfp4ap_2level_single_read(10, 65536, 0, ctypes.byref(flag)) == 3
+    assert L.nvfp4ap_2level_single_read(10, 3072, 3, ctypes.byref(flag)) == 8  # modulation
+    flag.value = 7
+    assert L.nvfp4ap_2level_single_read(0, 3072, 1, ctypes.byref(flag)) == 0 and flag.value == 0
 
 
 def test_wait_limit_setting(lib):

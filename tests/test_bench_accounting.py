@@ -65,3 +65,19 @@ def test_shape_suffixed_lines_count_as_their_producer():
     assert bench.page_context("fp8_broadcast_16x2048", 16, 2048)["us"] == 4.117
     assert bench.page_context("fp8_layer_norm", 4096, 3072)["us"] == 16.412
     assert bench.page_context("nvfp4_broadcast", 5070, 3072) is None
+
+
+@pytest.mark.parametrize("passes", [1, 2])
+def test_two_level_layer_norm_bytes_follow_the_passes(monkeypatch, passes):
+    # the input is counted once per pass the library makes over it
+    monkeypatch.setattr(bench, "two_level_passes", lambda name, w: passes)
+    R, D = 5070, 3072
+    assert bench.alg_bytes("nvfp4_2level_layer_norm", _w(R, D)) == passes * 2 * R * D + R * D // 2 + _sf(R, D) + 4
+    assert bench.launches_per_call("nvfp4_2level_layer_norm", _w(R, D)) == 1 + passes
+
+
+def test_two_level_passes_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device answers the query")
+    assert bench.two_level_passes("nvfp4_2level_layer_norm", _w(5070, 3072)) == 2

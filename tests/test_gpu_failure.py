@@ -1,21 +1,21 @@
 """GPU failure path of the bounded waits (no GPU fault is involved).
 
 The kernels that stage rows through shared memory with bulk copies (the
-table form's default kernel, and the allocation-free producer's ring kernel)
-bound every wait on a copy.  nvfp4ap_set_wait_limit shrinks that bound to a
-few SM clock cycles, so the first wait of each CTA gives up before its copy
-lands: the kernel must then wait for every copy it has in flight (with the
-default bound), stop, and report through nvfp4ap_take_device_fault
-(NVFP4AP_ERR_TIMEOUT) -- the call itself returns normally.  A normal call
-right after (default bound restored) must match the oracle within the parity
-tolerance of tests/parity.py.
+table form's default kernel, the allocation-free producer's ring kernel and
+the single-read two-level NVFP4 kernel) bound every wait on a copy.
+nvfp4ap_set_wait_limit shrinks that bound to a few SM clock cycles, so the
+first wait of each CTA gives up before its copy lands: the kernel must then
+wait for every copy it has in flight (with the default bound), stop, and
+report through nvfp4ap_take_device_fault (NVFP4AP_ERR_TIMEOUT) -- the call
+itself returns normally.  A normal call right after (default bound restored)
+must match the oracle within the parity tolerance of tests/parity.py.
 """
 import pytest
 import torch
 
 import oracle
 import synth
-from parity import check_fp8
+from parity import check_fp8, check_nvfp4
 
 pytestmark = pytest.mark.gpu
 
@@ -91,3 +91,26 @@ def test_noalloc_wait_runs_out_then_recovers(tiny_wait, dev):
     u = {k: synth.u16(w.inputs[k]) for k in ("x", "scale", "shift")}
     ref = oracle.ln_quant_fp8(u["x"], _act(w), oracle.MOD_BCAST, scale=u["scale"], shift=u["shift"])
     check_fp8(out.cpu().numpy(), ref, _act(w), "noalloc after a timeout")
+
+
+def test_two_level_single_read_wait_runs_out_then_recovers(tiny_wait, dev):
+    # 2048 x 3072 fits the single-read kernel (14 rows per SM); a CTA whose row
+    # wait gives up still arrives at the grid barrier, so the others do not wait
+    ap = tiny_wait
+    rows, dim = 2048, 3072
+    w = synth.nvfp4_ln(rows, dim, seed=4244)
+    x = w.inputs["x"].to(dev)
+    ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x)
+    torch.cuda.synchronize()
+    with pytest.raises(ap.NvFp4ApError) as e:
+        ap.take_device_fault()
+    assert e.value.status == ap.ERR_TIMEOUT
+    ap.set_wait_limit(0)
+    pk, sf, ts = ap.layer_norm_no_affine_quant_nvfp4_2level_bf16(x)
+    torch.cuda.synchronize()
+    ap.take_device_fault()
+    u = synth.u16(w.inputs["x"])
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(u)
+    assert float(ts.cpu()[0]) == ots
+    v = torch.from_numpy(oracle.staged(u, oracle.MOD_NONE).view("int16")).view(torch.bfloat16).double().numpy()
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, v, "two-level after a timeout", ts=ots)
