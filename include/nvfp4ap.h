@@ -103,7 +103,9 @@ int64_t nvfp4ap_2level_workspace_bytes(int64_t rows);
  * none, 1 broadcast, 2 segmented.  Status: NVFP4AP_ERR_NULL (single_read),
  * _SHAPE, _DIM, _VALUE (modulation), _LAUNCH (no CUDA device); *single_read
  * is 0 whenever the status is not NVFP4AP_OK, for rows = 0, and when
- * NVFP4AP_KERNEL forces a kernel family.  Host-only: launches nothing. */
+ * NVFP4AP_KERNEL forces a kernel family.  A device that refuses the
+ * cooperative launch at run time still gets the two passes.  Host-only:
+ * launches nothing. */
 int nvfp4ap_2level_single_read(int64_t rows, int64_t dim, int modulation, int* single_read);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -329,8 +331,9 @@ int ada_layer_norm_quant_nvfp4_swizzled_seg_bf16(const void* x, const int32_t* s
  * written past its end.  Kernels on `stream`: a clear of the workspace words,
  * then -- when every SM's share of the rows fits in its shared memory -- one
  * cooperative launch that reads the tensor once (statistics and maximum, a
- * grid-wide barrier, then the codes), else the maximum pass and the
- * quantising pass (graph-capturable either way). */
+ * grid-wide barrier, then the codes), else (or when the device refuses that
+ * launch) the maximum pass and the quantising pass (graph-capturable either
+ * way). */
 int layer_norm_no_affine_quant_nvfp4_2level_bf16(const void* x, float eps, void* packed, void* sf_swizzled,
                                                  float* tensor_scale, void* workspace, int64_t rows, int64_t dim,
                                                  nvfp4ap_stream_t stream);

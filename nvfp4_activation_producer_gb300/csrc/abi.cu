@@ -338,8 +338,12 @@ int run_2level(LnArgs& a, int mod, cudaStream_t st) {
   // fit in the SMs' shared memory
   if (f.family == FAM_AUTO) {
     const int sms = sm_count();
-    if (ln_2level_onchip_fits(mod, a.rows, a.dim, sms))
-      return finish(launch_ln_2level_onchip(a, mod, sms, wait_limit_cycles(), st));
+    if (ln_2level_onchip_fits(mod, a.rows, a.dim, sms)) {
+      // a cooperative launch the device refuses (fewer SMs available to this
+      // context than it has, say) leaves nothing running: take the two passes
+      if (launch_ln_2level_onchip(a, mod, sms, wait_limit_cycles(), st) == cudaSuccess) return NVFP4AP_OK;
+      (void)cudaGetLastError();
+    }
   }
   if (f.family != FAM_ROWS && ln_blk_supported(BLK_2LEVEL, mod, a.dim, a.nseg) && aligned(a.x, 32)) {
     BlkShape bs{};
