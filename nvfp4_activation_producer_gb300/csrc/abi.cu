@@ -236,7 +236,7 @@ int run_fp8(LnArgs& a, int mod, cudaStream_t st) {
     if (fam == FAM_ROWBLK) {
       RbShape rb{};
       if ((mod == MOD_NONE || mod_is_bcast(mod)) && aligned(a.x, 32) && aligned(a.out, 16) &&
-          pick_rowblk(a.dim, 0, &rb))
+          pick_rowblk(a.dim, 0, &rb, mod == MOD_NONE))
         return finish(launch_ln_rowblk(a, false, mod, rb, st));
     }
     if (fam == FAM_BLK && sms > 0 && ln_blk_supported(BLK_FP8, mod, a.dim, 0) && aligned(a.x, 32) &&
@@ -395,7 +395,10 @@ int run_nvfp4(LnArgs& a, int mod, cudaStream_t st) {
   int fam = f.family;
   if (fam == FAM_AUTO || fam == FAM_ROWBLK) {
     RbShape rb{};
-    if (aligned(a.x, 32) && pick_rowblk(a.dim, 0, &rb)) return finish(launch_ln_rowblk(a, true, mod, rb, st));
+    // the broadcast and modfp8 sources take the same shape, so that they
+    // reduce to each other bit for bit
+    if (aligned(a.x, 32) && pick_rowblk(a.dim, 0, &rb, mod == MOD_BCAST || mod == MOD_MODFP8))
+      return finish(launch_ln_rowblk(a, true, mod, rb, st));
     BlkShape bs{};
     fam = (fam == FAM_AUTO && a.rows >= kBlkNvfp4Rows && blk_ok && blk_default_shape(a.dim, false, &bs)) ? FAM_BLK
                                                                                                          : FAM_ROWS;

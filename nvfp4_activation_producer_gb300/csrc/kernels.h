@@ -154,11 +154,12 @@ cudaError_t take_warpreg_seg_fault(unsigned int* fault);
 // threads per row (64..128, a multiple of 32), `bpt` 16-element blocks per
 // thread (2..4), rows exactly tpr * bpt blocks; mod MOD_NONE, MOD_BCAST,
 // MOD_MODFP8 (and MOD_AWQ for FP8); x 32-byte aligned, FP8 out 16-byte
-// aligned.  pick_rowblk: the shape for `dim` (forced_bpt > 0: only that one).
+// aligned.  pick_rowblk: the shape for `dim` (forced_bpt > 0: only that one;
+// two_first: two blocks per lane preferred over three).
 struct RbShape {
   int tpr, bpt;
 };
-bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s);
+bool pick_rowblk(int64_t dim, int forced_bpt, RbShape* s, bool two_first);
 cudaError_t launch_ln_rowblk(const LnArgs& a, bool nvfp4, int mod, RbShape s, cudaStream_t st);
 
 // Element-wise LayerNorm producers (ln_scalar.cu) for pointers that are only
