@@ -151,3 +151,18 @@ def test_swiglu_two_level_graph_and_workspace_reuse(ap, dev):
         gr.replay()
     st.synchronize()
     assert torch.equal(pk, a[0]) and torch.equal(sf, a[1]) and torch.equal(ts, a[2])
+
+
+@pytest.mark.parametrize("rows,dim", [(129, 80), (300, 3072)])
+def test_swiglu_two_level_tiny_tensor(ap, dev, rows, dim):
+    # gate and up of order 2^-40: v = bf16(bf16(silu(g)) * u) near 2^-81, the
+    # tensor scale near 2^-92 and every code divisor s * ts below 2^-64 (the
+    # rescaled code path)
+    g = synth.bf16(synth.normal(rows + dim, 0, (rows, dim), 2.0 ** -40))
+    u = synth.bf16(synth.normal(rows + dim, 1, (rows, dim), 2.0 ** -40))
+    pk, sf, ts = ap.swiglu_quant_nvfp4_2level_bf16(g.to(dev), u.to(dev))
+    opk, osf, ots = oracle.swiglu_quant_nvfp4_2level(_bits(g), _bits(u))
+    assert 0.0 < ots < 2.0 ** -80
+    assert float(ts.cpu()[0]) == ots
+    v = torch.from_numpy(oracle.swiglu_values(_bits(g), _bits(u)).view(np.int16)).view(torch.bfloat16).double()
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, v.numpy(), "swiglu two-level tiny", ts=ots)

@@ -295,3 +295,24 @@ def test_two_level_single_read_path(ap, dev, family, kind, rows, dim, onchip):
         if names is None:
             pytest.skip("the profiler recorded no CUDA kernels")
         assert any("nv2l_onchip" in n for n in names) == onchip, sorted(names)
+
+
+@pytest.mark.parametrize("rows,dim", [(300, 3072), (20000, 64)])
+@pytest.mark.parametrize("e", [-60, -110])
+def test_two_level_tiny_tensor(ap, dev, rows, dim, e):
+    # scale = -1 makes 1 + scale = 0, so v = bf16(shift) exactly; shifts of
+    # order 2^e put the tensor scale near the bottom of the fp32 range and the
+    # code divisors s * ts below 2^-64 (the rescaled code path; at 2^-60 both
+    # sides of that bound occur in one tensor)
+    rng = np.random.default_rng(17 + rows - e)
+    x = synth.bf16(rng.standard_normal((rows, dim)).astype(np.float32))
+    sc = np.full(dim, -1.0, dtype=np.float32)
+    sh = (rng.standard_normal(dim) * 2.0 ** e).astype(np.float32)
+    scale, shift = synth.bf16(sc), synth.bf16(sh)
+    pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_bf16(x.to(dev), scale.to(dev), shift.to(dev))
+    mod = dict(scale=_u(scale), shift=_u(shift))
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(_u(x), oracle.MOD_BCAST, **mod)
+    assert 0.0 < ots < 2.0 ** (e - 8)
+    assert float(ts.cpu()[0]) == ots
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(_u(x), oracle.MOD_BCAST, **mod),
+                f"two-level tiny 2^{e}", ts=ots)
