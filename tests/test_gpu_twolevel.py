@@ -316,3 +316,34 @@ def test_two_level_tiny_tensor(ap, dev, rows, dim, e):
     assert float(ts.cpu()[0]) == ots
     check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(_u(x), oracle.MOD_BCAST, **mod),
                 f"two-level tiny 2^{e}", ts=ots)
+
+
+@pytest.mark.parametrize("rows,dim", [(300, 3072), (20000, 64)])
+def test_two_level_out_of_range_segment_index(ap, dev, rows, dim):
+    # rows whose segment index is outside [0, nseg) take zero modulation and set
+    # the fault word; the expected output is the oracle's with those rows
+    # pointed at an appended all-zero table row (the tensor maximum couples
+    # every row, so the whole tensor is compared)
+    import nvfp4_activation_producer_gb300 as m
+    ap.take_device_fault()
+    w = synth.segmented(rows, dim, seed=rows + 5)
+    nseg = int(w.inputs["seg_scale"].shape[0])
+    idx = w.inputs["seg_idx"].clone()
+    bad_rows = [5, rows // 2, rows - 1]
+    idx[bad_rows[0]], idx[bad_rows[1]], idx[bad_rows[2]] = nseg, -1, 1 << 20
+    d = {k: v.to(dev) for k, v in w.inputs.items()}
+    pk, sf, ts = ap.ada_layer_norm_quant_nvfp4_2level_seg_bf16(d["x"], idx.to(dev), d["seg_scale"], d["seg_shift"])
+    torch.cuda.synchronize()
+    with pytest.raises(ap.NvFp4ApError) as e:
+        ap.take_device_fault()
+    assert e.value.status == m.ERR_FAULT
+    oidx = idx.numpy().astype(np.int32).copy()
+    oidx[bad_rows] = nseg
+    zero = np.zeros((1, dim), dtype=np.uint16)
+    src = dict(seg_idx=oidx, seg_scale=np.concatenate([_u(w.inputs["seg_scale"]), zero]),
+               seg_shift=np.concatenate([_u(w.inputs["seg_shift"]), zero]))
+    x = _u(w.inputs["x"])
+    opk, osf, ots = oracle.ln_quant_nvfp4_2level(x, oracle.MOD_SEG, **src)
+    assert float(ts.cpu()[0]) == ots
+    check_nvfp4(pk.cpu().numpy(), sf.cpu().numpy(), opk, osf, rows, dim, _v(x, oracle.MOD_SEG, **src),
+                "two-level, out-of-range segment rows", ts=ots)
