@@ -349,13 +349,24 @@ cudaError_t launch_ln_2level_onchip(const LnArgs& a, int mod, int sms, long long
   cfg.blockDim = dim3(kOnchipThreads);
   cfg.dynamicSmemBytes = (size_t)onchip_smem(a.dim, nr);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  // cooperative (every CTA resident: the grid barrier) and, as every launch of
+  // the library, programmatic serialisation (the kernel waits for the previous
+  // grid before it touches memory); without the latter if refused
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   const float inv_d = (float)(1.0 / (double)a.dim);
-  return cudaLaunchKernelEx(&cfg, k, a, inv_d, wait_limit);
+  e = cudaLaunchKernelEx(&cfg, k, a, inv_d, wait_limit);
+  if (e != cudaSuccess && cfg.numAttrs == 2) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k, a, inv_d, wait_limit);
+  }
+  return e;
 }
 
 cudaError_t take_onchip_fault(unsigned int* fault) {
