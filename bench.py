@@ -637,6 +637,10 @@ def run_ours(args, rank, world, local_rank):
                "in_step": i < len(ops)}
         if launch_bound:
             rec["launch_bound"] = True
+        kind = op_kind(o.name)
+        if kind.startswith("nvfp4_2level"):
+            # passes over the input counted in alg_bytes (SwiGLU: always two)
+            rec["input_passes"] = two_level_passes(o.name, o.w) if kind != "nvfp4_2level_swiglu_h3" else 2
         page = page_context(o.name, o.w.rows, o.w.dim)
         if page:
             rec["page"] = page

@@ -248,3 +248,19 @@ def test_noalloc_argument_errors(lib):
     assert f(A + 4, A, A, A, 1e-5, A, 4, 64, NULL) == 5        # x not 16-byte aligned
     assert f(A, A, A, A, 1e-5, NULL, 4, 64, NULL) == 1
     assert f(NULL, NULL, NULL, NULL, 1e-5, NULL, 0, 64, NULL) == 0
+
+
+def test_two_level_single_read_binding(lib):
+    # the binding's checks before any device query; without a device a valid
+    # query reports NVFP4AP_ERR_LAUNCH (on a GPU machine it answers)
+    import torch
+    import nvfp4_activation_producer_gb300 as ap
+    with pytest.raises(ValueError):
+        ap.two_level_single_read(10, 3072, "diagonal")
+    with pytest.raises(ap.NvFp4ApArgumentError):
+        ap.two_level_single_read(10, 40)
+    assert ap.two_level_single_read(0, 3072, "segmented") is False
+    if not torch.cuda.is_available():
+        with pytest.raises(ap.NvFp4ApError) as e:
+            ap.two_level_single_read(5070, 3072)
+        assert e.value.status == ap.ERR_LAUNCH
