@@ -191,21 +191,13 @@ __global__ void __launch_bounds__(kOnchipThreads, 1)
     const float2 A2 = splat2(rstd), B2 = splat2(-m1 * rstd);
     // the statistics' reads of the row are done (warp_sum consumed them)
     // before any lane writes v over it
-    // two blocks per step (b and b + 32): independent work for a warp that
-    // takes the last row alone
     uint16_t* brow = bmax + j * nblk;
-    for (int b = lane; b < nblk; b += 64) {
-      const bool two = b + 32 < nblk;
+    for (int b = lane; b < nblk; b += 32) {
       const int64_t col = (int64_t)b * 16;
       const uint32_t m = bf16x2_absmax(stage_half<MOD>(a, xq + 2 * b + h0, col + h0 * 8, seg, nk, A2, B2),
                                        stage_half<MOD>(a, xq + 2 * b + (h0 ^ 1), col + (h0 ^ 1) * 8, seg, nk, A2, B2));
-      uint32_t m2 = 0u;
-      if (two)
-        m2 = bf16x2_absmax(stage_half<MOD>(a, xq + 2 * b + 64 + h0, col + 512 + h0 * 8, seg, nk, A2, B2),
-                           stage_half<MOD>(a, xq + 2 * b + 64 + (h0 ^ 1), col + 512 + (h0 ^ 1) * 8, seg, nk, A2, B2));
-      wmax2 = bf16x2_absmax(wmax2, bf16x2_absmax(m, m2));
+      wmax2 = bf16x2_absmax(wmax2, m);
       brow[b] = (uint16_t)(__float_as_uint(fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)))) >> 16);
-      if (two) brow[b + 32] = (uint16_t)(__float_as_uint(fmaxf(fabsf(bf16_lo(m2)), fabsf(bf16_hi(m2)))) >> 16);
     }
   }
   float wmax = fmaxf(fabsf(bf16_lo(wmax2)), fabsf(bf16_hi(wmax2)));
