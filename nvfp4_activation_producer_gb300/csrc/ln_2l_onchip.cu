@@ -153,21 +153,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 1)
     const float K = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xq)[0] << 16);
     const float2 nk = splat2(-K);
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-    float2 s1b = make_float2(0.f, 0.f), s2b = make_float2(0.f, 0.f);
-    int q = lane;
-    for (; q + 32 < nq; q += 64) {  // two independent chains
-      const uint4 u = xq[q], v = xq[q + 32];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w}, y[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 d = add2(bf16x2_to_f2(w[i]), nk), e = add2(bf16x2_to_f2(y[i]), nk);
-        s1 = add2(s1, d);
-        s2 = fma2(d, d, s2);
-        s1b = add2(s1b, e);
-        s2b = fma2(e, e, s2b);
-      }
-    }
-    if (q < nq) {
+    for (int q = lane; q < nq; q += 32) {
       const uint4 u = xq[q];
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -177,8 +163,6 @@ __global__ void __launch_bounds__(kOnchipThreads, 1)
         s2 = fma2(d, d, s2);
       }
     }
-    s1 = add2(s1, s1b);
-    s2 = add2(s2, s2b);
     const float m1 = warp_sum(s1.x + s1.y) * inv_d;  // mean - K
     const float var = fmaxf(fmaf(warp_sum(s2.x + s2.y), inv_d, -m1 * m1), 0.f);
     const float rstd = rsqrtf(var + a.eps);
